@@ -1,0 +1,433 @@
+#!/usr/bin/env python
+"""SFI decode-attention benchmark on GB300.
+
+One bench "step" is one whole SFI decode run of the workload (default: the Llama-3-8B-
+shaped layer, batch 4, 32K context, 256 decode steps with boundary-triggered slow steps):
+every hot-path row runs inside it (append, dense attention + evidence, Selector, packing,
+sparse attention, scheduler). The run is issued by the native driver and replayed as one
+CUDA graph. Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Multi-GPU: units never exchange data, so N GPUs run N independent replicas (no collective
+on the data path); value = all tokens / slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SFI decode-attn tokens/s (slow/fast mix) at 32K/128K; % of HBM roofline"
+BYTES_PER_ROW = 512          # one K row + one V row of 128 bf16
+LOGIT_BYTES = 16             # the slow step's fp32 logits (4 heads) written per position
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="llama8b_ctx32k_b4")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the dense-only/fast-only modes and the CPU baseline")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- utilities
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons while it runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *a):
+        time.sleep(0.15)
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def traffic_record(kernel: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on the current
+    kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "sparse_long_context_sfi_gb300", "csrc", "attn.cu")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return rec if rec.get("attn_cu_sha256_16") == h else None
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if n_gpus > 0 else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def bytes_model(wl, slow, sel_rows):
+    """Algorithmic bytes of every step's attention kernel: dense = KV rows + logits; sparse =
+    packed rows + window rows (each 512 B of K+V), plus q/out (small)."""
+    cfg = wl.cfg
+    per_unit_q = cfg.group * 256 + cfg.group * 128 * 2
+    units_per_seq = cfg.n_layers * cfg.n_kv_heads
+    dense, sparse = [], []
+    for t in range(slow.shape[0]):
+        L = wl.len0 + t + 1
+        if slow[t].any():
+            rows = (L * slow[t]).sum() * units_per_seq
+            dense.append(rows * (BYTES_PER_ROW + LOGIT_BYTES) +
+                         slow[t].sum() * units_per_seq * per_unit_q)
+        else:
+            dense.append(0)
+        fast = ~slow[t].astype(bool)
+        if fast.any():
+            n_s = np.minimum(cfg.n_sink, L)
+            win = L - np.maximum(n_s, L - cfg.n_window)
+            rows = ((sel_rows + win) * fast).sum() * units_per_seq
+            sparse.append(rows * BYTES_PER_ROW + fast.sum() * units_per_seq * per_unit_q)
+        else:
+            sparse.append(0)
+    return np.array(dense, float), np.array(sparse, float)
+
+
+# ------------------------------------------------------------------------- reference arm
+
+def run_reference(args, world, rank):
+    """The CPU oracle, as it stands, on the host cores: each step is a bounded sample of the
+    workload (the first decode steps of every unit), extrapolated to the whole run's mix."""
+    if rank != 0:
+        return
+    import oracle
+    from oracle import decode as odecode
+    from synth.configs import WORKLOADS
+    from synth.workload import HostWorkload
+    wl = HostWorkload(WORKLOADS[args.workload])
+    cfg = wl.cfg
+    n_sample = 12
+    prepared = odecode.prepare(wl, n_sample)
+    slow_full = np.stack([oracle.schedule(wl.masks[b], cfg.t_max) for b in range(cfg.batch)], 1)
+    n_slow_full = int(slow_full.any(axis=1).sum())
+    vals = []
+    for i in range(args.warmup + args.steps):
+        r = odecode.run(wl, steps=n_sample, prepared=prepared)
+        sl = r["slow"].any(axis=0)
+        t_slow = r["seconds"][sl].mean()
+        t_fast = r["seconds"][~sl].mean()
+        full = n_slow_full * t_slow + (cfg.steps - n_slow_full) * t_fast
+        if i >= args.warmup:
+            vals.append(cfg.batch * cfg.steps / full)
+    v = float(np.mean(vals))
+    cores = os.cpu_count()
+    sample = (f"first {n_sample} decode steps of all {wl.n_units} units per step "
+              f"({int(slow_full[:n_sample].any(axis=1).sum())} slow), per-step costs extrapolated "
+              f"to the run's {n_slow_full} slow + {cfg.steps - n_slow_full} fast steps")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * cfg.batch * cfg.steps / v, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+# ------------------------------------------------------------------------------- our arm
+
+def cpu_baseline(wl):
+    import oracle
+    from oracle import decode as odecode
+    cfg = wl.cfg
+    n_sample = 12
+    prepared = odecode.prepare(wl, n_sample)
+    r = odecode.run(wl, steps=n_sample, prepared=prepared)
+    slow_full = np.stack([oracle.schedule(wl.masks[b], cfg.t_max) for b in range(cfg.batch)], 1)
+    n_slow = int(slow_full.any(axis=1).sum())
+    sl = r["slow"].any(axis=0)
+    full = n_slow * r["seconds"][sl].mean() + (cfg.steps - n_slow) * r["seconds"][~sl].mean()
+    return {"value": cfg.batch * cfg.steps / full, "unit": "tokens/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"first {n_sample} decode steps of all {wl.n_units} units "
+                      f"({int(sl.sum())} slow), per-step costs extrapolated to the full mix",
+            "seconds": float(r["seconds"].sum())}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from synth import device as sdev
+    from synth.configs import WORKLOADS
+    from synth.workload import HostWorkload
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = HostWorkload(WORKLOADS[args.workload])
+    cfg = wl.cfg
+    st = sdev.make_state(wl, device=dev)
+    ins = sdev.DeviceInputs(wl, cfg.steps, dev)
+    slow = st.schedule(wl.masks)                       # [steps][B]
+    out = torch.empty((cfg.steps, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
+                      dtype=torch.bfloat16, device=dev)
+    len0 = st.seq_len.clone()
+    stream = torch.cuda.Stream(device=dev)
+
+    def capture(plan):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            st.seq_len.copy_(len0)
+            st.run(plan, stream=stream)            # eager warm-up: builds maps, checks args
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            st.seq_len.copy_(len0)
+            st.run(plan, stream=stream)
+        return g
+
+    def time_graph(g, k, w):
+        for _ in range(w):
+            g.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(k):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        return e0.elapsed_time(e1)
+
+    plan = st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, out_fp32=False)
+    g_mix = capture(plan)
+    with torch.cuda.stream(stream):
+        with Clocks(local) as clk:
+            ms = time_graph(g_mix, args.steps, args.warmup)
+    ms = allreduce_max(ms, world)
+    torch.cuda.synchronize()
+    err = int(st.err[0])
+    tokens_per_step = cfg.batch * cfg.steps
+    value = world * tokens_per_step * args.steps / (ms / 1000.0)
+    n_slow_steps = int(slow.any(axis=1).sum())
+    sel_rows = (st.rows.view(cfg.n_layers, cfg.batch, cfg.n_kv_heads).float().mean(dim=(0, 2))
+                .cpu().numpy())
+    launches_per_run = int(sum(1 + (4 if r.any() else 0) + (0 if r.all() else 1) for r in slow))
+
+    # -- live kernel timing: the same run with external event nodes around each attention
+    #    kernel, replayed a few times --------------------------------------------------------
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * cfg.steps)]
+    plan_ev = st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, out_fp32=False, events=events)
+    g_ev = capture(plan_ev)
+    reps = 5
+    d_dense, d_sparse = [], []
+    is_slow = slow.any(axis=1)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g_ev.replay()
+            torch.cuda.synchronize()
+            for t in range(cfg.steps):
+                dt = events[2 * t].elapsed_time(events[2 * t + 1]) * 1e-3
+                (d_dense if is_slow[t] else d_sparse).append((t, dt))
+    bd, bs = bytes_model(wl, slow.astype(bool), sel_rows)
+    peak, peak_kind = measured_peaks()
+
+    def kstats(d, bytes_per):
+        if not d:
+            return None
+        secs = np.array([x[1] for x in d])
+        byt = np.array([bytes_per[x[0]] for x in d])
+        avg = float(secs.mean())
+        gbs = float(byt.mean() / avg / 1e9)
+        return {"launches_per_step": len(d) // reps, "avg_us": avg * 1e6,
+                "bytes_per_launch": float(byt.mean()), "achieved_gbs": gbs,
+                "frac_of_peak": gbs / peak, "total_us_per_step": float(secs.sum() / reps * 1e6)}
+
+    kd, ks = kstats(d_dense, bd), kstats(d_sparse, bs)
+    dom_name, dom = max([("sfi_dense_decode_attn", kd), ("sfi_sparse_decode_attn", ks)],
+                        key=lambda x: -1 if x[1] is None else x[1]["total_us_per_step"])
+    traffic = traffic_record(dom_name)
+    roofline = {"bound": "hbm", "achieved": dom["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                "frac": dom["achieved_gbs"] / peak, "kernel": dom_name,
+                "peak_kind": f"{peak_kind} (hbm_gbs, STREAM-style copy)",
+                "bytes_per_launch": dom["bytes_per_launch"], "avg_launch_us": dom["avg_us"],
+                "traffic": None if traffic is None else traffic["dram_bytes_per_launch"]}
+
+    # -- end to end through the public API with host buffers --------------------------------
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    hq, hk, hv, ho = pin(ins.q), pin(ins.k_new), pin(ins.v_new), pin(out)
+    hq.copy_(ins.q.cpu())
+    hk.copy_(ins.k_new.cpu())
+    hv.copy_(ins.v_new.cpu())
+    h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
+    d2h = ho.numel() * 2
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            if i == args.warmup:
+                torch.cuda.synchronize()
+                barrier(world)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+            ins.q.copy_(hq, non_blocking=True)
+            ins.k_new.copy_(hk, non_blocking=True)
+            ins.v_new.copy_(hv, non_blocking=True)
+            g_mix.replay()
+            ho.copy_(out, non_blocking=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e1.record()
+        torch.cuda.synchronize()
+    ms_e2e = allreduce_max(e0.elapsed_time(e1), world)
+    e2e = {"value": world * tokens_per_step * args.steps / (ms_e2e / 1000.0), "unit": "tokens/s",
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+           "ms_per_step": ms_e2e / args.steps}
+
+    # -- dense-only (full-KV baseline) and fast-only modes -----------------------------------
+    modes = {"sfi_mix": {"tokens_per_s": value, "ms_per_run": ms / args.steps,
+                         "slow_steps": n_slow_steps}}
+    if not args.no_extras:
+        k2 = max(3, args.steps // 4)
+        g_dense = capture(st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, out_fp32=False,
+                                       dense_only=True))
+        with torch.cuda.stream(stream):
+            ms_d = allreduce_max(time_graph(g_dense, k2, 2), world)
+        fast_only = np.zeros_like(slow)
+        fast_only[0] = 1
+        g_fast = capture(st.make_plan(fast_only, ins.q, ins.k_new, ins.v_new, out,
+                                      out_fp32=False))
+        with torch.cuda.stream(stream):
+            ms_f = allreduce_max(time_graph(g_fast, k2, 2), world)
+        modes["dense_only"] = {"tokens_per_s": world * tokens_per_step * k2 / (ms_d / 1000.0),
+                               "ms_per_run": ms_d / k2}
+        modes["fast_only"] = {"tokens_per_s": world * tokens_per_step * k2 / (ms_f / 1000.0),
+                              "ms_per_run": ms_f / k2, "note": "one slow step at t=0"}
+        modes["sfi_vs_dense_speedup"] = modes["sfi_mix"]["tokens_per_s"] / modes["dense_only"]["tokens_per_s"]
+    torch.cuda.synchronize()
+    err |= int(st.err[0])
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_extras:
+        cpu = cpu_baseline(wl)
+
+    if rank == 0:
+        L0 = int(wl.len0.max())
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded counter-based generator, Zipf(1.1) key-norm boost)",
+            "config": {"workload": cfg.name, "layers": cfg.n_layers, "batch": cfg.batch,
+                       "q_heads": cfg.n_q_heads, "kv_heads": cfg.n_kv_heads,
+                       "head_dim": cfg.head_dim, "context": L0, "decode_steps_per_step": cfg.steps,
+                       "slow_steps_per_step": n_slow_steps,
+                       "budget": f"{cfg.n_sink} sinks + {cfg.n_window} window + {cfg.n_select} selected",
+                       "l2": "inputs larger than L2: every slow step streams the "
+                             f"{st.k.numel() * 4 / 1e6:.0f} MB KV cache; no flush",
+                       "parallelism": "replicas" if world > 1 else "single"},
+            "roofline": roofline,
+            "kernels": {"sfi_dense_decode_attn": kd, "sfi_sparse_decode_attn": ks},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_run * args.steps,
+            "clocks": clk.summary(),
+            "modes": modes,
+            "device_error": err,
+        }
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

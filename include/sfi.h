@@ -1,0 +1,251 @@
+/*
+ * sfi.h -- C ABI of the Slow-Fast Inference (SFI) decode-attention path on sm_103a.
+ *
+ * The path (arXiv 2603.12038, "Slow-Fast Inference: Training-Free Inference Acceleration
+ * via Within-Sentence Support Stability"; sections cited below are from the gist.science
+ * technical summary of that paper unless named otherwise):
+ *   every step   sfi_append_kv            write the new token's K/V row
+ *   slow step    sfi_dense_decode_attn    dense attention + per-position evidence
+ *                sfi_select               evidence + positional prior -> Top-K positions
+ *                sfi_compact              pack sinks + selected rows contiguously
+ *   fast step    sfi_sparse_decode_attn   attention over the packed rows + recent window
+ *   host         sfi_schedule             trigger policy: slow or fast for each step
+ *
+ * Conventions for every call:
+ *   - All tensors are device memory owned by the caller; the library never allocates.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL = legacy
+ *     default stream) and never synchronise, except sfi_read_error.
+ *   - Argument errors are returned synchronously, before anything is launched.
+ *   - A failed launch returns SFI_ERR_CUDA (from cudaGetLastError).
+ *   - Kernels that find bad device-side data (a page-table entry out of range, an append
+ *     past capacity, a bounded wait that gave up) set bits in the caller's device error
+ *     word `err` and skip the bad access; they never trap. Read it with sfi_read_error.
+ *   - The library keeps no state between calls except a per-device table of resolved
+ *     driver entry points; calls sharing one workspace must not overlap on the GPU.
+ *   - Shapes: head_dim must be 128; group = n_q_heads / n_kv_heads must be 1, 2, 4 or 8;
+ *     batch <= 256. Query head h belongs to kv head h / group. A "unit" is one
+ *     (layer, sequence, kv head), numbered u = (layer * batch + b) * n_kv_heads + kv_head.
+ *   - bf16 pointers must be 16-byte aligned.
+ */
+#ifndef SFI_H
+#define SFI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sfi_status {
+    SFI_OK = 0,
+    SFI_ERR_INVALID_ARG = 1,  /* null pointer, inconsistent shape, misaligned pointer     */
+    SFI_ERR_UNSUPPORTED = 2,  /* head_dim != 128, group not in {1,2,4,8}, batch > 256       */
+    SFI_ERR_CAPACITY = 3,     /* a host-known length bound exceeds a buffer's capacity      */
+    SFI_ERR_WORKSPACE = 4,    /* workspace missing, too small or not 256-byte aligned      */
+    SFI_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed               */
+    SFI_ERR_DEVICE = 6        /* sfi_read_error: the device error word is non-zero          */
+} sfi_status;
+
+/* Bits of the device error word. */
+#define SFI_DEVERR_PAGE_RANGE 0x1u /* page-table entry outside [0, n_pages): access skipped  */
+#define SFI_DEVERR_CAPACITY 0x2u   /* append at a position >= capacity: row not written      */
+#define SFI_DEVERR_TIMEOUT 0x4u    /* a bounded pipeline wait gave up: outputs invalid,      */
+                                   /* re-initialise the workspace before further use         */
+#define SFI_DEVERR_LENGTH 0x8u     /* seq_len[b] > max_len: that sequence's work skipped     */
+
+/*
+ * The KV cache of all layers (summary section 3: recent tokens are read straight from the
+ * paged KV cache). Two layouts:
+ *   page_size == 0  contiguous  k, v: bf16 [n_layers][batch][n_kv_heads][capacity][128]
+ *   page_size == 16 paged       k, v: bf16 [n_layers][n_pages][n_kv_heads][16][128];
+ *                               position p of sequence b lives in page
+ *                               page_table[b * max_pages_per_seq + p / 16], row p % 16;
+ *                               capacity = max_pages_per_seq * 16.
+ * seq_len (device int32 [batch]) holds each sequence's current length; sfi_append_kv writes
+ * at seq_len[b] and increments it. max_len is a host-known upper bound of every seq_len
+ * entry during the call (used only to size grids and check capacity). err is a device
+ * uint32 error word, shared by every call that gets this descriptor.
+ */
+typedef struct sfi_kv_cache {
+    int32_t n_layers, batch, n_q_heads, n_kv_heads, head_dim;
+    int32_t capacity;
+    int32_t page_size;
+    int32_t n_pages;
+    int32_t max_pages_per_seq;
+    int32_t max_len;
+    void *k;
+    void *v;
+    const int32_t *page_table;
+    int32_t *seq_len;
+    uint32_t *err;
+} sfi_kv_cache;
+
+/*
+ * Sparse-state budget (summary 2A: sink tokens + sliding recent window + selected memory)
+ * and Selector parameters (summary 2B: fused score s = (1 - lambda) f + lambda r).
+ * prior_tau is the ramp length of the positional prior and must be a power of two.
+ */
+typedef struct sfi_budget {
+    int32_t n_sink;
+    int32_t n_window;
+    int32_t n_select;
+    int32_t prior_tau;
+    double lambda;
+} sfi_budget;
+
+/*
+ * The packed sparse memory (summary section 3: sinks and selected tokens are packed into
+ * one contiguous buffer after every slow step).
+ *   kc, vc   bf16 [n_layers][batch][n_kv_heads][n_sink + n_select][128]
+ *   sel_idx  int32 [n_layers][batch][n_kv_heads][n_select]  ascending positions (sfi_select)
+ *   sel_cnt  int32 [n_layers][batch][n_kv_heads]            valid entries of sel_idx
+ *   rows     int32 [n_layers][batch][n_kv_heads]            packed rows = sinks + sel_cnt
+ *                                                           (written by sfi_compact)
+ */
+typedef struct sfi_sparse_mem {
+    void *kc;
+    void *vc;
+    int32_t *sel_idx;
+    int32_t *sel_cnt;
+    int32_t *rows;
+} sfi_sparse_mem;
+
+/* Human-readable name of a status code (static storage). */
+const char *sfi_status_string(sfi_status s);
+
+/* Library version string (static storage). */
+const char *sfi_version(void);
+
+/*
+ * Bytes of device workspace that sfi_dense_decode_attn and sfi_sparse_decode_attn need
+ * for this cache shape on the current device: split-KV partials, per-unit tickets,
+ * per-unit softmax statistics and the dense step's fp32 logits
+ * ([units][capacity][group]). 0 on invalid arguments.
+ */
+size_t sfi_workspace_bytes(const sfi_kv_cache *kv, const sfi_budget *budget);
+
+/* Zero a workspace (its tickets must start at zero). Call once after allocating it, and
+ * again after a SFI_DEVERR_TIMEOUT. Asynchronous on stream. */
+sfi_status sfi_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Append one token per sequence (implied by every decode step; summary section 1).
+ * k_new, v_new: bf16 [n_layers][batch][n_kv_heads][128]. For each sequence b with
+ * active[b] != 0 (active: device uint8 [batch], NULL = all), writes row seq_len[b] of every
+ * (layer, kv head) and then increments seq_len[b]. Requires max_len + 1 <= capacity.
+ */
+sfi_status sfi_append_kv(const sfi_kv_cache *kv, const void *k_new, const void *v_new,
+                         const uint8_t *active, void *stream);
+
+/*
+ * Slow step: dense decode attention (blog, "How SFI Works": the slow step attends to the
+ * whole KV cache; summary 2A "Slow Steps"). For every unit of an active sequence, each of
+ * its `group` query heads h computes
+ *     z_hj = q_h . k_j / sqrt(128),  p_hj = softmax_j(z_h),  o_h = sum_j p_hj v_j
+ * over j in [0, seq_len[b]). Split-KV: persistent CTAs stream contiguous tile ranges and the
+ * last CTA of a unit merges the partials.
+ *   q        bf16 [n_layers][batch][n_q_heads][128]
+ *   out      [n_layers][batch][n_q_heads][128], fp32 if out_fp32 else bf16
+ *   scores_f optional fp32 [n_layers][batch][n_kv_heads][capacity]: the Selector's evidence
+ *            (summary 2B "Evidenz") f_j = (1/group) sum_h p_hj for j < seq_len[b];
+ *            NULL = dense-only, no emission.
+ *   ws       workspace of at least sfi_workspace_bytes(), 256-byte aligned, initialised.
+ */
+sfi_status sfi_dense_decode_attn(const sfi_kv_cache *kv, const void *q, void *out,
+                                 int32_t out_fp32, float *scores_f, const uint8_t *active,
+                                 void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * The Selector (summary 2B) for every unit of an active sequence of length L = seq_len[b]:
+ * over the candidates j in [n_sink, L - n_window), with d_j = (L - n_window) - j and
+ * n_C candidates,
+ *     rt_j = fl32(min(1, d_j / prior_tau)),  Z = sum_j min(1, d_j / prior_tau)  (closed form)
+ *     s_j  = fl32(fl32(c1 * f_j) + fl32(c2 * rt_j)),  c1 = fl32(1 - lambda), c2 = fl32(lambda/Z)
+ * and keeps the min(n_select, n_C) largest s_j (ties to the lower position), written in
+ * ascending position order to sel_idx with their count in sel_cnt. Radix select, one CTA
+ * per unit. The sinks and the window are part of the sparse state by construction.
+ */
+sfi_status sfi_select(const sfi_kv_cache *kv, const float *scores_f, const sfi_budget *budget,
+                      const sfi_sparse_mem *mem, const uint8_t *active, void *stream);
+
+/*
+ * Pack the sparse memory (summary section 3, memory-coalesced sparse kernel): for every
+ * unit of an active sequence, copies the rows of the sinks [0, min(n_sink, L)) followed by
+ * the selected positions sel_idx[0 .. sel_cnt) from the cache into kc/vc, and writes the
+ * packed row count to mem->rows.
+ */
+sfi_status sfi_compact(const sfi_kv_cache *kv, const sfi_budget *budget,
+                       const sfi_sparse_mem *mem, const uint8_t *active, void *stream);
+
+/*
+ * Fast step (blog, "How SFI Works": attention restricted to the support of the last slow
+ * step; summary 2A "Fast Steps"): attention of each query head over the packed rows
+ * kc/vc[0 .. mem->rows) of its unit plus the recent window [max(n_s, L - n_window), L) read
+ * from the cache, where n_s = mem->rows - sel_cnt (the packed sinks) and L = seq_len[b].
+ * Same q/out layouts and workspace as sfi_dense_decode_attn; no evidence is emitted.
+ */
+sfi_status sfi_sparse_decode_attn(const sfi_kv_cache *kv, const sfi_sparse_mem *mem,
+                                  const sfi_budget *budget, const void *q, void *out,
+                                  int32_t out_fp32, const uint8_t *active, void *ws,
+                                  size_t ws_bytes, void *stream);
+
+/*
+ * Trigger policy (summary 2C), host only: slow[t] = 1 when t == 0, when mask[t - 1] != 0
+ * (the previous token is a boundary token), or when t_max > 0 steps have passed since the
+ * last slow step. mask, slow: host uint8 [steps].
+ */
+sfi_status sfi_schedule(int32_t steps, const uint8_t *mask, int32_t t_max, uint8_t *slow);
+
+/*
+ * A whole decode run on one stream (blog "How SFI Works": the two-speed loop). For each
+ * step t: sfi_append_kv with row t of k_new/v_new; then, for the sequences whose slow flag
+ * is set, sfi_dense_decode_attn (with evidence) -> sfi_select -> sfi_compact, and for the
+ * others sfi_sparse_decode_attn. Nothing is synchronised, so the run can be captured in a
+ * CUDA graph and replayed (the caller restores seq_len before each replay).
+ *   slow      host uint8 [n_steps][batch], e.g. from sfi_schedule per sequence
+ *   q         device bf16 [n_steps][n_layers][batch][n_q_heads][128]
+ *   k_new/v_new device bf16 [n_steps][n_layers][batch][n_kv_heads][128]
+ *   out       device [n_steps or 1][n_layers][batch][n_q_heads][128] (fp32 if out_fp32)
+ *   scores_f  device fp32 [n_layers][batch][n_kv_heads][capacity] (evidence scratch)
+ *   masks     device uint8 [n_steps][2][batch]: per-step (slow, fast) sequence masks, used
+ *             when some step mixes slow and fast sequences; NULL if no step does
+ *   len_start host bound of every seq_len before the first append
+ *   dense_only 1: every step is append + dense attention without evidence (the full-KV
+ *             baseline the pages compare against); slow is ignored
+ *   events    optional host array of 2 * n_steps cudaEvent_t (as void*): events[2t] and
+ *             events[2t+1] are recorded (external, so they survive graph capture) right
+ *             before and after step t's attention kernel; NULL = none
+ */
+typedef struct sfi_decode_plan {
+    int32_t n_steps;
+    const uint8_t *slow;
+    const void *q;
+    const void *k_new;
+    const void *v_new;
+    void *out;
+    int32_t out_fp32;
+    int32_t out_per_step;
+    float *scores_f;
+    const uint8_t *masks;
+    int32_t len_start;
+    int32_t dense_only;
+    void *const *events;
+} sfi_decode_plan;
+
+sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
+                          const sfi_sparse_mem *mem, const sfi_decode_plan *plan, void *ws,
+                          size_t ws_bytes, void *stream);
+
+/* Copy the device error word to *bits (synchronises `stream`). Returns SFI_OK when it is
+ * zero, SFI_ERR_DEVICE when any bit is set. */
+sfi_status sfi_read_error(const sfi_kv_cache *kv, uint32_t *bits, void *stream);
+
+/* Clear the device error word (asynchronous). */
+sfi_status sfi_clear_error(const sfi_kv_cache *kv, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SFI_H */

@@ -9,6 +9,8 @@ mask. Units (layer, sequence, kv head) are independent, so a subset can be simul
 """
 from __future__ import annotations
 
+import time
+
 import numpy as np
 
 import oracle
@@ -21,8 +23,28 @@ def epochs(mask: np.ndarray) -> np.ndarray:
     return e
 
 
+def prepare(wl, steps: int, units=None):
+    """Generate (untimed) the K/V rows every simulated unit will read: prefill + appended."""
+    cfg = wl.cfg
+    units = list(range(wl.n_units)) if units is None else list(units)
+    coords = []
+    for u in units:
+        kvh = u % cfg.n_kv_heads
+        b = (u // cfg.n_kv_heads) % cfg.batch
+        layer = u // (cfg.n_kv_heads * cfg.batch)
+        coords.append((layer, b, kvh))
+    cap = int(max(wl.len0)) + steps
+    kc = np.zeros((len(units), cap, cfg.head_dim), np.uint16)
+    vc = np.zeros((len(units), cap, cfg.head_dim), np.uint16)
+    for i, (layer, b, kvh) in enumerate(coords):
+        n = int(wl.len0[b]) + steps
+        kc[i, :n] = wl.rows("k", layer, b, kvh, np.arange(n))
+        vc[i, :n] = wl.rows("v", layer, b, kvh, np.arange(n))
+    return {"units": units, "coords": coords, "k": kc, "v": vc, "steps": steps}
+
+
 def run(wl, steps: int | None = None, units=None, threads: int = 0, want_f: bool = False,
-        gpu_selection=None):
+        gpu_selection=None, prepared=None):
     """Simulate `steps` decode steps for the given units (default: all).
 
     gpu_selection (optional): {(t, u): ascending positions} to use instead of the oracle's
@@ -31,29 +53,20 @@ def run(wl, steps: int | None = None, units=None, threads: int = 0, want_f: bool
     'sel' {(t, u): positions}, 'f' {(t, u): fp32 evidence} when want_f."""
     cfg = wl.cfg
     steps = cfg.steps if steps is None else steps
-    units = list(range(wl.n_units)) if units is None else list(units)
+    if prepared is None or prepared["steps"] < steps:
+        prepared = prepare(wl, steps, units)
+    units, coords = prepared["units"], prepared["coords"]
+    kc, vc = prepared["k"], prepared["v"]
     G, D = cfg.group, cfg.head_dim
     S, W, K = cfg.n_sink, cfg.n_window, cfg.n_select
-    coords = []
-    for u in units:
-        kvh = u % cfg.n_kv_heads
-        b = (u // cfg.n_kv_heads) % cfg.batch
-        layer = u // (cfg.n_kv_heads * cfg.batch)
-        coords.append((layer, b, kvh))
-    cap = int(max(wl.len0)) + steps
     nU = len(units)
-    kc = np.zeros((nU, cap, D), np.uint16)
-    vc = np.zeros((nU, cap, D), np.uint16)
-    for i, (layer, b, kvh) in enumerate(coords):
-        n = int(wl.len0[b]) + steps
-        kc[i, :n] = wl.rows("k", layer, b, kvh, np.arange(n))
-        vc[i, :n] = wl.rows("v", layer, b, kvh, np.arange(n))
     slow = np.stack([oracle.schedule(wl.masks[b][:steps], cfg.t_max) for b in range(cfg.batch)])
     ep = np.stack([epochs(wl.masks[b][:steps]) for b in range(cfg.batch)])
     L_slow = np.zeros(nU, np.int64)
     sel = [np.zeros(0, np.int32) for _ in range(nU)]
-    res = {"slow": slow, "out": {}, "sel": {}, "f": {}}
+    res = {"slow": slow, "out": {}, "sel": {}, "f": {}, "seconds": np.zeros(steps)}
     for t in range(steps):
+        t0 = time.perf_counter()
         if cfg.drift and t > 0:
             for i, (layer, b, kvh) in enumerate(coords):
                 if ep[b, t] != ep[b, t - 1]:
@@ -92,4 +105,5 @@ def run(wl, steps: int | None = None, units=None, threads: int = 0, want_f: bool
                                        threads=threads)
             out[idx] = o
         res["out"][t] = out
+        res["seconds"][t] = time.perf_counter() - t0
     return res

@@ -1,0 +1,479 @@
+// api.cpp -- the extern "C" entry points declared in include/sfi.h: argument checks,
+// workspace layout, TMA tensor-map encoding and kernel launches. No allocation, no
+// synchronisation (except sfi_read_error), no state beyond the resolved driver entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "sfi.h"
+#include "sfi_internal.h"
+
+using namespace sfi;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 view [rows][128] with 256-byte rows; box = 64 columns x box_rows rows, 128-byte
+// swizzle (the canonical K-major / MN-major operand layout of the UMMA descriptors).
+bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || rows == 0)
+        return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), rows};
+    const cuuint64_t strides[1] = {kHeadDim * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+sfi_status check_kv(const sfi_kv_cache *kv)
+{
+    if (!kv || !kv->k || !kv->v || !kv->seq_len || !kv->err)
+        return SFI_ERR_INVALID_ARG;
+    if (kv->n_layers < 1 || kv->batch < 1 || kv->n_kv_heads < 1 || kv->n_q_heads < 1)
+        return SFI_ERR_INVALID_ARG;
+    if (kv->head_dim != kHeadDim || kv->batch > kMaxBatch)
+        return SFI_ERR_UNSUPPORTED;
+    if (kv->n_q_heads % kv->n_kv_heads != 0)
+        return SFI_ERR_INVALID_ARG;
+    const int g = kv->n_q_heads / kv->n_kv_heads;
+    if (g != 1 && g != 2 && g != 4 && g != 8)
+        return SFI_ERR_UNSUPPORTED;
+    if (!aligned16(kv->k) || !aligned16(kv->v))
+        return SFI_ERR_INVALID_ARG;
+    if (kv->max_len < 0 || kv->capacity < 1)
+        return SFI_ERR_INVALID_ARG;
+    if (kv->page_size != 0) {
+        if (kv->page_size != 16)
+            return SFI_ERR_UNSUPPORTED;
+        if (!kv->page_table || kv->n_pages < 1 || kv->max_pages_per_seq < 1 ||
+            kv->capacity != kv->max_pages_per_seq * kv->page_size)
+            return SFI_ERR_INVALID_ARG;
+    }
+    if (kv->max_len > kv->capacity)
+        return SFI_ERR_CAPACITY;
+    const long long units = 1LL * kv->n_layers * kv->batch * kv->n_kv_heads;
+    const long long rows = kv->page_size ? 1LL * kv->n_layers * kv->n_pages * kv->n_kv_heads * 16
+                                         : units * kv->capacity;
+    if (units > 65535 || rows >= (1LL << 31))
+        return SFI_ERR_UNSUPPORTED;
+    return SFI_OK;
+}
+
+sfi_status check_budget(const sfi_budget *bd)
+{
+    if (!bd || bd->n_sink < 0 || bd->n_window < 1 || bd->n_select < 0 || bd->prior_tau < 1)
+        return SFI_ERR_INVALID_ARG;
+    if ((bd->prior_tau & (bd->prior_tau - 1)) != 0 || !(bd->lambda >= 0.0 && bd->lambda <= 1.0))
+        return SFI_ERR_INVALID_ARG;
+    if (bd->n_sink + bd->n_select < 1)
+        return SFI_ERR_INVALID_ARG;
+    return SFI_OK;
+}
+
+int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+    size_t tickets_dense, tickets_sparse, stats, part_dense, part_sparse, zbuf, total;
+};
+
+WsLayout ws_layout(const sfi_kv_cache *kv, int sms)
+{
+    const size_t units = static_cast<size_t>(kv->n_layers) * kv->batch * kv->n_kv_heads;
+    const int g = kv->n_q_heads / kv->n_kv_heads;
+    const size_t part = static_cast<size_t>(2) * sms * kPartialFloats(g) * sizeof(float);
+    WsLayout w;
+    size_t o = 0;
+    w.tickets_dense = o;  o = align256(o + units * sizeof(int));
+    w.tickets_sparse = o; o = align256(o + units * sizeof(int));
+    w.stats = o;          o = align256(o + units * g * sizeof(float2));
+    w.part_dense = o;     o = align256(o + part);
+    w.part_sparse = o;    o = align256(o + part);
+    w.zbuf = o;           o = align256(o + units * static_cast<size_t>(kv->capacity) * g * sizeof(float));
+    w.total = o;
+    return w;
+}
+
+cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+
+sfi_status launch_status(cudaError_t e) { return e == cudaSuccess ? SFI_OK : SFI_ERR_CUDA; }
+
+void fill_common(AttnParams &p, const sfi_kv_cache *kv, const uint8_t *active)
+{
+    std::memset(&p, 0, sizeof p);
+    p.n_layers = kv->n_layers;
+    p.batch = kv->batch;
+    p.n_kv_heads = kv->n_kv_heads;
+    p.group = kv->n_q_heads / kv->n_kv_heads;
+    p.capacity = kv->capacity;
+    p.page_size = kv->page_size;
+    p.n_pages = kv->n_pages;
+    p.max_pages = kv->max_pages_per_seq;
+    p.max_len = kv->max_len;
+    p.page_table = kv->page_table;
+    p.seq_len = kv->seq_len;
+    p.active = active;
+    p.err = kv->err;
+    p.scale_log2 = static_cast<float>(1.4426950408889634074 / std::sqrt(static_cast<double>(kHeadDim)));
+}
+
+uint64_t cache_rows(const sfi_kv_cache *kv)
+{
+    if (kv->page_size)
+        return static_cast<uint64_t>(kv->n_layers) * kv->n_pages * kv->n_kv_heads * kv->page_size;
+    return static_cast<uint64_t>(kv->n_layers) * kv->batch * kv->n_kv_heads * kv->capacity;
+}
+
+sfi_status dense_impl(const sfi_kv_cache *kv, const void *q, void *out, int32_t out_fp32,
+                      float *scores_f, const uint8_t *active, void *ws, size_t ws_bytes,
+                      void *stream, cudaEvent_t e0, cudaEvent_t e1)
+{
+    sfi_status st = check_kv(kv);
+    if (st != SFI_OK)
+        return st;
+    if (!q || !out || !aligned16(q))
+        return SFI_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    if (sms <= 0)
+        return SFI_ERR_CUDA;
+    const WsLayout w = ws_layout(kv, sms);
+    if (!ws || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return SFI_ERR_WORKSPACE;
+    if (kv->max_len == 0)
+        return SFI_OK;
+    char *base = static_cast<char *>(ws);
+    AttnParams p;
+    fill_common(p, kv, active);
+    p.out = out;
+    p.out_fp32 = out_fp32 ? 1 : 0;
+    p.zbuf = scores_f ? reinterpret_cast<float *>(base + w.zbuf) : nullptr;
+    p.stats = reinterpret_cast<float2 *>(base + w.stats);
+    p.partials = reinterpret_cast<float *>(base + w.part_dense);
+    p.tickets = reinterpret_cast<int *>(base + w.tickets_dense);
+    const int g = p.group;
+    const long long units = 1LL * kv->n_layers * kv->batch * kv->n_kv_heads;
+    CUtensorMap tk, tv, tq;
+    const uint32_t box = kv->page_size ? 16u : static_cast<uint32_t>(kTile);
+    if (!make_map(&tk, kv->k, cache_rows(kv), box) || !make_map(&tv, kv->v, cache_rows(kv), box) ||
+        !make_map(&tq, q, static_cast<uint64_t>(units) * g, static_cast<uint32_t>(g)))
+        return SFI_ERR_CUDA;
+    const long long t_upper = units * ((kv->max_len + kTile - 1) / kTile);
+    const int grid = static_cast<int>(t_upper < sms ? t_upper : sms);
+    if (e0 && cudaEventRecordWithFlags(e0, as_stream(stream), cudaEventRecordExternal) != cudaSuccess)
+        return SFI_ERR_CUDA;
+    cudaError_t e = launch_attention(true, g, tk, tv, tq, tk, tv, p, grid, as_stream(stream));
+    if (e != cudaSuccess)
+        return SFI_ERR_CUDA;
+    if (e1 && cudaEventRecordWithFlags(e1, as_stream(stream), cudaEventRecordExternal) != cudaSuccess)
+        return SFI_ERR_CUDA;
+    if (scores_f) {
+        e = launch_evidence(p.zbuf, p.stats, scores_f, kv->seq_len, active, kv->n_layers,
+                            kv->batch, kv->n_kv_heads, g, kv->capacity, kv->max_len,
+                            as_stream(stream));
+        if (e != cudaSuccess)
+            return SFI_ERR_CUDA;
+    }
+    return SFI_OK;
+}
+
+sfi_status sparse_impl(const sfi_kv_cache *kv, const sfi_sparse_mem *mem,
+                       const sfi_budget *budget, const void *q, void *out, int32_t out_fp32,
+                       const uint8_t *active, void *ws, size_t ws_bytes, void *stream,
+                       cudaEvent_t e0, cudaEvent_t e1)
+{
+    sfi_status st = check_kv(kv);
+    if (st != SFI_OK)
+        return st;
+    if ((st = check_budget(budget)) != SFI_OK)
+        return st;
+    if (!mem || !mem->kc || !mem->vc || !mem->sel_cnt || !mem->rows || !q || !out ||
+        !aligned16(q) || !aligned16(mem->kc) || !aligned16(mem->vc))
+        return SFI_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    if (sms <= 0)
+        return SFI_ERR_CUDA;
+    const WsLayout w = ws_layout(kv, sms);
+    if (!ws || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return SFI_ERR_WORKSPACE;
+    char *base = static_cast<char *>(ws);
+    AttnParams p;
+    fill_common(p, kv, active);
+    p.out = out;
+    p.out_fp32 = out_fp32 ? 1 : 0;
+    p.partials = reinterpret_cast<float *>(base + w.part_sparse);
+    p.tickets = reinterpret_cast<int *>(base + w.tickets_sparse);
+    p.comp_rows = mem->rows;
+    p.sel_cnt = mem->sel_cnt;
+    p.comp_cap = budget->n_sink + budget->n_select;
+    p.n_window = budget->n_window;
+    p.n_cbox = (p.comp_cap + 63) / 64;
+    p.n_wbox = (budget->n_window + 15) / 16 + (kv->page_size ? 1 : 0);
+    p.tiles_per_unit = (64 * p.n_cbox + 16 * p.n_wbox + kTile - 1) / kTile;
+    const int g = p.group;
+    const long long units = 1LL * kv->n_layers * kv->batch * kv->n_kv_heads;
+    CUtensorMap tk, tv, tq, tkc, tvc;
+    if (!make_map(&tk, kv->k, cache_rows(kv), 16u) || !make_map(&tv, kv->v, cache_rows(kv), 16u) ||
+        !make_map(&tq, q, static_cast<uint64_t>(units) * g, static_cast<uint32_t>(g)) ||
+        !make_map(&tkc, mem->kc, static_cast<uint64_t>(units) * p.comp_cap, 64u) ||
+        !make_map(&tvc, mem->vc, static_cast<uint64_t>(units) * p.comp_cap, 64u))
+        return SFI_ERR_CUDA;
+    const long long t_upper = units * p.tiles_per_unit;
+    const int grid = static_cast<int>(t_upper < sms ? t_upper : sms);
+    if (e0 && cudaEventRecordWithFlags(e0, as_stream(stream), cudaEventRecordExternal) != cudaSuccess)
+        return SFI_ERR_CUDA;
+    if (launch_attention(false, g, tk, tv, tq, tkc, tvc, p, grid, as_stream(stream)) != cudaSuccess)
+        return SFI_ERR_CUDA;
+    if (e1 && cudaEventRecordWithFlags(e1, as_stream(stream), cudaEventRecordExternal) != cudaSuccess)
+        return SFI_ERR_CUDA;
+    return SFI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *sfi_status_string(sfi_status s)
+{
+    switch (s) {
+    case SFI_OK: return "ok";
+    case SFI_ERR_INVALID_ARG: return "invalid argument";
+    case SFI_ERR_UNSUPPORTED: return "unsupported shape";
+    case SFI_ERR_CAPACITY: return "length bound exceeds capacity";
+    case SFI_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case SFI_ERR_CUDA: return "CUDA error";
+    case SFI_ERR_DEVICE: return "device error word set";
+    }
+    return "unknown status";
+}
+
+const char *sfi_version(void) { return "sfi-gb300 0.1 (sm_103a, tcgen05/TMA)"; }
+
+size_t sfi_workspace_bytes(const sfi_kv_cache *kv, const sfi_budget *budget)
+{
+    (void)budget;
+    if (check_kv(kv) != SFI_OK)
+        return 0;
+    const int sms = sm_count();
+    if (sms <= 0)
+        return 0;
+    return ws_layout(kv, sms).total;
+}
+
+sfi_status sfi_workspace_init(void *ws, size_t ws_bytes, void *stream)
+{
+    if (!ws || ws_bytes == 0)
+        return SFI_ERR_WORKSPACE;
+    return launch_status(cudaMemsetAsync(ws, 0, ws_bytes, as_stream(stream)));
+}
+
+sfi_status sfi_append_kv(const sfi_kv_cache *kv, const void *k_new, const void *v_new,
+                         const uint8_t *active, void *stream)
+{
+    sfi_status st = check_kv(kv);
+    if (st != SFI_OK)
+        return st;
+    if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
+        return SFI_ERR_INVALID_ARG;
+    if (kv->max_len + 1 > kv->capacity)
+        return SFI_ERR_CAPACITY;
+    return launch_status(launch_append(k_new, v_new, kv->k, kv->v, kv->seq_len, active,
+                                       kv->page_table, kv->n_layers, kv->batch, kv->n_kv_heads,
+                                       kv->capacity, kv->page_size, kv->n_pages,
+                                       kv->max_pages_per_seq, kv->err, as_stream(stream)));
+}
+
+sfi_status sfi_dense_decode_attn(const sfi_kv_cache *kv, const void *q, void *out,
+                                 int32_t out_fp32, float *scores_f, const uint8_t *active,
+                                 void *ws, size_t ws_bytes, void *stream)
+{
+    return dense_impl(kv, q, out, out_fp32, scores_f, active, ws, ws_bytes, stream, nullptr,
+                      nullptr);
+}
+
+sfi_status sfi_select(const sfi_kv_cache *kv, const float *scores_f, const sfi_budget *budget,
+                      const sfi_sparse_mem *mem, const uint8_t *active, void *stream)
+{
+    sfi_status st = check_kv(kv);
+    if (st != SFI_OK)
+        return st;
+    if ((st = check_budget(budget)) != SFI_OK)
+        return st;
+    if (!scores_f || !mem || !mem->sel_idx || !mem->sel_cnt)
+        return SFI_ERR_INVALID_ARG;
+    SelectParams p;
+    p.f = scores_f;
+    p.capacity = kv->capacity;
+    p.batch = kv->batch;
+    p.n_kv_heads = kv->n_kv_heads;
+    p.n_units = kv->n_layers * kv->batch * kv->n_kv_heads;
+    p.seq_len = kv->seq_len;
+    p.active = active;
+    p.n_sink = budget->n_sink;
+    p.n_window = budget->n_window;
+    p.n_select = budget->n_select;
+    p.prior_tau = budget->prior_tau;
+    p.lambda = budget->lambda;
+    p.sel_idx = mem->sel_idx;
+    p.sel_cnt = mem->sel_cnt;
+    return launch_status(launch_select(p, as_stream(stream)));
+}
+
+sfi_status sfi_compact(const sfi_kv_cache *kv, const sfi_budget *budget,
+                       const sfi_sparse_mem *mem, const uint8_t *active, void *stream)
+{
+    sfi_status st = check_kv(kv);
+    if (st != SFI_OK)
+        return st;
+    if ((st = check_budget(budget)) != SFI_OK)
+        return st;
+    if (!mem || !mem->kc || !mem->vc || !mem->sel_idx || !mem->sel_cnt || !mem->rows ||
+        !aligned16(mem->kc) || !aligned16(mem->vc))
+        return SFI_ERR_INVALID_ARG;
+    return launch_status(launch_compact(
+        kv->k, kv->v, mem->kc, mem->vc, mem->sel_idx, mem->sel_cnt, mem->rows, kv->seq_len, active,
+        kv->page_table, kv->n_layers, kv->batch, kv->n_kv_heads, kv->capacity, kv->page_size,
+        kv->n_pages, kv->max_pages_per_seq, budget->n_sink, budget->n_select, kv->err,
+        as_stream(stream)));
+}
+
+sfi_status sfi_sparse_decode_attn(const sfi_kv_cache *kv, const sfi_sparse_mem *mem,
+                                  const sfi_budget *budget, const void *q, void *out,
+                                  int32_t out_fp32, const uint8_t *active, void *ws,
+                                  size_t ws_bytes, void *stream)
+{
+    return sparse_impl(kv, mem, budget, q, out, out_fp32, active, ws, ws_bytes, stream, nullptr,
+                       nullptr);
+}
+
+sfi_status sfi_schedule(int32_t steps, const uint8_t *mask, int32_t t_max, uint8_t *slow)
+{
+    if (steps < 0 || (steps > 0 && (!mask || !slow)))
+        return SFI_ERR_INVALID_ARG;
+    int32_t last = 0;
+    for (int32_t t = 0; t < steps; ++t) {
+        const bool s = t == 0 || mask[t - 1] != 0 || (t_max > 0 && t - last >= t_max);
+        slow[t] = s ? 1 : 0;
+        if (s)
+            last = t;
+    }
+    return SFI_OK;
+}
+
+sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
+                          const sfi_sparse_mem *mem, const sfi_decode_plan *plan, void *ws,
+                          size_t ws_bytes, void *stream)
+{
+    sfi_status st = check_kv(kv);
+    if (st != SFI_OK)
+        return st;
+    if ((st = check_budget(budget)) != SFI_OK)
+        return st;
+    if (!plan || !mem || plan->n_steps < 0 || !plan->slow || !plan->q || !plan->k_new ||
+        !plan->v_new || !plan->out || !plan->scores_f || plan->len_start < 0)
+        return SFI_ERR_INVALID_ARG;
+    if (plan->len_start + plan->n_steps > kv->capacity)
+        return SFI_ERR_CAPACITY;
+    const int B = kv->batch, g = kv->n_q_heads / kv->n_kv_heads;
+    const size_t q_step = static_cast<size_t>(kv->n_layers) * B * kv->n_q_heads * kHeadDim;
+    const size_t kv_step = static_cast<size_t>(kv->n_layers) * B * kv->n_kv_heads * kHeadDim;
+    const size_t o_step = plan->out_per_step ? q_step * (plan->out_fp32 ? 4 : 2) : 0;
+    (void)g;
+    sfi_kv_cache k = *kv;
+    for (int32_t t = 0; t < plan->n_steps; ++t) {
+        const uint8_t *row = plan->slow + static_cast<size_t>(t) * B;
+        int n_slow = 0;
+        for (int b = 0; b < B; ++b)
+            n_slow += row[b] ? 1 : 0;
+        const bool mixed = n_slow != 0 && n_slow != B;
+        if (mixed && !plan->masks && !plan->dense_only)
+            return SFI_ERR_INVALID_ARG;
+        const uint8_t *m_slow = mixed ? plan->masks + static_cast<size_t>(t) * 2 * B : nullptr;
+        const uint8_t *m_fast = mixed ? m_slow + B : nullptr;
+        k.max_len = plan->len_start + t;
+        st = sfi_append_kv(&k, static_cast<const char *>(plan->k_new) + t * kv_step * 2,
+                           static_cast<const char *>(plan->v_new) + t * kv_step * 2, nullptr, stream);
+        if (st != SFI_OK)
+            return st;
+        k.max_len = plan->len_start + t + 1;
+        const void *q = static_cast<const char *>(plan->q) + t * q_step * 2;
+        void *out = static_cast<char *>(plan->out) + t * o_step;
+        cudaEvent_t e0 = plan->events ? static_cast<cudaEvent_t>(plan->events[2 * t]) : nullptr;
+        cudaEvent_t e1 = plan->events ? static_cast<cudaEvent_t>(plan->events[2 * t + 1]) : nullptr;
+        if (plan->dense_only) {
+            if ((st = dense_impl(&k, q, out, plan->out_fp32, nullptr, nullptr, ws, ws_bytes, stream,
+                                 e0, e1)) != SFI_OK)
+                return st;
+            continue;
+        }
+        if (n_slow > 0) {
+            if ((st = dense_impl(&k, q, out, plan->out_fp32, plan->scores_f, m_slow, ws, ws_bytes,
+                                 stream, e0, e1)) != SFI_OK ||
+                (st = sfi_select(&k, plan->scores_f, budget, mem, m_slow, stream)) != SFI_OK ||
+                (st = sfi_compact(&k, budget, mem, m_slow, stream)) != SFI_OK)
+                return st;
+        }
+        if (n_slow < B) {
+            if ((st = sparse_impl(&k, mem, budget, q, out, plan->out_fp32, m_fast, ws, ws_bytes,
+                                  stream, n_slow > 0 ? nullptr : e0, n_slow > 0 ? nullptr : e1)) != SFI_OK)
+                return st;
+        }
+    }
+    return SFI_OK;
+}
+
+sfi_status sfi_read_error(const sfi_kv_cache *kv, uint32_t *bits, void *stream)
+{
+    if (!kv || !kv->err || !bits)
+        return SFI_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    if (cudaMemcpyAsync(bits, kv->err, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return SFI_ERR_CUDA;
+    return *bits ? SFI_ERR_DEVICE : SFI_OK;
+}
+
+sfi_status sfi_clear_error(const sfi_kv_cache *kv, void *stream)
+{
+    if (!kv || !kv->err)
+        return SFI_ERR_INVALID_ARG;
+    return launch_status(cudaMemsetAsync(kv->err, 0, sizeof(uint32_t), as_stream(stream)));
+}
+
+}  // extern "C"

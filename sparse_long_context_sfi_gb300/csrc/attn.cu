@@ -1,0 +1,771 @@
+// attn.cu -- GQA decode attention for the SFI slow step (dense over the whole KV cache,
+// emitting the Selector's evidence) and fast step (packed sparse memory + recent window).
+//
+// Slow step: the blog "How SFI Works" (dense attention over the full cache) and section 2A
+// of the gist.science technical summary ("Slow Steps"). Fast step: the same attention over
+// the sparse state of section 2A (sinks + selected memory + sliding window), read as
+// section 3 describes: packed sink/selected rows streamed contiguously, recent tokens
+// straight from the (possibly paged) cache.
+//
+// Design (one kernel template for both steps):
+//   * Persistent CTAs, one per SM. The tiles of all units (layer, sequence, kv head) are
+//     concatenated; CTA c streams the contiguous tile range [c T / P, (c+1) T / P). Units
+//     cut by a range boundary are merged by the last CTA to finish them (atomic ticket, no
+//     waiting); a unit inside one range is written directly.
+//   * Warp 0 issues TMA loads of 128-row K and V tiles (128-byte swizzle) into a 3-stage
+//     shared-memory ring. Warp 1 issues tcgen05 UMMAs: S^T = K Q^T (M = 128 positions,
+//     N = 16 = query heads padded) and O^T = V^T P^T (M = 128 dims, V read MN-major),
+//     accumulating in TMEM. Warps 2-5 run the online softmax one position per thread
+//     (tcgen05.ld of S^T), write P^T as bf16 and accumulate O^T one dim per thread.
+//   * Every wait is bounded; a wait that gives up flags SFI_DEVERR_TIMEOUT, drains the
+//     CTA's copies and MMAs, frees TMEM and returns.
+#include <math.h>
+
+#include "sfi_device.cuh"
+
+namespace sfi {
+namespace {
+
+constexpr int kChunkBytes = kTile * 128;       // 128 rows x 128 B: one 64-dim half of a tile
+constexpr int kStageBytes = 4 * kChunkBytes;   // K[0:64), K[64:128), V[0:64), V[64:128)
+constexpr int kOpRows = 16;                    // UMMA N: query heads padded to 16 rows
+constexpr int kOpChunk = kOpRows * 128;        // one 64-element K-chunk of Q^T or P^T
+constexpr int kOpBytes = 2 * kOpChunk;
+constexpr uint32_t kTmemCols = 64;             // S^T x2 (cols 0, 16), O^T x2 (cols 32, 48)
+
+constexpr int kQOff = kStages * kStageBytes;
+constexpr int kPOff = kQOff + 2 * kOpBytes;
+constexpr int kCtrlOff = kPOff + 2 * kOpBytes;
+
+constexpr int kFlagFirst = 1;   // first tile of a segment (a unit's tiles inside one CTA)
+constexpr int kFlagLast = 2;    // last tile of a segment
+
+struct TileMeta {
+    int unit;
+    int tile;
+    int flags;
+    int pad;
+    uint32_t valid[4];          // bit r: row r of the tile holds a real position
+};
+
+struct Ctrl {
+    uint64_t full[kStages], empty[kStages];
+    uint64_t s_full[2], s_free[2], p_full[2], o_full[2], o_free[2], q_free[2];
+    uint64_t gsync;             // softmax-group barrier (one arrive per warp)
+    uint64_t drain;             // MMA drain on exit
+    TileMeta meta[kStages];
+    float red_max[2][4][8];
+    float red_sum[4][16];
+    uint32_t tmem_base;
+    int abort;
+    int last_flag;
+    int P;
+    long long T, TL, g0, g1;
+    int nt[kMaxBatch];
+    int pre[kMaxBatch];
+    int len[kMaxBatch];
+};
+
+constexpr int kSmemBytes = kCtrlOff + static_cast<int>(sizeof(Ctrl)) + 1024;
+
+__device__ __forceinline__ float warp_max(float x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Barrier over the four softmax warps through an mbarrier, so it can give up.
+__device__ __forceinline__ bool group_sync(Ctrl &c, uint32_t &phase, int lane)
+{
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive(&c.gsync);
+    const bool ok = mbar_wait(&c.gsync, phase & 1u, &c.abort);
+    ++phase;
+    return ok;
+}
+
+__device__ __forceinline__ void fail(Ctrl &c, uint32_t *err)
+{
+    c.abort = 1;
+    raise_error(err, 0x4u);  // SFI_DEVERR_TIMEOUT
+}
+
+template <int G>
+__device__ __forceinline__ void store_out(const AttnParams &p, int u, int d, const float (&o)[G])
+{
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        const size_t idx = (static_cast<size_t>(u) * G + h) * kHeadDim + d;
+        if (p.out_fp32)
+            static_cast<float *>(p.out)[idx] = o[h];
+        else
+            static_cast<__nv_bfloat16 *>(p.out)[idx] = __float2bfloat16_rn(o[h]);
+    }
+}
+
+template <int G, bool DENSE>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
+                const __grid_constant__ CUtensorMap tm_vc, const AttnParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    Ctrl &c = *reinterpret_cast<Ctrl *>(smem + kCtrlOff);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int B = p.batch, Hkv = p.n_kv_heads;
+
+    // ---- tile space: per-sequence tile counts and this CTA's range --------------------
+    if (tid == 0) {
+        long long acc = 0;
+        for (int b = 0; b < B; ++b) {
+            int L = p.seq_len[b];
+            int act = p.active ? p.active[b] : 1;
+            if (act && (L < 0 || L > p.max_len || L > p.capacity)) {
+                raise_error(p.err, 0x8u);  // SFI_DEVERR_LENGTH
+                act = 0;
+            }
+            int n = 0;
+            if (act && L > 0)
+                n = DENSE ? (L + kTile - 1) / kTile : p.tiles_per_unit;
+            c.nt[b] = n;
+            c.pre[b] = static_cast<int>(acc * Hkv);
+            c.len[b] = L;
+            acc += n;
+        }
+        c.TL = acc * Hkv;
+        c.T = c.TL * p.n_layers;
+        c.P = static_cast<int>(c.T < gridDim.x ? c.T : gridDim.x);
+        c.g0 = static_cast<long long>(blockIdx.x) * c.T / (c.P > 0 ? c.P : 1);
+        c.g1 = static_cast<long long>(blockIdx.x + 1) * c.T / (c.P > 0 ? c.P : 1);
+        c.abort = 0;
+    }
+    __syncthreads();
+    if (static_cast<int>(blockIdx.x) >= c.P)
+        return;
+    const long long g0 = c.g0, g1 = c.g1;
+    const int n_tiles = static_cast<int>(g1 - g0);
+
+    // ---- set-up ----------------------------------------------------------------------
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&c.full[s], 1);
+            mbar_init(&c.empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&c.s_full[b], 1);
+            mbar_init(&c.s_free[b], 4);
+            mbar_init(&c.p_full[b], 4);
+            mbar_init(&c.o_full[b], 1);
+            mbar_init(&c.o_free[b], 4);
+            mbar_init(&c.q_free[b], 1);
+        }
+        mbar_init(&c.gsync, 4);
+        mbar_init(&c.drain, 1);
+        mbar_fence_init();
+        tma_prefetch_map(&tm_k);
+        tma_prefetch_map(&tm_v);
+        tma_prefetch_map(&tm_q);
+        if (!DENSE) {
+            tma_prefetch_map(&tm_kc);
+            tma_prefetch_map(&tm_vc);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(&c.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    // Q^T and P^T operands: rows >= G stay zero for the whole kernel.
+    for (int i = tid; i < 4 * kOpBytes / 16; i += kAttnThreads)
+        reinterpret_cast<uint4 *>(smem + kQOff)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = c.tmem_base;
+
+    if (warp == 0) {
+        // =============================== TMA producer ===================================
+        if (lane == 0 && n_tiles > 0) {
+            const uint64_t pol = policy_evict_first();
+            // decode the first tile of the range
+            long long g = g0;
+            int layer = static_cast<int>(g / c.TL);
+            int r = static_cast<int>(g - static_cast<long long>(layer) * c.TL);
+            int b = 0;
+            while (b + 1 < B && (c.nt[b] == 0 || c.pre[b] + Hkv * c.nt[b] <= r))
+                ++b;
+            int kvh = (r - c.pre[b]) / c.nt[b];
+            int t = (r - c.pre[b]) - kvh * c.nt[b];
+            int seg = -1, issued = 0;
+            for (int i = 0; i < n_tiles; ++i, ++g) {
+                if (i > 0 && ++t == c.nt[b]) {
+                    t = 0;
+                    if (++kvh == Hkv) {
+                        kvh = 0;
+                        do {
+                            if (++b == B) {
+                                b = 0;
+                                ++layer;
+                            }
+                        } while (c.nt[b] == 0);
+                    }
+                }
+                const int s = i % kStages;
+                if (!mbar_wait(&c.empty[s], ((i / kStages) & 1) ^ 1, &c.abort)) {
+                    fail(c, p.err);
+                    break;
+                }
+                const int u = (layer * B + b) * Hkv + kvh;
+                const bool first = (i == 0) || (t == 0);
+                const bool last = (i == n_tiles - 1) || (t == c.nt[b] - 1);
+                if (first) {
+                    ++seg;
+                    if (seg >= 2 && !mbar_wait(&c.q_free[seg & 1], ((seg >> 1) - 1) & 1, &c.abort)) {
+                        fail(c, p.err);
+                        break;
+                    }
+                }
+                uint8_t *st = smem + s * kStageBytes;
+                TileMeta &mt = c.meta[s];
+                mt.unit = u;
+                mt.tile = t;
+                mt.flags = (first ? kFlagFirst : 0) | (last ? kFlagLast : 0);
+                uint32_t valid[4] = {0u, 0u, 0u, 0u};
+                uint32_t bytes = first ? 2u * G * 128u : 0u;
+                const int L = c.len[b];
+                // Box plan for this tile: up to 8 boxes of 16 rows, or fewer larger boxes.
+                struct Box { const CUtensorMap *mk, *mv; int y; int row0; int rows; };
+                Box box[8];
+                int nbox = 0;
+                if (DENSE) {
+                    const int pos0 = t * kTile;
+                    const int nvalid = min(kTile, L - pos0);
+                    for (int rr = 0; rr < nvalid; ++rr)
+                        valid[rr >> 5] |= 1u << (rr & 31);
+                    if (p.page_size == 0) {
+                        box[nbox++] = {&tm_k, &tm_v, u * p.capacity + pos0, 0, kTile};
+                    } else {
+                        for (int q = 0; q * 16 < nvalid; ++q) {
+                            const int lp = (pos0 >> 4) + q;
+                            const int page = p.page_table[b * p.max_pages + lp];
+                            if (page < 0 || page >= p.n_pages) {
+                                raise_error(p.err, 0x1u);
+                                for (int rr = 16 * q; rr < 16 * q + 16; ++rr)
+                                    valid[rr >> 5] &= ~(1u << (rr & 31));
+                                continue;
+                            }
+                            box[nbox++] = {&tm_k, &tm_v,
+                                           ((layer * p.n_pages + page) * Hkv + kvh) * 16, 16 * q, 16};
+                        }
+                    }
+                } else {
+                    const int rows_c = max(0, min(p.comp_rows[u], p.comp_cap));
+                    const int n_s = max(0, rows_c - max(0, p.sel_cnt[u]));
+                    const int ws = max(n_s, L - p.n_window);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int R = t * kTile + 64 * h2;
+                        if (R < 64 * p.n_cbox) {
+                            const int k = R >> 6;
+                            const int vr = max(0, min(64, rows_c - 64 * k));
+                            if (vr > 0) {
+                                box[nbox++] = {&tm_kc, &tm_vc, u * p.comp_cap + 64 * k, 64 * h2, 64};
+                                for (int rr = 0; rr < vr; ++rr)
+                                    valid[(64 * h2 + rr) >> 5] |= 1u << ((64 * h2 + rr) & 31);
+                            }
+                            continue;
+                        }
+                        for (int q = 0; q < 4; ++q) {
+                            const int j = (R + 16 * q - 64 * p.n_cbox) >> 4;
+                            if (j >= p.n_wbox)
+                                break;
+                            const int row0 = 64 * h2 + 16 * q;
+                            if (p.page_size == 0) {
+                                const int p0 = ws + 16 * j;
+                                const int vr = max(0, min(16, L - p0));
+                                if (vr == 0)
+                                    continue;
+                                box[nbox++] = {&tm_k, &tm_v, u * p.capacity + p0, row0, 16};
+                                for (int rr = 0; rr < vr; ++rr)
+                                    valid[(row0 + rr) >> 5] |= 1u << ((row0 + rr) & 31);
+                            } else {
+                                const int lp = (ws >> 4) + j;
+                                const int p0 = lp * 16;
+                                uint32_t m = 0;
+                                for (int rr = 0; rr < 16; ++rr)
+                                    if (p0 + rr >= ws && p0 + rr < L)
+                                        m |= 1u << rr;
+                                if (m == 0)
+                                    continue;
+                                const int page = p.page_table[b * p.max_pages + lp];
+                                if (page < 0 || page >= p.n_pages) {
+                                    raise_error(p.err, 0x1u);
+                                    continue;
+                                }
+                                box[nbox++] = {&tm_k, &tm_v,
+                                               ((layer * p.n_pages + page) * Hkv + kvh) * 16, row0, 16};
+                                for (int rr = 0; rr < 16; ++rr)
+                                    if (m & (1u << rr))
+                                        valid[(row0 + rr) >> 5] |= 1u << ((row0 + rr) & 31);
+                            }
+                        }
+                    }
+                }
+                for (int w = 0; w < 4; ++w)
+                    mt.valid[w] = valid[w];
+                for (int k = 0; k < nbox; ++k)
+                    bytes += 4u * static_cast<uint32_t>(box[k].rows) * 128u;
+                mbar_arrive_expect_tx(&c.full[s], bytes);
+                if (first) {
+                    uint8_t *qb = smem + kQOff + (seg & 1) * kOpBytes;
+                    tma_load_2d(qb, &tm_q, &c.full[s], 0, u * G);
+                    tma_load_2d(qb + kOpChunk, &tm_q, &c.full[s], 64, u * G);
+                }
+                for (int k = 0; k < nbox; ++k) {
+                    uint8_t *dk = st + box[k].row0 * 128;
+                    uint8_t *dv = dk + 2 * kChunkBytes;
+                    if (DENSE) {  // streamed once per slow step: do not displace reusable lines
+                        tma_load_2d_hint(dk, box[k].mk, &c.full[s], 0, box[k].y, pol);
+                        tma_load_2d_hint(dk + kChunkBytes, box[k].mk, &c.full[s], 64, box[k].y, pol);
+                        tma_load_2d_hint(dv, box[k].mv, &c.full[s], 0, box[k].y, pol);
+                        tma_load_2d_hint(dv + kChunkBytes, box[k].mv, &c.full[s], 64, box[k].y, pol);
+                    } else {
+                        tma_load_2d(dk, box[k].mk, &c.full[s], 0, box[k].y);
+                        tma_load_2d(dk + kChunkBytes, box[k].mk, &c.full[s], 64, box[k].y);
+                        tma_load_2d(dv, box[k].mv, &c.full[s], 0, box[k].y);
+                        tma_load_2d(dv + kChunkBytes, box[k].mv, &c.full[s], 64, box[k].y);
+                    }
+                }
+                ++issued;
+            }
+            // Never leave a copy in flight into shared memory we are about to give up.
+            for (int j = max(0, issued - kStages); j < issued; ++j)
+                mbar_wait(&c.full[j % kStages], (j / kStages) & 1, nullptr);
+        }
+    } else if (warp == 1) {
+        // ================================ MMA issuer =====================================
+        if (lane == 0 && n_tiles > 0) {
+            constexpr uint32_t idesc_s = idesc_bf16(kTile, kOpRows, false, false);
+            constexpr uint32_t idesc_o = idesc_bf16(kTile, kOpRows, true, false);
+            int seg = -1;
+            bool ok = true;
+            auto pv = [&](int j) -> bool {
+                const int s = j % kStages, bb = j & 1, use = j >> 1;
+                if (!mbar_wait(&c.p_full[bb], use & 1, &c.abort))
+                    return false;
+                if (!mbar_wait(&c.o_free[bb], (use & 1) ^ 1, &c.abort))
+                    return false;
+                tc_fence_after();
+                const uint32_t va = smem_u32(smem + s * kStageBytes + 2 * kChunkBytes);
+                const uint32_t pa = smem_u32(smem + kPOff + bb * kOpBytes);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t a = smem_desc_sw128(va + kk * 2048, kChunkBytes, 1024);
+                    const uint64_t bd = smem_desc_sw128(pa + (kk >> 2) * kOpChunk + (kk & 3) * 32, 16, 1024);
+                    umma_bf16(tmem + 32 + bb * 16, a, bd, idesc_o, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&c.o_full[bb]);
+                umma_commit(&c.empty[s]);
+                return true;
+            };
+            for (int i = 0; i < n_tiles && ok; ++i) {
+                const int s = i % kStages, bb = i & 1, use = i >> 1;
+                if (!mbar_wait(&c.full[s], (i / kStages) & 1, &c.abort)) {
+                    ok = false;
+                    break;
+                }
+                const int flags = c.meta[s].flags;
+                if (flags & kFlagFirst)
+                    ++seg;
+                if (!mbar_wait(&c.s_free[bb], (use & 1) ^ 1, &c.abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t ka = smem_u32(smem + s * kStageBytes);
+                const uint32_t qa = smem_u32(smem + kQOff + (seg & 1) * kOpBytes);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t a = smem_desc_sw128(ka + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(qa + (kk >> 2) * kOpChunk + (kk & 3) * 32, 16, 1024);
+                    umma_bf16(tmem + bb * 16, a, bd, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&c.s_full[bb]);
+                if (flags & kFlagLast)
+                    umma_commit(&c.q_free[seg & 1]);
+                if (i > 0 && !pv(i - 1))
+                    ok = false;
+            }
+            if (ok && !pv(n_tiles - 1))
+                ok = false;
+            if (!ok)
+                fail(c, p.err);
+            // All MMAs of this thread are complete once `drain` fires.
+            umma_commit(&c.drain);
+            mbar_wait(&c.drain, 0, nullptr);
+        }
+    } else {
+        // ========================= softmax / epilogue warps ============================
+        const int wq = warp & 3;              // TMEM lane quarter this warp may access
+        const int row = wq * 32 + lane;       // S^T row (tile position) / O^T row (dim)
+        const int gw = warp - 2;              // index within the softmax group
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        uint32_t gphase = 0;
+        float m_run[G], le[G], lr[G], acc[G];
+        // the tile waiting for its O^T accumulation
+        float a_alpha[G], a_m[G], a_le[G], a_lr[G];
+        int a_flags = 0, a_unit = 0;
+        bool ok = true;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            m_run[h] = -INFINITY;
+            le[h] = lr[h] = acc[h] = 0.f;
+        }
+
+        auto finalize = [&](int u, const float (&fm)[G], const float (&fle)[G],
+                            const float (&flr)[G]) -> bool {
+            const int kvh = u % Hkv, b = (u / Hkv) % B, layer = u / (Hkv * B);
+            const long long su = layer * c.TL + c.pre[b] + static_cast<long long>(kvh) * c.nt[b];
+            const long long eu = su + c.nt[b];
+            const long long P = c.P, T = c.T;
+            const int cf = static_cast<int>(((su + 1) * P - 1) / T);
+            const int cl = static_cast<int>((eu * P - 1) / T);
+            float o[G];
+            if (cf == cl) {
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+                    o[h] = flr[h] > 0.f ? acc[h] / flr[h] : 0.f;
+                store_out<G>(p, u, row, o);
+                if (DENSE && row < G)
+                    p.stats[u * G + row] = make_float2(fm[row], fle[row]);
+                return true;
+            }
+            const int slot = (su <= g0) ? 0 : 1;
+            float *part = p.partials + (2 * static_cast<size_t>(blockIdx.x) + slot) * kPartialFloats(G);
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+                part[h * kHeadDim + row] = acc[h];
+            if (row < G) {
+                part[G * kHeadDim + row] = fm[row];
+                part[G * kHeadDim + G + row] = fle[row];
+                part[G * kHeadDim + 2 * G + row] = flr[row];
+            }
+            __threadfence();
+            if (!group_sync(c, gphase, lane))
+                return false;
+            if (row == 0) {
+                const int tk = atomicAdd(&p.tickets[u], 1);
+                const int is_last = (tk == cl - cf) ? 1 : 0;
+                if (is_last)
+                    p.tickets[u] = 0;
+                c.last_flag = is_last;
+            }
+            if (!group_sync(c, gphase, lane))
+                return false;
+            if (!c.last_flag)
+                return true;
+            __threadfence();
+            float M[G], Le[G], Lr[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                M[h] = -INFINITY;
+                Le[h] = Lr[h] = o[h] = 0.f;
+            }
+            for (int cc = cf; cc <= cl; ++cc) {
+                const long long start = static_cast<long long>(cc) * T / P;
+                const int sl = (cc == cf && start < su) ? 1 : 0;
+                const float *pc = p.partials + (2 * static_cast<size_t>(cc) + sl) * kPartialFloats(G);
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+                    M[h] = fmaxf(M[h], __ldcg(pc + G * kHeadDim + h));
+            }
+            for (int cc = cf; cc <= cl; ++cc) {
+                const long long start = static_cast<long long>(cc) * T / P;
+                const int sl = (cc == cf && start < su) ? 1 : 0;
+                const float *pc = p.partials + (2 * static_cast<size_t>(cc) + sl) * kPartialFloats(G);
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float mc = __ldcg(pc + G * kHeadDim + h);
+                    const float w = (M[h] == -INFINITY) ? 0.f : exp2f(mc - M[h]);
+                    Le[h] += w * __ldcg(pc + G * kHeadDim + G + h);
+                    Lr[h] += w * __ldcg(pc + G * kHeadDim + 2 * G + h);
+                    o[h] += w * __ldcg(pc + h * kHeadDim + row);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+                o[h] = Lr[h] > 0.f ? o[h] / Lr[h] : 0.f;
+            store_out<G>(p, u, row, o);
+            if (DENSE && row < G)
+                p.stats[u * G + row] = make_float2(M[row], Le[row]);
+            return true;
+        };
+
+        auto correct = [&](int j) -> bool {
+            const int bb = j & 1, use = j >> 1;
+            if (!mbar_wait(&c.o_full[bb], use & 1, &c.abort))
+                return false;
+            float ov[G];
+            tmem_load<G>(t_lane + 32 + bb * 16, ov);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&c.o_free[bb]);
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+                acc[h] = (a_flags & kFlagFirst) ? ov[h] : fmaf(acc[h], a_alpha[h], ov[h]);
+            if (a_flags & kFlagLast) {
+                if (!finalize(a_unit, a_m, a_le, a_lr))
+                    return false;
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+                    acc[h] = 0.f;
+            }
+            return true;
+        };
+
+        for (int i = 0; i < n_tiles && ok; ++i) {
+            const int s = i % kStages, bb = i & 1, use = i >> 1;
+            if (!mbar_wait(&c.s_full[bb], use & 1, &c.abort) ||
+                !mbar_wait(&c.full[s], (i / kStages) & 1, &c.abort)) {
+                ok = false;
+                break;
+            }
+            const int u = c.meta[s].unit;
+            const int tile = c.meta[s].tile;
+            const int flags = c.meta[s].flags;
+            const bool valid = (c.meta[s].valid[row >> 5] >> (row & 31)) & 1u;
+            if (flags & kFlagFirst) {
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    m_run[h] = -INFINITY;
+                    le[h] = lr[h] = 0.f;
+                }
+            }
+            float sv[G];
+            tmem_load<G>(t_lane + bb * 16, sv);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&c.s_free[bb]);
+            float z[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+                z[h] = valid ? sv[h] * p.scale_log2 : -INFINITY;
+            if (DENSE && p.zbuf != nullptr && valid) {
+                float *zp = p.zbuf + (static_cast<size_t>(u) * p.capacity + tile * kTile + row) * G;
+                if constexpr (G == 4) {
+                    *reinterpret_cast<float4 *>(zp) = make_float4(z[0], z[1], z[2], z[3]);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < G; ++h)
+                        zp[h] = z[h];
+                }
+            }
+            // tile max over the 128 positions, per head
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float wm = warp_max(z[h]);
+                if (lane == 0)
+                    c.red_max[i & 1][gw][h] = wm;
+            }
+            if (!group_sync(c, gphase, lane)) {
+                ok = false;
+                break;
+            }
+            float alpha[G];
+            uint8_t *pb = smem + kPOff + bb * kOpBytes;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float tm = fmaxf(fmaxf(c.red_max[i & 1][0][h], c.red_max[i & 1][1][h]),
+                                       fmaxf(c.red_max[i & 1][2][h], c.red_max[i & 1][3][h]));
+                const float mn = fmaxf(m_run[h], tm);
+                const float mb = (mn == -INFINITY) ? 0.f : mn;
+                alpha[h] = exp2f(m_run[h] - mb);
+                const float pe = valid ? exp2f(z[h] - mb) : 0.f;
+                const __nv_bfloat16 pbf = __float2bfloat16_rn(pe);
+                le[h] = fmaf(le[h], alpha[h], pe);
+                lr[h] = fmaf(lr[h], alpha[h], __bfloat162float(pbf));
+                m_run[h] = mn;
+                // P^T[h][row], K-major, 128-byte swizzle
+                const int off = (row >> 6) * kOpChunk + h * 128 +
+                                ((((row & 63) >> 3) ^ h) << 4) + (row & 7) * 2;
+                *reinterpret_cast<__nv_bfloat16 *>(pb + off) = pbf;
+            }
+            if (!valid) {
+                // keep P = 0 rows from meeting stale (possibly non-finite) V data
+                uint8_t *vrow = smem + s * kStageBytes + 2 * kChunkBytes + row * 128;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    reinterpret_cast<uint4 *>(vrow)[k] = make_uint4(0u, 0u, 0u, 0u);
+                    reinterpret_cast<uint4 *>(vrow + kChunkBytes)[k] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&c.p_full[bb]);
+            float fm[G], fle[G], flr[G];
+            if (flags & kFlagLast) {
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float s1 = warp_sum(le[h]), s2 = warp_sum(lr[h]);
+                    if (lane == 0) {
+                        c.red_sum[gw][h] = s1;
+                        c.red_sum[gw][8 + h] = s2;
+                    }
+                }
+                if (!group_sync(c, gphase, lane)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    fm[h] = m_run[h];
+                    fle[h] = c.red_sum[0][h] + c.red_sum[1][h] + c.red_sum[2][h] + c.red_sum[3][h];
+                    flr[h] = c.red_sum[0][8 + h] + c.red_sum[1][8 + h] + c.red_sum[2][8 + h] +
+                             c.red_sum[3][8 + h];
+                }
+            }
+            if (i > 0 && !correct(i - 1)) {
+                ok = false;
+                break;
+            }
+            // this tile now waits for its accumulation
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                a_alpha[h] = alpha[h];
+                if (flags & kFlagLast) {
+                    a_m[h] = fm[h];
+                    a_le[h] = fle[h];
+                    a_lr[h] = flr[h];
+                }
+            }
+            a_flags = flags;
+            a_unit = u;
+            (void)tile;
+        }
+        if (ok && n_tiles > 0 && !correct(n_tiles - 1))
+            ok = false;
+        if (!ok)
+            fail(c, p.err);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// Evidence f_j = (1/G) sum_h exp2(z_hj - M_h) / L_h from the dense step's base-2 logits
+// and merged statistics; one pass over [units][positions].
+template <int G>
+__global__ void __launch_bounds__(256) evidence_kernel(const float *__restrict__ zbuf,
+                                                       const float2 *__restrict__ stats,
+                                                       float *__restrict__ f,
+                                                       const int32_t *__restrict__ seq_len,
+                                                       const uint8_t *__restrict__ active,
+                                                       int batch, int n_kv_heads, int capacity)
+{
+    const int u = blockIdx.y;
+    const int b = (u / n_kv_heads) % batch;
+    if (active && !active[b])
+        return;
+    const int L = min(seq_len[b], capacity);
+    float M[G], inv[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        const float2 st = stats[u * G + h];
+        M[h] = st.x;
+        inv[h] = st.y > 0.f ? 1.f / st.y : 0.f;
+    }
+    const float rg = 1.f / static_cast<float>(G);
+    const float *zu = zbuf + static_cast<size_t>(u) * capacity * G;
+    float *fu = f + static_cast<size_t>(u) * capacity;
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < L; j += gridDim.x * blockDim.x) {
+        float z[G];
+        if constexpr (G == 4) {
+            const float4 v = __ldcs(reinterpret_cast<const float4 *>(zu) + j);
+            z[0] = v.x; z[1] = v.y; z[2] = v.z; z[3] = v.w;
+        } else {
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+                z[h] = __ldcs(zu + static_cast<size_t>(j) * G + h);
+        }
+        float acc = 0.f;
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+            acc += exp2f(z[h] - M[h]) * inv[h];
+        fu[j] = acc * rg;
+    }
+}
+
+template <int G, bool DENSE>
+cudaError_t launch_attn_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
+                          const CUtensorMap &tm_kc, const CUtensorMap &tm_vc, const AttnParams &p,
+                          int grid, cudaStream_t stream)
+{
+    auto kern = attn_kernel<G, DENSE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
+    kern<<<grid, kAttnThreads, kSmemBytes, stream>>>(tm_k, tm_v, tm_q, tm_kc, tm_vc, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t attention_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_attention(bool dense, int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                             const CUtensorMap &tm_q, const CUtensorMap &tm_kc,
+                             const CUtensorMap &tm_vc, const AttnParams &p, int grid,
+                             cudaStream_t stream)
+{
+#define SFI_ATTN_CASE(G)                                                                      \
+    case G:                                                                                   \
+        return dense ? launch_attn_t<G, true>(tm_k, tm_v, tm_q, tm_kc, tm_vc, p, grid, stream) \
+                     : launch_attn_t<G, false>(tm_k, tm_v, tm_q, tm_kc, tm_vc, p, grid, stream);
+    switch (group) {
+        SFI_ATTN_CASE(1)
+        SFI_ATTN_CASE(2)
+        SFI_ATTN_CASE(4)
+        SFI_ATTN_CASE(8)
+    default:
+        return cudaErrorInvalidValue;
+    }
+#undef SFI_ATTN_CASE
+}
+
+cudaError_t launch_evidence(const float *zbuf, const float2 *stats, float *f, const int32_t *seq_len,
+                            const uint8_t *active, int n_layers, int batch, int n_kv_heads, int group,
+                            int capacity, int max_len, cudaStream_t stream)
+{
+    const int units = n_layers * batch * n_kv_heads;
+    dim3 grid((max_len + 256 * 4 - 1) / (256 * 4), units);
+    if (grid.x == 0)
+        grid.x = 1;
+    switch (group) {
+    case 1: evidence_kernel<1><<<grid, 256, 0, stream>>>(zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity); break;
+    case 2: evidence_kernel<2><<<grid, 256, 0, stream>>>(zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity); break;
+    case 4: evidence_kernel<4><<<grid, 256, 0, stream>>>(zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity); break;
+    case 8: evidence_kernel<8><<<grid, 256, 0, stream>>>(zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace sfi

@@ -1,0 +1,80 @@
+// sfi_internal.h -- declarations shared by the library's host code and its kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sfi {
+
+constexpr int kHeadDim = 128;           // elements per K/V/Q row (256 bytes of bf16)
+constexpr int kTile = 128;              // KV rows per attention tile (UMMA M)
+constexpr int kStages = 3;              // shared-memory ring depth of the attention kernels
+constexpr int kMaxBatch = 256;
+constexpr int kAttnThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2-5 softmax/epilogue
+constexpr int kSelectThreads = 1024;
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // bounded pipeline waits: 1 s
+constexpr int kPartialFloats(int G) { return G * kHeadDim + 3 * G; }
+
+// Everything the attention kernels read besides the tensor maps.
+struct AttnParams {
+    int n_layers, batch, n_kv_heads, group;
+    int capacity, page_size, n_pages, max_pages;
+    int max_len;
+    const int32_t *page_table;
+    const int32_t *seq_len;
+    const uint8_t *active;
+    uint32_t *err;
+    // sparse step
+    const int32_t *comp_rows;   // packed rows per unit
+    const int32_t *sel_cnt;     // selected rows per unit
+    int comp_cap;               // n_sink + n_select: packed-buffer rows per unit
+    int n_window;
+    int n_cbox;                 // 64-row boxes of the packed region per unit
+    int n_wbox;                 // 16-row boxes of the window region per unit
+    int tiles_per_unit;         // sparse: ceil((64 n_cbox + 16 n_wbox) / 128)
+    // outputs and workspace
+    void *out;
+    int out_fp32;
+    float *zbuf;                // dense: base-2 logits [units][capacity][G] (or null)
+    float2 *stats;              // dense: (max, sum) of base-2 logits per (unit, head)
+    float *partials;            // [2 * gridDim.x][kPartialFloats(G)]
+    int *tickets;               // [units]
+    float scale_log2;           // log2(e) / sqrt(128)
+};
+
+struct SelectParams {
+    const float *f;             // [units][capacity]
+    int capacity, batch, n_kv_heads, n_units;
+    const int32_t *seq_len;
+    const uint8_t *active;
+    int n_sink, n_window, n_select, prior_tau;
+    double lambda;
+    int32_t *sel_idx;           // [units][n_select]
+    int32_t *sel_cnt;           // [units]
+};
+
+// Launchers (return the cudaGetLastError() of the launch).
+cudaError_t launch_attention(bool dense, int group, const CUtensorMap &tm_k,
+                             const CUtensorMap &tm_v, const CUtensorMap &tm_q,
+                             const CUtensorMap &tm_kc, const CUtensorMap &tm_vc,
+                             const AttnParams &p, int grid, cudaStream_t stream);
+cudaError_t launch_evidence(const float *zbuf, const float2 *stats, float *f,
+                            const int32_t *seq_len, const uint8_t *active, int n_layers,
+                            int batch, int n_kv_heads, int group, int capacity, int max_len,
+                            cudaStream_t stream);
+cudaError_t launch_select(const SelectParams &p, cudaStream_t stream);
+cudaError_t launch_append(const void *k_new, const void *v_new, void *k, void *v,
+                          int32_t *seq_len, const uint8_t *active, const int32_t *page_table,
+                          int n_layers, int batch, int n_kv_heads, int capacity, int page_size,
+                          int n_pages, int max_pages, uint32_t *err, cudaStream_t stream);
+cudaError_t launch_compact(const void *k, const void *v, void *kc, void *vc,
+                           const int32_t *sel_idx, const int32_t *sel_cnt, int32_t *rows,
+                           const int32_t *seq_len, const uint8_t *active,
+                           const int32_t *page_table, int n_layers, int batch, int n_kv_heads,
+                           int capacity, int page_size, int n_pages, int max_pages, int n_sink,
+                           int n_select, uint32_t *err, cudaStream_t stream);
+
+size_t attention_smem_bytes();
+
+}  // namespace sfi

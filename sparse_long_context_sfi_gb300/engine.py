@@ -1,0 +1,134 @@
+"""Device state of one SFI decode workload and the calls that step it.
+
+`SfiState` owns (through PyTorch allocations) the KV cache, the packed sparse memory, the
+evidence buffer and the workspace, and builds the C descriptors. Stepping goes through the
+C ABI only: `step()` issues the per-step calls, `run()` hands a whole decode run to the
+native driver `sfi_decode_run` (capturable in a CUDA graph).
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import numpy as np
+import torch
+
+from . import (SfiBudget, SfiDecodePlan, SfiKvCache, SfiSparseMem, sfi_append_kv, sfi_compact,
+               sfi_decode_run, sfi_dense_decode_attn, sfi_schedule, sfi_select,
+               sfi_sparse_decode_attn, sfi_workspace_bytes, sfi_workspace_init)
+
+
+class SfiState:
+    def __init__(self, cfg, len0, device="cuda", page_table=None, n_pages=0, capacity=None):
+        self.cfg = cfg
+        self.device = torch.device(device)
+        B, Ly, Hkv, Hq, D = cfg.batch, cfg.n_layers, cfg.n_kv_heads, cfg.n_q_heads, cfg.head_dim
+        self.len0 = np.asarray(len0, dtype=np.int64)
+        self.capacity = capacity or int(self.len0.max()) + cfg.steps
+        bf = torch.bfloat16
+        if cfg.page_size:
+            pt = np.asarray(page_table, dtype=np.int32)
+            self.page_table = torch.from_numpy(pt).to(self.device)
+            self.n_pages = int(n_pages)
+            self.max_pages = int(pt.shape[1])
+            self.capacity = self.max_pages * cfg.page_size
+            shape = (Ly, self.n_pages, Hkv, cfg.page_size, D)
+        else:
+            self.page_table = None
+            self.n_pages = 0
+            self.max_pages = 0
+            shape = (Ly, B, Hkv, self.capacity, D)
+        self.k = torch.zeros(shape, dtype=bf, device=self.device)
+        self.v = torch.zeros(shape, dtype=bf, device=self.device)
+        self.seq_len = torch.from_numpy(self.len0.astype(np.int32)).to(self.device)
+        self.err = torch.zeros(4, dtype=torch.int32, device=self.device)
+        U = Ly * B * Hkv
+        self.n_units = U
+        comp = cfg.n_sink + cfg.n_select
+        self.kc = torch.zeros((Ly, B, Hkv, comp, D), dtype=bf, device=self.device)
+        self.vc = torch.zeros((Ly, B, Hkv, comp, D), dtype=bf, device=self.device)
+        self.sel_idx = torch.zeros((U, max(1, cfg.n_select)), dtype=torch.int32, device=self.device)
+        self.sel_cnt = torch.zeros(U, dtype=torch.int32, device=self.device)
+        self.rows = torch.zeros(U, dtype=torch.int32, device=self.device)
+        self.scores = torch.zeros((U, self.capacity), dtype=torch.float32, device=self.device)
+        self.kv = SfiKvCache(
+            n_layers=Ly, batch=B, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, capacity=self.capacity,
+            page_size=cfg.page_size, n_pages=self.n_pages, max_pages_per_seq=self.max_pages,
+            max_len=int(self.len0.max()), k=self.k.data_ptr(), v=self.v.data_ptr(),
+            page_table=None if self.page_table is None else self.page_table.data_ptr(),
+            seq_len=self.seq_len.data_ptr(), err=self.err.data_ptr())
+        self.budget = SfiBudget(n_sink=cfg.n_sink, n_window=cfg.n_window, n_select=cfg.n_select,
+                                prior_tau=cfg.prior_tau, lambda_=cfg.lam)
+        self.mem = SfiSparseMem(kc=self.kc.data_ptr(), vc=self.vc.data_ptr(),
+                                sel_idx=self.sel_idx.data_ptr(), sel_cnt=self.sel_cnt.data_ptr(),
+                                rows=self.rows.data_ptr())
+        self.ws_bytes = sfi_workspace_bytes(self.kv, self.budget)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        sfi_workspace_init(self.ws, self.ws_bytes)
+        self.t = 0
+
+    # -- host bookkeeping -------------------------------------------------------------------
+    def reset_lengths(self):
+        self.seq_len.copy_(torch.from_numpy(self.len0.astype(np.int32)))
+        self.t = 0
+
+    def schedule(self, masks: np.ndarray) -> np.ndarray:
+        """Slow flags [steps][B] from per-sequence boundary masks [B][steps]."""
+        return np.stack([sfi_schedule(masks[b], self.cfg.t_max) for b in range(self.cfg.batch)], 1)
+
+    # -- one decode step through the individual calls -----------------------------------------
+    def step(self, q, k_new, v_new, slow_b: np.ndarray, out, out_fp32=True, stream=None):
+        """q [Ly][B][Hq][D] bf16, k_new/v_new [Ly][B][Hkv][D] bf16 (device); slow_b [B] bool."""
+        kv = self.kv
+        kv.max_len = int(self.len0.max()) + self.t
+        sfi_append_kv(kv, k_new, v_new, stream=stream)
+        kv.max_len = int(self.len0.max()) + self.t + 1
+        slow_b = np.asarray(slow_b, bool)
+        mixed = slow_b.any() and not slow_b.all()
+        if mixed:
+            m = torch.from_numpy(np.stack([slow_b, ~slow_b]).astype(np.uint8)).to(self.device)
+            a_slow, a_fast = m[0], m[1]
+        else:
+            a_slow = a_fast = None
+        if slow_b.any():
+            sfi_dense_decode_attn(kv, q, out, out_fp32, self.scores, self.ws, self.ws_bytes,
+                                  active=a_slow, stream=stream)
+            sfi_select(kv, self.scores, self.budget, self.mem, active=a_slow, stream=stream)
+            sfi_compact(kv, self.budget, self.mem, active=a_slow, stream=stream)
+        if not slow_b.all():
+            sfi_sparse_decode_attn(kv, self.mem, self.budget, q, out, out_fp32, self.ws,
+                                   self.ws_bytes, active=a_fast, stream=stream)
+        self.t += 1
+        return mixed and (a_slow, a_fast)
+
+    # -- a whole run through the native driver --------------------------------------------------
+    def make_plan(self, slow: np.ndarray, q, k_new, v_new, out, out_fp32=True, out_per_step=True,
+                  dense_only=False, events=None):
+        """slow: uint8 [steps][B]; q/k_new/v_new/out: device tensors with a leading step axis.
+        events: optional list of 2 * steps torch.cuda.Event(enable_timing=True), recorded
+        around each step's attention kernel."""
+        slow = np.ascontiguousarray(slow, dtype=np.uint8)
+        steps = slow.shape[0]
+        mixed = np.array([(r.any() and not r.all()) for r in slow])
+        masks = None
+        if mixed.any():
+            m = np.stack([slow, 1 - slow], axis=1).astype(np.uint8)
+            masks = torch.from_numpy(m).to(self.device)
+        plan = SfiDecodePlan(
+            n_steps=steps, slow=slow.ctypes.data, q=q.data_ptr(), k_new=k_new.data_ptr(),
+            v_new=v_new.data_ptr(), out=out.data_ptr(), out_fp32=1 if out_fp32 else 0,
+            out_per_step=1 if out_per_step else 0, scores_f=self.scores.data_ptr(),
+            masks=None if masks is None else masks.data_ptr(), len_start=int(self.len0.max()),
+            dense_only=1 if dense_only else 0)
+        ev_arr = None
+        if events is not None:
+            assert len(events) == 2 * steps
+            for e in events:          # make sure the driver-level event objects exist
+                e.record()
+            torch.cuda.synchronize()
+            ev_arr = (C.c_void_p * (2 * steps))(*[e.cuda_event for e in events])
+            plan.events = C.cast(ev_arr, C.c_void_p)
+        plan._keep = (slow, masks, q, k_new, v_new, out, ev_arr, events)
+        return plan
+
+    def run(self, plan: SfiDecodePlan, stream=None):
+        sfi_decode_run(self.kv, self.budget, self.mem, plan, self.ws, self.ws_bytes, stream=stream)

@@ -1,0 +1,63 @@
+"""Put a synthetic workload on the GPU: cache contents, the decode queries and the tokens
+appended at every step, generated in place by the GPU twin of synth.gen (or uploaded
+from the host generator for small cases). Input generation only."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import gpu
+from .workload import HostWorkload
+
+
+def _bf16(a: np.ndarray, device):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+class DeviceInputs:
+    """q [steps][Ly][B][Hq][D], k_new/v_new [steps][Ly][B][Hkv][D] (bf16, device)."""
+
+    def __init__(self, wl: HostWorkload, steps: int, device, on_device: bool = True):
+        cfg = wl.cfg
+        self.steps = steps
+        if on_device:
+            self.model = gpu.DeviceModel(wl, device)
+            self.q = torch.empty((steps, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
+                                 dtype=torch.bfloat16, device=device)
+            shape = (steps, cfg.n_layers, cfg.batch, cfg.n_kv_heads, cfg.head_dim)
+            self.k_new = torch.empty(shape, dtype=torch.bfloat16, device=device)
+            self.v_new = torch.empty(shape, dtype=torch.bfloat16, device=device)
+            len0 = torch.from_numpy(wl.len0.astype(np.int64)).to(device)
+            gpu.fill_queries(wl, self.q, self.model)
+            gpu.fill_new_tokens(wl, self.k_new, self.v_new, len0, self.model)
+        else:
+            self.model = None
+            self.q = _bf16(wl.queries(steps), device)
+            self.k_new = _bf16(wl.new_tokens("k", steps), device)
+            self.v_new = _bf16(wl.new_tokens("v", steps), device)
+
+
+def fill_state_cache(wl: HostWorkload, state, on_device: bool = True, model=None):
+    """Write the prefill rows of every sequence into state.k / state.v."""
+    cfg = wl.cfg
+    dev = state.k.device
+    if on_device:
+        model = model or gpu.DeviceModel(wl, dev)
+        fill = torch.from_numpy(wl.len0.astype(np.int64)).to(dev)
+        owners = gpu.page_owners(wl, dev) if cfg.page_size else None
+        gpu.fill_cache(wl, state.k, state.v, fill, model, owners)
+    else:
+        if cfg.page_size:
+            state.k.copy_(_bf16(wl.cache_paged("k"), dev))
+            state.v.copy_(_bf16(wl.cache_paged("v"), dev))
+        else:
+            state.k.copy_(_bf16(wl.cache_contiguous("k", state.capacity), dev))
+            state.v.copy_(_bf16(wl.cache_contiguous("v", state.capacity), dev))
+    return model
+
+
+def make_state(wl: HostWorkload, device="cuda", on_device: bool = True):
+    from sparse_long_context_sfi_gb300.engine import SfiState
+    state = SfiState(wl.cfg, wl.len0, device=device, page_table=wl.table, n_pages=wl.n_pages)
+    fill_state_cache(wl, state, on_device)
+    return state

@@ -1,0 +1,88 @@
+"""The C-ABI library loads and exports every entry point include/sfi.h declares; its
+host-only paths (status strings, argument checks that fail before any CUDA call, the
+trigger-policy scheduler) work without a GPU."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import sparse_long_context_sfi_gb300 as sfi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    return sfi.lib()
+
+
+def declared():
+    src = open(os.path.join(ROOT, "include", "sfi.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sfi_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared()
+    assert "sfi_dense_decode_attn" in names and "sfi_select" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in sfi.h but not exported"
+    assert sorted(sfi.ENTRY_POINTS) == names
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert sfi.status_string(s)
+    assert "sm_103a" in sfi.sfi_version()
+
+
+def test_argument_errors_return_before_any_launch(lib):
+    kv = sfi.SfiKvCache()  # all zero: null pointers
+    st = lib.sfi_append_kv(C.byref(kv), None, None, None, None)
+    assert st == sfi.SFI_ERR_INVALID_ARG
+    dummy = 1 << 20  # never dereferenced: the checks fail first
+    kv = sfi.SfiKvCache(n_layers=1, batch=1, n_q_heads=8, n_kv_heads=2, head_dim=64, capacity=16,
+                        max_len=4, k=dummy, v=dummy, seq_len=dummy, err=dummy)
+    assert lib.sfi_append_kv(C.byref(kv), dummy, dummy, None, None) == sfi.SFI_ERR_UNSUPPORTED
+    kv.head_dim = 128
+    kv.n_q_heads = 12  # group 6
+    assert lib.sfi_append_kv(C.byref(kv), dummy, dummy, None, None) == sfi.SFI_ERR_UNSUPPORTED
+    kv.n_q_heads = 8
+    kv.max_len = 16    # no room to append
+    assert lib.sfi_append_kv(C.byref(kv), dummy, dummy, None, None) == sfi.SFI_ERR_CAPACITY
+    kv.max_len = 4
+    kv.k = dummy + 8   # misaligned
+    assert lib.sfi_append_kv(C.byref(kv), dummy, dummy, None, None) == sfi.SFI_ERR_INVALID_ARG
+    kv.k = dummy
+    kv.page_size = 16  # paged without a page table
+    assert lib.sfi_append_kv(C.byref(kv), dummy, dummy, None, None) == sfi.SFI_ERR_INVALID_ARG
+    kv.page_size = 0
+    bad = sfi.SfiBudget(n_sink=4, n_window=64, n_select=16, prior_tau=48, lambda_=0.1)
+    mem = sfi.SfiSparseMem(kc=dummy, vc=dummy, sel_idx=dummy, sel_cnt=dummy, rows=dummy)
+    assert lib.sfi_select(C.byref(kv), dummy, C.byref(bad), C.byref(mem), None, None) == \
+        sfi.SFI_ERR_INVALID_ARG  # tau not a power of two
+    bad.prior_tau, bad.lambda_ = 64, 1.5
+    assert lib.sfi_compact(C.byref(kv), C.byref(bad), C.byref(mem), None, None) == \
+        sfi.SFI_ERR_INVALID_ARG  # lambda outside [0, 1]
+
+
+@pytest.mark.parametrize("t_max", [0, 1, 5, 64])
+def test_native_scheduler_matches_oracle(lib, t_max):
+    rng = np.random.default_rng(t_max)
+    for _ in range(20):
+        m = (rng.random(rng.integers(1, 200)) < 0.15).astype(np.uint8)
+        np.testing.assert_array_equal(sfi.sfi_schedule(m, t_max), oracle.schedule(m, t_max))
+
+
+def test_decode_plan_layout_matches_header(lib):
+    """ctypes structs mirror the C layouts (field offsets of the 64-bit ABI)."""
+    assert C.sizeof(sfi.SfiKvCache) == 10 * 4 + 5 * 8
+    assert C.sizeof(sfi.SfiBudget) == 4 * 4 + 8
+    assert C.sizeof(sfi.SfiSparseMem) == 5 * 8
+    assert sfi.SfiDecodePlan.masks.offset == 64 and sfi.SfiDecodePlan.events.offset == 80
+    assert C.sizeof(sfi.SfiDecodePlan) == 88

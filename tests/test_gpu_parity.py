@@ -1,0 +1,248 @@
+"""GPU parity: every step of the SFI decode path, called through the C ABI, against the CPU
+oracle on the same seeded inputs.
+
+Tolerances: attention outputs |gpu - oracle| <= 2e-3 + 1e-2 |oracle| (bf16 inputs, fp32
+accumulation, fp32 output); selections bit-exact when both sides get the same evidence;
+end-to-end selected sets overlap >= 99.5 % when each side uses its own evidence; the
+evidence itself within 2e-3 relative + 1e-9 absolute (fp32 logits from bf16 products).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import decode as odecode
+from synth import device as sdev
+from synth import gen
+from synth.configs import WORKLOADS
+from synth.workload import HostWorkload
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 2e-3, 1e-2
+
+
+def close(g, o):
+    g = np.asarray(g, np.float64)
+    o = np.asarray(o, np.float64)
+    bad = np.abs(g - o) > ATOL + RTOL * np.abs(o)
+    return not bad.any(), float(np.abs(g - o).max())
+
+
+def small(name, **kw):
+    return HostWorkload(WORKLOADS[name].scaled(**kw))
+
+
+def unit_coords(cfg, u):
+    return u // (cfg.n_kv_heads * cfg.batch), (u // cfg.n_kv_heads) % cfg.batch, u % cfg.n_kv_heads
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+
+
+# ------------------------------------------------------------------------- input generator
+
+@pytest.mark.parametrize("model", ["zipf", "hh", "paged"])
+def test_gpu_generator_bit_identical(model):
+    if model == "paged":
+        wl = small("ragged_paged_b32", batch=3, ctx=700, ctx_lo=300, steps=5)
+    elif model == "hh":
+        wl = small("gqa4_ctx4k_hh", ctx=1000, steps=6, n_layers=2)
+    else:
+        wl = small("llama8b_ctx32k_b4", ctx=900, steps=6, batch=2)
+    st = sdev.make_state(wl, on_device=True)
+    if wl.cfg.page_size:
+        ref_k, ref_v = wl.cache_paged("k"), wl.cache_paged("v")
+    else:
+        ref_k = wl.cache_contiguous("k", st.capacity)
+        ref_v = wl.cache_contiguous("v", st.capacity)
+    assert np.array_equal(st.k.view(torch.int16).cpu().numpy().view(np.uint16), ref_k)
+    assert np.array_equal(st.v.view(torch.int16).cpu().numpy().view(np.uint16), ref_v)
+    ins = sdev.DeviceInputs(wl, wl.cfg.steps, st.k.device, on_device=True)
+    as16 = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(as16(ins.q), wl.queries())
+    assert np.array_equal(as16(ins.k_new), wl.new_tokens("k"))
+    assert np.array_equal(as16(ins.v_new), wl.new_tokens("v"))
+
+
+# ------------------------------------------------------------------- slow step, piece by piece
+
+def run_first_slow_step(wl, out_fp32=True):
+    st = sdev.make_state(wl, on_device=True)
+    ins = sdev.DeviceInputs(wl, 1, st.k.device, on_device=True)
+    cfg = wl.cfg
+    out = torch.zeros((cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
+                      dtype=torch.float32 if out_fp32 else torch.bfloat16, device=st.k.device)
+    st.step(ins.q[0], ins.k_new[0], ins.v_new[0], np.ones(cfg.batch, bool), out, out_fp32)
+    torch.cuda.synchronize()
+    assert int(st.err[0]) == 0
+    return st, out.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("case", [
+    dict(name="gqa4_ctx4k_hh"),                                      # the small workload
+    dict(name="gqa4_ctx4k_hh", ctx=1000),                            # ragged last tile
+    dict(name="gqa4_ctx4k_hh", ctx=100),                             # one partial tile
+    dict(name="llama8b_ctx32k_b4", ctx=3000, batch=3, n_layers=2),   # many units, splits
+    dict(name="llama8b_ctx32k_b4", ctx=20000, batch=1),              # long units
+    dict(name="llama8b_ctx32k_b4", ctx=1500, n_q_heads=8, n_kv_heads=8),   # group 1
+    dict(name="llama8b_ctx32k_b4", ctx=1500, n_q_heads=16, n_kv_heads=8),  # group 2
+    dict(name="llama8b_ctx32k_b4", ctx=1500, n_q_heads=64, n_kv_heads=8),  # group 8
+    dict(name="ragged_paged_b32", batch=5, ctx=3000, ctx_lo=200),    # paged, ragged
+])
+def test_dense_select_compact_vs_oracle(case):
+    case = dict(case)
+    wl = small(case.pop("name"), steps=2, **case)
+    cfg = wl.cfg
+    st, out = run_first_slow_step(wl)
+    G, D, S, W, K = cfg.group, cfg.head_dim, cfg.n_sink, cfg.n_window, cfg.n_select
+    f_gpu = st.scores.cpu().numpy()
+    sel_gpu = st.sel_idx.cpu().numpy()
+    cnt_gpu = st.sel_cnt.cpu().numpy()
+    rows_gpu = st.rows.cpu().numpy()
+    kc = st.kc.view(torch.int16).cpu().numpy().view(np.uint16).reshape(st.n_units, S + K, D)
+    vc = st.vc.view(torch.int16).cpu().numpy().view(np.uint16).reshape(st.n_units, S + K, D)
+    for u in range(st.n_units):
+        layer, b, kvh = unit_coords(cfg, u)
+        L = int(wl.len0[b]) + 1
+        k = wl.rows("k", layer, b, kvh, np.arange(L))
+        v = wl.rows("v", layer, b, kvh, np.arange(L))
+        q = wl.query(0, layer, b)[kvh * G:(kvh + 1) * G]
+        o, p = oracle.attend(q, k, v, want_p=True)
+        ok, err = close(out[layer, b, kvh * G:(kvh + 1) * G], o)
+        assert ok, f"unit {u}: dense output max err {err}"
+        f_or = oracle.evidence(p)
+        np.testing.assert_allclose(f_gpu[u, :L], f_or, rtol=2e-3, atol=1e-9)
+        # the Selector is bit-exact given the same (GPU) evidence
+        sel_or = oracle.select(L, S, W, K, cfg.prior_tau, cfg.lam, f_gpu[u, :L])
+        assert cnt_gpu[u] == len(sel_or)
+        np.testing.assert_array_equal(sel_gpu[u, :cnt_gpu[u]], sel_or)
+        # ... and close to the oracle's own selection
+        sel_own = oracle.select(L, S, W, K, cfg.prior_tau, cfg.lam, f_or.astype(np.float32))
+        if len(sel_own):
+            assert len(np.intersect1d(sel_own, sel_or)) >= 0.995 * len(sel_own)
+        # packed rows: sinks then selected positions, copied verbatim
+        n_s = min(S, L)
+        assert rows_gpu[u] == n_s + cnt_gpu[u]
+        want = np.concatenate([np.arange(n_s), sel_or]).astype(np.int64)
+        np.testing.assert_array_equal(kc[u, :rows_gpu[u]], k[want])
+        np.testing.assert_array_equal(vc[u, :rows_gpu[u]], v[want])
+
+
+def test_dense_bf16_output():
+    wl = small("gqa4_ctx4k_hh", ctx=777, steps=2)
+    _, o32 = run_first_slow_step(wl, True)
+    _, o16 = run_first_slow_step(wl, False)
+    np.testing.assert_allclose(o16, o32, rtol=2 ** -8, atol=1e-6)
+
+
+# ------------------------------------------------------------------------------ fast step
+
+@pytest.mark.parametrize("case", [
+    dict(name="gqa4_ctx4k_hh"),
+    dict(name="llama8b_ctx32k_b4", ctx=5000, batch=2),
+    dict(name="llama8b_ctx32k_b4", ctx=150, batch=2),                # n_C < K: all selected
+    dict(name="llama8b_ctx32k_b4", ctx=40, batch=1),                 # window clipped at sinks
+    dict(name="ragged_paged_b32", batch=4, ctx=2500, ctx_lo=700),    # paged window
+])
+def test_sparse_step_vs_oracle(case):
+    """Slow step at t=0, then fast steps: each fast output equals attention over sinks +
+    the (GPU-selected) memory + the sliding window."""
+    case = dict(case)
+    wl = small(case.pop("name"), steps=20, **case)
+    cfg = wl.cfg
+    st = sdev.make_state(wl, on_device=True)
+    n = 20
+    ins = sdev.DeviceInputs(wl, n, st.k.device)
+    outs = torch.zeros((n, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
+                       dtype=torch.float32, device=st.k.device)
+    sel = None
+    for t in range(n):
+        slow = np.full(cfg.batch, t == 0)
+        st.step(ins.q[t], ins.k_new[t], ins.v_new[t], slow, outs[t])
+        if t == 0:
+            torch.cuda.synchronize()
+            sel = [st.sel_idx[u, :int(st.sel_cnt[u])].cpu().numpy() for u in range(st.n_units)]
+    torch.cuda.synchronize()
+    assert int(st.err[0]) == 0
+    outs = outs.cpu().numpy()
+    G, S, W = cfg.group, cfg.n_sink, cfg.n_window
+    for u in range(st.n_units):
+        layer, b, kvh = unit_coords(cfg, u)
+        Ls = int(wl.len0[b]) + 1
+        k = wl.rows("k", layer, b, kvh, np.arange(Ls + n))
+        v = wl.rows("v", layer, b, kvh, np.arange(Ls + n))
+        for t in range(1, n, 3):
+            rows = oracle.sparse_rows(Ls, Ls + t, S, W, sel[u])
+            q = wl.query(t, layer, b)[kvh * G:(kvh + 1) * G]
+            o, _ = oracle.attend(q, k, v, rows)
+            ok, err = close(outs[t, layer, b, kvh * G:(kvh + 1) * G], o)
+            assert ok, f"unit {u} step {t}: sparse max err {err}"
+
+
+# ------------------------------------------------------------------ whole decode, end to end
+
+def decode_on_gpu(wl, steps, on_device=True):
+    cfg = wl.cfg
+    st = sdev.make_state(wl, on_device=on_device)
+    ins = sdev.DeviceInputs(wl, steps, st.k.device, on_device=on_device)
+    slow = st.schedule(wl.masks[:, :steps])
+    out = torch.zeros((steps, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
+                      dtype=torch.float32, device=st.k.device)
+    plan = st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out)
+    st.run(plan)
+    torch.cuda.synchronize()
+    assert int(st.err[0]) == 0
+    return st, slow, out.cpu().numpy()
+
+
+def compare_run(wl, steps, units=None, check_steps=None):
+    cfg = wl.cfg
+    st, slow, out = decode_on_gpu(wl, steps)
+    ref = odecode.run(wl, steps=steps, units=units)
+    assert np.array_equal(ref["slow"].T, slow)
+    units = list(range(st.n_units)) if units is None else units
+    G = cfg.group
+    for t in (range(steps) if check_steps is None else check_steps):
+        for i, u in enumerate(units):
+            layer, b, kvh = unit_coords(cfg, u)
+            ok, err = close(out[t, layer, b, kvh * G:(kvh + 1) * G], ref["out"][t][i])
+            assert ok, f"step {t} unit {u}: max err {err}"
+    return st, ref
+
+
+def test_end_to_end_small_workload():
+    """The 4K-context workload, all 32 steps (slow at 0 and 16), every unit."""
+    wl = HostWorkload(WORKLOADS["gqa4_ctx4k_hh"])
+    compare_run(wl, wl.cfg.steps)
+
+
+def test_end_to_end_ragged_paged_per_sequence_schedule():
+    wl = small("ragged_paged_b32", batch=6, ctx=2400, ctx_lo=600, steps=40, mask_param=6)
+    compare_run(wl, 40, check_steps=range(0, 40, 3))
+
+
+def test_end_to_end_32k_batch4_sampled():
+    """The 32K-context, batch-4 workload at full size through the native driver: sampled
+    units over the first steps (a slow step and the fast steps that reuse its memory)."""
+    wl = HostWorkload(WORKLOADS["llama8b_ctx32k_b4"])
+    compare_run(wl, 6, units=[0, 7, 13, 31])
+
+
+# ------------------------------------------------------------------------------ error paths
+
+def test_bad_page_entry_sets_device_error_and_skips():
+    from sparse_long_context_sfi_gb300 import SFI_DEVERR_PAGE_RANGE, sfi_read_error
+    wl = small("ragged_paged_b32", batch=2, ctx=600, ctx_lo=300, steps=2)
+    st = sdev.make_state(wl, on_device=True)
+    st.page_table[1, 3] = wl.n_pages + 5          # out of range: caught by the kernels' checks
+    ins = sdev.DeviceInputs(wl, 1, st.k.device)
+    out = torch.zeros((1, 2, 32, 128), dtype=torch.float32, device=st.k.device)
+    st.step(ins.q[0], ins.k_new[0], ins.v_new[0], np.ones(2, bool), out)
+    bits = sfi_read_error(st.kv)
+    assert bits & SFI_DEVERR_PAGE_RANGE
+    assert np.isfinite(out.cpu().numpy()).all()
