@@ -133,6 +133,18 @@ WsLayout ws_layout(const sfi_kv_cache *kv, int sms)
 
 cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 
+// Timing events: recorded as external event nodes while the stream is being captured
+// (so graph replays time the kernel), as plain records otherwise.
+cudaError_t record_event(cudaEvent_t e, cudaStream_t s)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t err = cudaStreamIsCapturing(s, &cs);
+    if (err != cudaSuccess)
+        return err;
+    return cudaEventRecordWithFlags(e, s, cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal
+                                                                              : cudaEventRecordDefault);
+}
+
 sfi_status launch_status(cudaError_t e) { return e == cudaSuccess ? SFI_OK : SFI_ERR_CUDA; }
 
 void fill_common(AttnParams &p, const sfi_kv_cache *kv, const uint8_t *active)
@@ -196,12 +208,12 @@ sfi_status dense_impl(const sfi_kv_cache *kv, const void *q, void *out, int32_t 
         return SFI_ERR_CUDA;
     const long long t_upper = units * ((kv->max_len + kTile - 1) / kTile);
     const int grid = static_cast<int>(t_upper < sms ? t_upper : sms);
-    if (e0 && cudaEventRecordWithFlags(e0, as_stream(stream), cudaEventRecordExternal) != cudaSuccess)
+    if (e0 && record_event(e0, as_stream(stream)) != cudaSuccess)
         return SFI_ERR_CUDA;
     cudaError_t e = launch_attention(true, g, tk, tv, tq, tk, tv, p, grid, as_stream(stream));
     if (e != cudaSuccess)
         return SFI_ERR_CUDA;
-    if (e1 && cudaEventRecordWithFlags(e1, as_stream(stream), cudaEventRecordExternal) != cudaSuccess)
+    if (e1 && record_event(e1, as_stream(stream)) != cudaSuccess)
         return SFI_ERR_CUDA;
     if (scores_f) {
         e = launch_evidence(p.zbuf, p.stats, scores_f, kv->seq_len, active, kv->n_layers,
@@ -256,11 +268,11 @@ sfi_status sparse_impl(const sfi_kv_cache *kv, const sfi_sparse_mem *mem,
         return SFI_ERR_CUDA;
     const long long t_upper = units * p.tiles_per_unit;
     const int grid = static_cast<int>(t_upper < sms ? t_upper : sms);
-    if (e0 && cudaEventRecordWithFlags(e0, as_stream(stream), cudaEventRecordExternal) != cudaSuccess)
+    if (e0 && record_event(e0, as_stream(stream)) != cudaSuccess)
         return SFI_ERR_CUDA;
     if (launch_attention(false, g, tk, tv, tq, tkc, tvc, p, grid, as_stream(stream)) != cudaSuccess)
         return SFI_ERR_CUDA;
-    if (e1 && cudaEventRecordWithFlags(e1, as_stream(stream), cudaEventRecordExternal) != cudaSuccess)
+    if (e1 && record_event(e1, as_stream(stream)) != cudaSuccess)
         return SFI_ERR_CUDA;
     return SFI_OK;
 }

@@ -139,33 +139,47 @@ def hh_direction(key, n_layers: int, n_kv_heads: int, head_dim: int):
     return (a * u).astype(np.float32), (4.0 * a * u).astype(np.float32)
 
 
+def _draw_distinct(key, stream, layer, b, head, base, n, ctx, taken):
+    """n distinct positions in [0, ctx) not in `taken`, by rejection: candidate i is
+    hash(stream, layer, b, head, base + i) mod ctx (uniform without replacement)."""
+    out = []
+    i = 0
+    while len(out) < n:
+        p = int(hash_at(key, stream, layer, b, head, np.array([base + i]), 0)[0] % np.uint64(ctx))
+        i += 1
+        if p not in taken:
+            taken.add(p)
+            out.append(p)
+    return out
+
+
+def hh_epochs(key, layer: int, b: int, head: int, ctx: int, n_epochs: int,
+              count: int = HEAVY_HITTERS, drift_frac: float = 0.1):
+    """Heavy-hitter position sets (sorted) of one (layer, sequence, kv head) for epochs
+    0 .. n_epochs-1, in [0, ctx).
+
+    Epoch 0: `count` positions uniform without replacement (rejection on the hash). Each
+    later epoch re-seeds round(drift_frac * count) of them: the ones with the smallest
+    drift hash are dropped and as many new positions, not already in the set, are drawn
+    from that epoch's own stream."""
+    cur = sorted(_draw_distinct(key, STREAM_HH, layer, b, head, 0, count, ctx, set()))
+    out = [np.array(cur, dtype=np.int64)]
+    n_move = int(round(drift_frac * count))
+    for e in range(1, n_epochs):
+        dh = hash_at(key, STREAM_DRIFT, layer, b, head, np.array(cur), 2 * e)
+        drop = set(np.array(cur)[np.argsort(dh, kind="stable")[:n_move]].tolist())
+        keep = [p for p in cur if p not in drop]
+        new = _draw_distinct(key, STREAM_DRIFT, layer, b, head, (2 * e + 1) << 12, n_move, ctx,
+                             set(cur))
+        cur = sorted(keep + new)
+        out.append(np.array(cur, dtype=np.int64))
+    return out
+
+
 def hh_positions(key, layer: int, b: int, head: int, ctx: int, epoch: int = 0,
                  count: int = HEAVY_HITTERS, drift_frac: float = 0.1) -> np.ndarray:
-    """Sorted heavy-hitter positions of one (layer, sequence, kv head) in [0, ctx).
-
-    Epoch 0: the `count` positions with the smallest hash values (uniform without
-    replacement). Each later epoch re-seeds round(drift_frac * count) of them: the ones
-    of smallest drift hash are dropped and replaced by the smallest-hash positions not
-    already in the set, drawn from the epoch's own stream."""
-    pos = np.arange(ctx, dtype=np.int64)
-    hv = hash_at(key, STREAM_HH, layer, b, head, pos, 0)
-    cur = np.sort(np.argsort(hv, kind="stable")[:count])
-    n_move = int(round(drift_frac * count))
-    for e in range(1, epoch + 1):
-        dh = hash_at(key, STREAM_DRIFT, layer, b, head, cur, 2 * e)
-        drop = set(cur[np.argsort(dh, kind="stable")[:n_move]].tolist())
-        keep = [p for p in cur.tolist() if p not in drop]
-        nh = hash_at(key, STREAM_DRIFT, layer, b, head, pos, 2 * e + 1)
-        order = np.argsort(nh, kind="stable")
-        taken = set(cur.tolist())
-        new = []
-        for p in order.tolist():
-            if p not in taken:
-                new.append(p)
-                if len(new) == n_move:
-                    break
-        cur = np.sort(np.array(keep + new, dtype=np.int64))
-    return cur
+    """Heavy-hitter positions of one unit at one epoch (see hh_epochs)."""
+    return hh_epochs(key, layer, b, head, ctx, epoch + 1, count, drift_frac)[epoch]
 
 
 def hh_bitmap(positions_per_unit, cap: int) -> np.ndarray:

@@ -47,11 +47,16 @@ class HostWorkload:
         c = self.cfg
         return (layer * c.batch + b) * c.n_kv_heads + kvh
 
+    def n_epochs(self) -> int:
+        """Heavy-hitter epochs a run can reach (one more per boundary token)."""
+        return 1 + int(self.masks.sum(axis=1).max()) if self.cfg.drift else 1
+
     def hh_positions(self, layer: int, b: int, kvh: int, epoch: int = 0) -> np.ndarray:
-        k = (layer, b, kvh, epoch)
-        if k not in self._hh:
-            self._hh[k] = gen.hh_positions(self.key, layer, b, kvh, self.cfg.ctx, epoch)
-        return self._hh[k]
+        k = (layer, b, kvh)
+        if k not in self._hh or len(self._hh[k]) <= epoch:
+            self._hh[k] = gen.hh_epochs(self.key, layer, b, kvh, self.cfg.ctx,
+                                        max(epoch + 1, self.n_epochs()))
+        return self._hh[k][epoch]
 
     # -- content --------------------------------------------------------------------------
     def rows(self, which: str, layer: int, b: int, kvh: int, positions, epoch: int = 0):
