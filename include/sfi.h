@@ -191,6 +191,31 @@ sfi_status sfi_sparse_decode_attn(const sfi_kv_cache *kv, const sfi_sparse_mem *
                                   size_t ws_bytes, void *stream);
 
 /*
+ * The fast step for callers that cannot allocate device memory. The paper has no
+ * counterpart of this call: it is an interface convenience. Some callers get only their
+ * input and output buffers (for example a plug-in inside a host framework that owns all
+ * device memory), or run a decode loop that must never call cudaMalloc because it may
+ * synchronise the device; they cannot provide the workspace that sfi_sparse_decode_attn
+ * needs.
+ *
+ * Same computation, arguments and layouts as sfi_sparse_decode_attn, minus the workspace.
+ * The split-KV scratch (partials and per-unit tickets, about 2.1 MiB) lives in a fixed-size
+ * device array inside the library, held by every GPU that loads the library until the
+ * process exits. Limits: at most 16384 units (n_layers * batch * n_kv_heads), otherwise
+ * SFI_ERR_CAPACITY and nothing is launched; at most 256 CTAs are used. The call allocates
+ * nothing and calls no allocating routine; it clears the tickets it uses with an
+ * asynchronous memset on `stream`.
+ *
+ * The first call on a device looks up the array's device address (once per device, with
+ * that device current); make that first call before any stream capture. All calls share
+ * the one array: calls whose execution overlaps on the GPU (different streams, or
+ * different host threads without ordering) race and give wrong results.
+ */
+sfi_status sfi_sparse_decode_attn_static(const sfi_kv_cache *kv, const sfi_sparse_mem *mem,
+                                         const sfi_budget *budget, const void *q, void *out,
+                                         int32_t out_fp32, const uint8_t *active, void *stream);
+
+/*
  * Trigger policy (summary 2C), host only: slow[t] = 1 when t == 0, when mask[t - 1] != 0
  * (the previous token is a boundary token), or when t_max > 0 steps have passed since the
  * last slow step. mask, slow: host uint8 [steps].

@@ -29,8 +29,8 @@ SFI_DEVERR_LENGTH = 0x8
 ENTRY_POINTS = (
     "sfi_status_string", "sfi_version", "sfi_workspace_bytes", "sfi_workspace_init",
     "sfi_append_kv", "sfi_dense_decode_attn", "sfi_select", "sfi_compact",
-    "sfi_sparse_decode_attn", "sfi_schedule", "sfi_decode_run", "sfi_read_error",
-    "sfi_clear_error",
+    "sfi_sparse_decode_attn", "sfi_sparse_decode_attn_static", "sfi_schedule",
+    "sfi_decode_run", "sfi_read_error", "sfi_clear_error",
 )
 
 
@@ -90,6 +90,7 @@ def lib():
             "sfi_select": (C.c_int, [KV, P, BD, MEM, P, P]),
             "sfi_compact": (C.c_int, [KV, BD, MEM, P, P]),
             "sfi_sparse_decode_attn": (C.c_int, [KV, MEM, BD, P, P, I32, P, P, SZ, P]),
+            "sfi_sparse_decode_attn_static": (C.c_int, [KV, MEM, BD, P, P, I32, P, P]),
             "sfi_schedule": (C.c_int, [I32, P, I32, P]),
             "sfi_decode_run": (C.c_int, [KV, BD, MEM, C.POINTER(SfiDecodePlan), P, SZ, P]),
             "sfi_read_error": (C.c_int, [KV, C.POINTER(C.c_uint32), P]),
@@ -176,6 +177,15 @@ def sfi_sparse_decode_attn(kv: SfiKvCache, mem: SfiSparseMem, budget: SfiBudget,
     _check("sfi_sparse_decode_attn", lib().sfi_sparse_decode_attn(
         C.byref(kv), C.byref(mem), C.byref(budget), _ptr(q), _ptr(out), 1 if out_fp32 else 0,
         _ptr(active), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def sfi_sparse_decode_attn_static(kv: SfiKvCache, mem: SfiSparseMem, budget: SfiBudget, q, out,
+                                  out_fp32: bool, active=None, stream=None):
+    """The fast step without a workspace: its scratch is a fixed device array inside the
+    library (for callers that cannot allocate device memory). Overlapping calls race."""
+    _check("sfi_sparse_decode_attn_static", lib().sfi_sparse_decode_attn_static(
+        C.byref(kv), C.byref(mem), C.byref(budget), _ptr(q), _ptr(out), 1 if out_fp32 else 0,
+        _ptr(active), _stream(stream)))
 
 
 def sfi_schedule(mask, t_max: int):

@@ -394,6 +394,51 @@ sfi_status sfi_sparse_decode_attn(const sfi_kv_cache *kv, const sfi_sparse_mem *
                        nullptr);
 }
 
+sfi_status sfi_sparse_decode_attn_static(const sfi_kv_cache *kv, const sfi_sparse_mem *mem,
+                                         const sfi_budget *budget, const void *q, void *out,
+                                         int32_t out_fp32, const uint8_t *active, void *stream)
+{
+    sfi_status st = check_kv(kv);
+    if (st != SFI_OK)
+        return st;
+    if ((st = check_budget(budget)) != SFI_OK)
+        return st;
+    if (!mem || !mem->kc || !mem->vc || !mem->sel_cnt || !mem->rows || !q || !out ||
+        !aligned16(q) || !aligned16(mem->kc) || !aligned16(mem->vc))
+        return SFI_ERR_INVALID_ARG;
+    const long long units = 1LL * kv->n_layers * kv->batch * kv->n_kv_heads;
+    if (units > kStaticMaxUnits)
+        return SFI_ERR_CAPACITY;  // beyond the static scratch: use sfi_sparse_decode_attn
+    const int sms = sm_count();
+    if (sms <= 0)
+        return SFI_ERR_CUDA;
+    AttnParams p;
+    fill_common(p, kv, active);
+    p.out = out;
+    p.out_fp32 = out_fp32 ? 1 : 0;
+    p.comp_rows = mem->rows;
+    p.sel_cnt = mem->sel_cnt;
+    p.comp_cap = budget->n_sink + budget->n_select;
+    p.n_window = budget->n_window;
+    p.n_cbox = (p.comp_cap + 63) / 64;
+    p.n_wbox = (budget->n_window + 15) / 16 + (kv->page_size ? 1 : 0);
+    p.tiles_per_unit = (64 * p.n_cbox + 16 * p.n_wbox + kTile - 1) / kTile;
+    const int g = p.group;
+    CUtensorMap tk, tv, tq, tkc, tvc;
+    if (!make_map(&tk, kv->k, cache_rows(kv), 16u) || !make_map(&tv, kv->v, cache_rows(kv), 16u) ||
+        !make_map(&tq, q, static_cast<uint64_t>(units) * g, static_cast<uint32_t>(g)) ||
+        !make_map(&tkc, mem->kc, static_cast<uint64_t>(units) * p.comp_cap, 64u) ||
+        !make_map(&tvc, mem->vc, static_cast<uint64_t>(units) * p.comp_cap, 64u))
+        return SFI_ERR_CUDA;
+    long long grid = units * p.tiles_per_unit;
+    if (grid > sms)
+        grid = sms;
+    if (grid > kStaticMaxCtas)
+        grid = kStaticMaxCtas;
+    return launch_status(launch_sparse_static(g, tk, tv, tq, tkc, tvc, p, static_cast<int>(units),
+                                              static_cast<int>(grid), as_stream(stream)));
+}
+
 sfi_status sfi_schedule(int32_t steps, const uint8_t *mask, int32_t t_max, uint8_t *slow)
 {
     if (steps < 0 || (steps > 0 && (!mask || !slow)))

@@ -21,6 +21,8 @@
 //     CTA's copies and MMAs, frees TMEM and returns.
 #include <math.h>
 
+#include <mutex>
+
 #include "sfi_device.cuh"
 
 namespace sfi {
@@ -766,6 +768,71 @@ cudaError_t launch_evidence(const float *zbuf, const float2 *stats, float *f, co
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------
+// Fast step without a caller workspace.
+//
+// Some callers cannot allocate device memory at all -- for example a host framework that
+// hands a plug-in only its input and output buffers, or a real-time decode loop that must
+// never call cudaMalloc (it can synchronise the device). For them the fast step keeps its
+// split-KV scratch (partials and tickets) in this file-scope array, which every GPU that
+// loads the library holds until the process exits. In host code the array's name is only
+// a host-side stand-in, so its device address is looked up once per device.
+
+constexpr size_t kStaticPartialBytes =
+    static_cast<size_t>(2) * kStaticMaxCtas * kPartialFloats(8) * sizeof(float);
+constexpr size_t kStaticScratchBytes = kStaticPartialBytes + kStaticMaxUnits * sizeof(int);
+
+static __device__ __align__(256) unsigned char g_sfi_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void *g_static_addr[kMaxDevices] = {};
+
+// Device address of g_sfi_static_scratch on the current device (set up on first use).
+cudaError_t static_scratch(void **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (g_static_addr[dev] == nullptr) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_sfi_static_scratch);
+        if (e != cudaSuccess)
+            return e;
+        g_static_addr[dev] = ptr;
+    }
+    *out = g_static_addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_static(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                 const CUtensorMap &tm_q, const CUtensorMap &tm_kc,
+                                 const CUtensorMap &tm_vc, AttnParams p, int units, int grid,
+                                 cudaStream_t stream)
+{
+    if (units > kStaticMaxUnits || grid > kStaticMaxCtas || group > 8)
+        return cudaErrorInvalidValue;
+    void *base = nullptr;
+    cudaError_t e = static_scratch(&base);
+    if (e != cudaSuccess)
+        return e;
+    p.partials = static_cast<float *>(base);
+    p.tickets = reinterpret_cast<int *>(static_cast<unsigned char *>(base) + kStaticPartialBytes);
+    // The tickets must start at zero; the array keeps whatever the previous call left.
+    e = cudaMemsetAsync(p.tickets, 0, static_cast<size_t>(units) * sizeof(int), stream);
+    if (e != cudaSuccess)
+        return e;
+    return launch_attention(false, group, tm_k, tm_v, tm_q, tm_kc, tm_vc, p, grid, stream);
 }
 
 }  // namespace sfi

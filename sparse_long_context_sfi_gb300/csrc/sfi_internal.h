@@ -77,4 +77,15 @@ cudaError_t launch_compact(const void *k, const void *v, void *kc, void *vc,
 
 size_t attention_smem_bytes();
 
+// Fast-step attention with its split-KV scratch in a library-owned device array instead of
+// a caller workspace (see sfi_sparse_decode_attn_static). p.partials and p.tickets are
+// filled in here. Limits: at most kStaticMaxUnits units; the grid is capped at
+// kStaticMaxCtas CTAs.
+constexpr int kStaticMaxCtas = 256;
+constexpr int kStaticMaxUnits = 16384;
+cudaError_t launch_sparse_static(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                 const CUtensorMap &tm_q, const CUtensorMap &tm_kc,
+                                 const CUtensorMap &tm_vc, AttnParams p, int units, int grid,
+                                 cudaStream_t stream);
+
 }  // namespace sfi
