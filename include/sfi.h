@@ -223,6 +223,15 @@ sfi_status sfi_sparse_decode_attn_static(const sfi_kv_cache *kv, const sfi_spars
 sfi_status sfi_schedule(int32_t steps, const uint8_t *mask, int32_t t_max, uint8_t *slow);
 
 /*
+ * Trigger policy on the generated tokens (summary 2C: a slow step follows a trigger token
+ * such as '.', '?', '!' or a newline), host only: slow[t] = 1 when t == 0, when
+ * tokens[t - 1] is one of the n_trigger ids in trigger_ids, or when t_max > 0 steps have
+ * passed since the last slow step. tokens: host int32 [steps]; slow: host uint8 [steps].
+ */
+sfi_status sfi_schedule_tokens(int32_t steps, const int32_t *tokens, const int32_t *trigger_ids,
+                               int32_t n_trigger, int32_t t_max, uint8_t *slow);
+
+/*
  * A whole decode run on one stream (blog "How SFI Works": the two-speed loop). For each
  * step t: sfi_append_kv with row t of k_new/v_new; then, for the sequences whose slow flag
  * is set, sfi_dense_decode_attn (with evidence) -> sfi_select -> sfi_compact, and for the

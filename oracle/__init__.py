@@ -45,6 +45,8 @@ def load(path: str | None = None):
     lib.sfi_oracle_sparse_rows.argtypes = [i32, i32, i32, i32, P, i32, P]
     lib.sfi_oracle_schedule.argtypes = [i32, P, i32, P]
     lib.sfi_oracle_schedule.restype = None
+    lib.sfi_oracle_schedule_tokens.argtypes = [i32, P, P, i32, i32, P]
+    lib.sfi_oracle_schedule_tokens.restype = None
     lib.sfi_oracle_attend_batch.argtypes = [i32, i32, i32, i32, P, P, P, P, i32, P, P, P, i32]
     return lib
 
@@ -147,6 +149,15 @@ def schedule(mask, t_max):
     mask = _c(mask, np.uint8)
     slow = np.zeros(mask.shape[0], dtype=np.uint8)
     lib().sfi_oracle_schedule(mask.shape[0], _p(mask), t_max, _p(slow))
+    return slow
+
+
+def schedule_tokens(tokens, trigger_ids, t_max):
+    tokens = _c(tokens, np.int32)
+    trig = _c(trigger_ids, np.int32)
+    slow = np.zeros(tokens.shape[0], dtype=np.uint8)
+    lib().sfi_oracle_schedule_tokens(tokens.shape[0], _p(tokens), _p(trig), trig.shape[0], t_max,
+                                     _p(slow))
     return slow
 
 

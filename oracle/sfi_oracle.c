@@ -367,6 +367,29 @@ void sfi_oracle_schedule(int steps, const uint8_t *mask, int t_max, uint8_t *slo
     }
 }
 
+/*
+ * Trigger policy on a token stream ([Sum 2C]: a slow step follows a trigger token such as
+ * '.', '?', '!' or a newline). tokens: host int32 [steps], the token emitted at each step;
+ * trigger_ids: the n_trigger token ids that end a span. Step t is slow when t == 0, when
+ * tokens[t-1] is a trigger id, or when t_max > 0 steps have passed since the last slow step.
+ */
+void sfi_oracle_schedule_tokens(int steps, const int32_t *tokens, const int32_t *trigger_ids,
+                                int n_trigger, int t_max, uint8_t *slow)
+{
+    int last = 0;
+    for (int t = 0; t < steps; ++t) {
+        int trig = 0;
+        if (t > 0)
+            for (int i = 0; i < n_trigger; ++i)
+                if (tokens[t - 1] == trigger_ids[i])
+                    trig = 1;
+        int s = (t == 0) || trig || (t_max > 0 && t - last >= t_max);
+        slow[t] = (uint8_t)s;
+        if (s)
+            last = t;
+    }
+}
+
 /* ------------------------------------------------------------------------------------ */
 /* Batched drivers (independent units on a few threads; no change to the arithmetic)     */
 /* ------------------------------------------------------------------------------------ */

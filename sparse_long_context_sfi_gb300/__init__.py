@@ -30,7 +30,7 @@ ENTRY_POINTS = (
     "sfi_status_string", "sfi_version", "sfi_workspace_bytes", "sfi_workspace_init",
     "sfi_append_kv", "sfi_dense_decode_attn", "sfi_select", "sfi_compact",
     "sfi_sparse_decode_attn", "sfi_sparse_decode_attn_static", "sfi_schedule",
-    "sfi_decode_run", "sfi_read_error", "sfi_clear_error",
+    "sfi_schedule_tokens", "sfi_decode_run", "sfi_read_error", "sfi_clear_error",
 )
 
 
@@ -92,6 +92,7 @@ def lib():
             "sfi_sparse_decode_attn": (C.c_int, [KV, MEM, BD, P, P, I32, P, P, SZ, P]),
             "sfi_sparse_decode_attn_static": (C.c_int, [KV, MEM, BD, P, P, I32, P, P]),
             "sfi_schedule": (C.c_int, [I32, P, I32, P]),
+            "sfi_schedule_tokens": (C.c_int, [I32, P, P, I32, I32, P]),
             "sfi_decode_run": (C.c_int, [KV, BD, MEM, C.POINTER(SfiDecodePlan), P, SZ, P]),
             "sfi_read_error": (C.c_int, [KV, C.POINTER(C.c_uint32), P]),
             "sfi_clear_error": (C.c_int, [KV, P]),
@@ -195,6 +196,18 @@ def sfi_schedule(mask, t_max: int):
     slow = np.zeros(mask.shape[0], dtype=np.uint8)
     _check("sfi_schedule", lib().sfi_schedule(mask.shape[0], mask.ctypes.data, t_max,
                                               slow.ctypes.data))
+    return slow
+
+
+def sfi_schedule_tokens(tokens, trigger_ids, t_max: int):
+    """Trigger policy on a host int32 token stream; returns the uint8 slow-step flags."""
+    import numpy as np
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    trig = np.ascontiguousarray(trigger_ids, dtype=np.int32)
+    slow = np.zeros(tokens.shape[0], dtype=np.uint8)
+    _check("sfi_schedule_tokens", lib().sfi_schedule_tokens(
+        tokens.shape[0], tokens.ctypes.data, trig.ctypes.data, trig.shape[0], t_max,
+        slow.ctypes.data))
     return slow
 
 

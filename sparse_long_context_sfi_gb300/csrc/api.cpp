@@ -515,6 +515,25 @@ sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
     return SFI_OK;
 }
 
+sfi_status sfi_schedule_tokens(int32_t steps, const int32_t *tokens, const int32_t *trigger_ids,
+                               int32_t n_trigger, int32_t t_max, uint8_t *slow)
+{
+    if (steps < 0 || n_trigger < 0 || (steps > 0 && (!tokens || !slow)) ||
+        (n_trigger > 0 && !trigger_ids))
+        return SFI_ERR_INVALID_ARG;
+    int32_t last = 0;
+    for (int32_t t = 0; t < steps; ++t) {
+        bool trig = false;
+        for (int32_t i = 0; t > 0 && i < n_trigger && !trig; ++i)
+            trig = tokens[t - 1] == trigger_ids[i];
+        const bool s = t == 0 || trig || (t_max > 0 && t - last >= t_max);
+        slow[t] = s ? 1 : 0;
+        if (s)
+            last = t;
+    }
+    return SFI_OK;
+}
+
 sfi_status sfi_read_error(const sfi_kv_cache *kv, uint32_t *bits, void *stream)
 {
     if (!kv || !kv->err || !bits)
@@ -532,5 +551,13 @@ sfi_status sfi_clear_error(const sfi_kv_cache *kv, void *stream)
         return SFI_ERR_INVALID_ARG;
     return launch_status(cudaMemsetAsync(kv->err, 0, sizeof(uint32_t), as_stream(stream)));
 }
+
+#ifdef SFI_TRACE
+// Tuning builds only: copy the per-CTA timeline of the last attention launch.
+int sfi_trace_read(unsigned long long *host, int n_ctas)
+{
+    return static_cast<int>(sfi::trace_read(host, n_ctas));
+}
+#endif
 
 }  // extern "C"

@@ -42,6 +42,17 @@ constexpr int kCtrlOff = kPOff + 2 * kOpBytes;
 constexpr int kFlagFirst = 1;   // first tile of a segment (a unit's tiles inside one CTA)
 constexpr int kFlagLast = 2;    // last tile of a segment
 
+// Optional per-CTA timeline for tuning (compile with -DSFI_TRACE): globaltimer stamps at
+// fixed checkpoints, read back through sfi_trace_read. Off in normal builds.
+#ifdef SFI_TRACE
+__device__ unsigned long long g_sfi_trace[1024][16];
+#define SFI_STAMP(slot) (g_sfi_trace[blockIdx.x & 1023][(slot)] = global_timer_ns())
+#define SFI_TRACE_SET(slot, v) (g_sfi_trace[blockIdx.x & 1023][(slot)] = (v))
+#else
+#define SFI_STAMP(slot) ((void)0)
+#define SFI_TRACE_SET(slot, v) ((void)0)
+#endif
+
 struct TileMeta {
     int unit;
     int tile;
@@ -103,6 +114,30 @@ __device__ __forceinline__ void fail(Ctrl &c, uint32_t *err)
     raise_error(err, 0x4u);  // SFI_DEVERR_TIMEOUT
 }
 
+// Set / clear rows [r0, r1) of a 128-row validity mask kept in four registers.
+__device__ __forceinline__ uint32_t word_bits(int r0, int r1, int w)
+{
+    const int lo = min(max(r0 - 32 * w, 0), 32), hi = min(max(r1 - 32 * w, 0), 32);
+    if (hi <= lo)
+        return 0u;
+    const uint32_t upto = hi == 32 ? 0xffffffffu : ((1u << hi) - 1u);
+    return upto & ~((1u << lo) - 1u);
+}
+
+__device__ __forceinline__ void mask_rows(uint32_t (&v)[4], int r0, int r1)
+{
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+        v[w] |= word_bits(r0, r1, w);
+}
+
+__device__ __forceinline__ void clear_rows(uint32_t (&v)[4], int r0, int r1)
+{
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+        v[w] &= ~word_bits(r0, r1, w);
+}
+
 template <int G>
 __device__ __forceinline__ void store_out(const AttnParams &p, int u, int d, const float (&o)[G])
 {
@@ -128,38 +163,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = p.batch, Hkv = p.n_kv_heads;
 
-    // ---- tile space: per-sequence tile counts and this CTA's range --------------------
-    if (tid == 0) {
-        long long acc = 0;
-        for (int b = 0; b < B; ++b) {
-            int L = p.seq_len[b];
-            int act = p.active ? p.active[b] : 1;
-            if (act && (L < 0 || L > p.max_len || L > p.capacity)) {
-                raise_error(p.err, 0x8u);  // SFI_DEVERR_LENGTH
-                act = 0;
-            }
-            int n = 0;
-            if (act && L > 0)
-                n = DENSE ? (L + kTile - 1) / kTile : p.tiles_per_unit;
-            c.nt[b] = n;
-            c.pre[b] = static_cast<int>(acc * Hkv);
-            c.len[b] = L;
-            acc += n;
-        }
-        c.TL = acc * Hkv;
-        c.T = c.TL * p.n_layers;
-        c.P = static_cast<int>(c.T < gridDim.x ? c.T : gridDim.x);
-        c.g0 = static_cast<long long>(blockIdx.x) * c.T / (c.P > 0 ? c.P : 1);
-        c.g1 = static_cast<long long>(blockIdx.x + 1) * c.T / (c.P > 0 ? c.P : 1);
-        c.abort = 0;
-    }
-    __syncthreads();
-    if (static_cast<int>(blockIdx.x) >= c.P)
-        return;
-    const long long g0 = c.g0, g1 = c.g1;
-    const int n_tiles = static_cast<int>(g1 - g0);
-
-    // ---- set-up ----------------------------------------------------------------------
+    // ---- set-up touching no global memory: overlaps the previous kernel's tail ----------
+    pdl_trigger();
+    if (threadIdx.x == 0)
+        SFI_STAMP(0);
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&c.full[s], 1);
@@ -183,6 +190,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tma_prefetch_map(&tm_kc);
             tma_prefetch_map(&tm_vc);
         }
+        c.abort = 0;
     }
     if (warp == 1) {
         tmem_alloc(&c.tmem_base, kTmemCols);
@@ -192,9 +200,69 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int i = tid; i < 4 * kOpBytes / 16; i += kAttnThreads)
         reinterpret_cast<uint4 *>(smem + kQOff)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
+
+    // ---- tile space: per-sequence tile counts and this CTA's range --------------------
+    pdl_wait();
+    if (threadIdx.x == 0)
+        SFI_STAMP(1);
+    for (int b = tid; b < B; b += kAttnThreads) {
+        const int L = p.seq_len[b];
+        int act = p.active ? p.active[b] : 1;
+        if (act && (L < 0 || L > p.max_len || L > p.capacity)) {
+            raise_error(p.err, 0x8u);  // SFI_DEVERR_LENGTH
+            act = 0;
+        }
+        c.nt[b] = (act && L > 0) ? (DENSE ? (L + kTile - 1) / kTile : p.tiles_per_unit) : 0;
+        c.len[b] = L;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        long long acc = 0;
+        for (int b = 0; b < B; ++b) {
+            c.pre[b] = static_cast<int>(acc * Hkv);
+            acc += c.nt[b];
+        }
+        c.TL = acc * Hkv;
+        c.T = c.TL * p.n_layers;
+        c.P = static_cast<int>(c.T < gridDim.x ? c.T : gridDim.x);
+        const long long P = c.P > 0 ? c.P : 1;
+        if (DENSE) {
+            // stream-K: equal contiguous tile ranges (balances ragged lengths)
+            c.g0 = static_cast<long long>(blockIdx.x) * c.T / P;
+            c.g1 = static_cast<long long>(blockIdx.x + 1) * c.T / P;
+        } else {
+            // every unit has the same tile count: ranges never straddle two units
+            const long long nt = p.tiles_per_unit, ua = c.T / nt, cta = blockIdx.x;
+            if (P >= ua) {
+                const long long q = P / ua, r = P % ua;
+                long long a, k, nc;
+                if (cta < r * (q + 1)) {
+                    a = cta / (q + 1);
+                    k = cta % (q + 1);
+                    nc = q + 1;
+                } else {
+                    a = r + (cta - r * (q + 1)) / q;
+                    k = (cta - r * (q + 1)) % q;
+                    nc = q;
+                }
+                c.g0 = a * nt + k * nt / nc;
+                c.g1 = a * nt + (k + 1) * nt / nc;
+            } else {
+                c.g0 = (cta * ua / P) * nt;
+                c.g1 = ((cta + 1) * ua / P) * nt;
+            }
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // CTAs beyond the tile count (short contexts) only tear down.
+    const long long g0 = c.g0, g1 = c.g1;
+    const int n_tiles = static_cast<int>(blockIdx.x) < c.P ? static_cast<int>(g1 - g0) : 0;
+    if (tid == 0) {
+        SFI_STAMP(2);
+        SFI_TRACE_SET(12, n_tiles);
+    }
     const uint32_t tmem = c.tmem_base;
 
     if (warp == 0) {
@@ -211,6 +279,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             int kvh = (r - c.pre[b]) / c.nt[b];
             int t = (r - c.pre[b]) - kvh * c.nt[b];
             int seg = -1, issued = 0;
+            int seg_len = 0, seg_rows_c = 0, seg_ws = 0;
             for (int i = 0; i < n_tiles; ++i, ++g) {
                 if (i > 0 && ++t == c.nt[b]) {
                     t = 0;
@@ -244,111 +313,117 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 mt.unit = u;
                 mt.tile = t;
                 mt.flags = (first ? kFlagFirst : 0) | (last ? kFlagLast : 0);
+                if (first) {
+                    // per-unit quantities, read once per segment
+                    seg_len = c.len[b];
+                    if (!DENSE) {
+                        const int rows_c = max(0, min(__ldg(p.comp_rows + u), p.comp_cap));
+                        const int n_s = max(0, rows_c - max(0, __ldg(p.sel_cnt + u)));
+                        seg_rows_c = rows_c;
+                        seg_ws = max(n_s, seg_len - p.n_window);
+                    }
+                }
                 uint32_t valid[4] = {0u, 0u, 0u, 0u};
-                uint32_t bytes = first ? 2u * G * 128u : 0u;
-                const int L = c.len[b];
-                // Box plan for this tile: up to 8 boxes of 16 rows, or fewer larger boxes.
-                struct Box { const CUtensorMap *mk, *mv; int y; int row0; int rows; };
-                Box box[8];
-                int nbox = 0;
+                uint64_t *bar = &c.full[s];
+                auto issue = [&](const CUtensorMap *mk, const CUtensorMap *mv, int y, int row0,
+                                 int rows) {
+                    mbar_expect_tx(bar, 4u * static_cast<uint32_t>(rows) * 128u);
+                    uint8_t *dk = st + row0 * 128;
+                    uint8_t *dv = dk + 2 * kChunkBytes;
+                    if (DENSE) {  // streamed once per slow step: do not displace reusable lines
+                        tma_load_2d_hint(dk, mk, bar, 0, y, pol);
+                        tma_load_2d_hint(dk + kChunkBytes, mk, bar, 64, y, pol);
+                        tma_load_2d_hint(dv, mv, bar, 0, y, pol);
+                        tma_load_2d_hint(dv + kChunkBytes, mv, bar, 64, y, pol);
+                    } else {
+                        tma_load_2d(dk, mk, bar, 0, y);
+                        tma_load_2d(dk + kChunkBytes, mk, bar, 64, y);
+                        tma_load_2d(dv, mv, bar, 0, y);
+                        tma_load_2d(dv + kChunkBytes, mv, bar, 64, y);
+                    }
+                };
+                if (first) {
+                    mbar_expect_tx(bar, 2u * G * 128u);
+                    uint8_t *qb = smem + kQOff + (seg & 1) * kOpBytes;
+                    tma_load_2d(qb, &tm_q, bar, 0, u * G);
+                    tma_load_2d(qb + kOpChunk, &tm_q, bar, 64, u * G);
+                }
+                const int L = seg_len;
                 if (DENSE) {
                     const int pos0 = t * kTile;
                     const int nvalid = min(kTile, L - pos0);
-                    for (int rr = 0; rr < nvalid; ++rr)
-                        valid[rr >> 5] |= 1u << (rr & 31);
+                    mask_rows(valid, 0, nvalid);
                     if (p.page_size == 0) {
-                        box[nbox++] = {&tm_k, &tm_v, u * p.capacity + pos0, 0, kTile};
+                        issue(&tm_k, &tm_v, u * p.capacity + pos0, 0, kTile);
                     } else {
-                        for (int q = 0; q * 16 < nvalid; ++q) {
-                            const int lp = (pos0 >> 4) + q;
-                            const int page = p.page_table[b * p.max_pages + lp];
-                            if (page < 0 || page >= p.n_pages) {
+                        const int *pt = p.page_table + b * p.max_pages + (pos0 >> 4);
+                        int page[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            page[q] = (16 * q < nvalid) ? __ldg(pt + q) : 0;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            if (16 * q >= nvalid)
+                                continue;
+                            if (page[q] < 0 || page[q] >= p.n_pages) {
                                 raise_error(p.err, 0x1u);
-                                for (int rr = 16 * q; rr < 16 * q + 16; ++rr)
-                                    valid[rr >> 5] &= ~(1u << (rr & 31));
+                                clear_rows(valid, 16 * q, 16 * q + 16);
                                 continue;
                             }
-                            box[nbox++] = {&tm_k, &tm_v,
-                                           ((layer * p.n_pages + page) * Hkv + kvh) * 16, 16 * q, 16};
+                            issue(&tm_k, &tm_v, ((layer * p.n_pages + page[q]) * Hkv + kvh) * 16,
+                                  16 * q, 16);
                         }
                     }
                 } else {
-                    const int rows_c = max(0, min(p.comp_rows[u], p.comp_cap));
-                    const int n_s = max(0, rows_c - max(0, p.sel_cnt[u]));
-                    const int ws = max(n_s, L - p.n_window);
+#pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
                         const int R = t * kTile + 64 * h2;
                         if (R < 64 * p.n_cbox) {
                             const int k = R >> 6;
-                            const int vr = max(0, min(64, rows_c - 64 * k));
+                            const int vr = max(0, min(64, seg_rows_c - 64 * k));
                             if (vr > 0) {
-                                box[nbox++] = {&tm_kc, &tm_vc, u * p.comp_cap + 64 * k, 64 * h2, 64};
-                                for (int rr = 0; rr < vr; ++rr)
-                                    valid[(64 * h2 + rr) >> 5] |= 1u << ((64 * h2 + rr) & 31);
+                                issue(&tm_kc, &tm_vc, u * p.comp_cap + 64 * k, 64 * h2, 64);
+                                mask_rows(valid, 64 * h2, 64 * h2 + vr);
                             }
                             continue;
                         }
+#pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const int j = (R + 16 * q - 64 * p.n_cbox) >> 4;
                             if (j >= p.n_wbox)
                                 break;
                             const int row0 = 64 * h2 + 16 * q;
                             if (p.page_size == 0) {
-                                const int p0 = ws + 16 * j;
+                                const int p0 = seg_ws + 16 * j;
                                 const int vr = max(0, min(16, L - p0));
                                 if (vr == 0)
                                     continue;
-                                box[nbox++] = {&tm_k, &tm_v, u * p.capacity + p0, row0, 16};
-                                for (int rr = 0; rr < vr; ++rr)
-                                    valid[(row0 + rr) >> 5] |= 1u << ((row0 + rr) & 31);
+                                issue(&tm_k, &tm_v, u * p.capacity + p0, row0, 16);
+                                mask_rows(valid, row0, row0 + vr);
                             } else {
-                                const int lp = (ws >> 4) + j;
-                                const int p0 = lp * 16;
-                                uint32_t m = 0;
-                                for (int rr = 0; rr < 16; ++rr)
-                                    if (p0 + rr >= ws && p0 + rr < L)
-                                        m |= 1u << rr;
-                                if (m == 0)
+                                const int lp = (seg_ws >> 4) + j;
+                                const int r0 = max(seg_ws - lp * 16, 0);
+                                const int r1 = min(L - lp * 16, 16);
+                                if (r1 <= r0)
                                     continue;
-                                const int page = p.page_table[b * p.max_pages + lp];
+                                const int page = __ldg(p.page_table + b * p.max_pages + lp);
                                 if (page < 0 || page >= p.n_pages) {
                                     raise_error(p.err, 0x1u);
                                     continue;
                                 }
-                                box[nbox++] = {&tm_k, &tm_v,
-                                               ((layer * p.n_pages + page) * Hkv + kvh) * 16, row0, 16};
-                                for (int rr = 0; rr < 16; ++rr)
-                                    if (m & (1u << rr))
-                                        valid[(row0 + rr) >> 5] |= 1u << ((row0 + rr) & 31);
+                                issue(&tm_k, &tm_v, ((layer * p.n_pages + page) * Hkv + kvh) * 16,
+                                      row0, 16);
+                                mask_rows(valid, row0 + r0, row0 + r1);
                             }
                         }
                     }
                 }
+#pragma unroll
                 for (int w = 0; w < 4; ++w)
                     mt.valid[w] = valid[w];
-                for (int k = 0; k < nbox; ++k)
-                    bytes += 4u * static_cast<uint32_t>(box[k].rows) * 128u;
-                mbar_arrive_expect_tx(&c.full[s], bytes);
-                if (first) {
-                    uint8_t *qb = smem + kQOff + (seg & 1) * kOpBytes;
-                    tma_load_2d(qb, &tm_q, &c.full[s], 0, u * G);
-                    tma_load_2d(qb + kOpChunk, &tm_q, &c.full[s], 64, u * G);
-                }
-                for (int k = 0; k < nbox; ++k) {
-                    uint8_t *dk = st + box[k].row0 * 128;
-                    uint8_t *dv = dk + 2 * kChunkBytes;
-                    if (DENSE) {  // streamed once per slow step: do not displace reusable lines
-                        tma_load_2d_hint(dk, box[k].mk, &c.full[s], 0, box[k].y, pol);
-                        tma_load_2d_hint(dk + kChunkBytes, box[k].mk, &c.full[s], 64, box[k].y, pol);
-                        tma_load_2d_hint(dv, box[k].mv, &c.full[s], 0, box[k].y, pol);
-                        tma_load_2d_hint(dv + kChunkBytes, box[k].mv, &c.full[s], 64, box[k].y, pol);
-                    } else {
-                        tma_load_2d(dk, box[k].mk, &c.full[s], 0, box[k].y);
-                        tma_load_2d(dk + kChunkBytes, box[k].mk, &c.full[s], 64, box[k].y);
-                        tma_load_2d(dv, box[k].mv, &c.full[s], 0, box[k].y);
-                        tma_load_2d(dv + kChunkBytes, box[k].mv, &c.full[s], 64, box[k].y);
-                    }
-                }
+                mbar_arrive(bar);  // releases the metadata; completes with the copies
+                if (i == 0)
+                    SFI_STAMP(3);
                 ++issued;
             }
             // Never leave a copy in flight into shared memory we are about to give up.
@@ -387,6 +462,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     ok = false;
                     break;
                 }
+                if (i == 0)
+                    SFI_STAMP(4);
                 const int flags = c.meta[s].flags;
                 if (flags & kFlagFirst)
                     ++seg;
@@ -441,8 +518,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const long long su = layer * c.TL + c.pre[b] + static_cast<long long>(kvh) * c.nt[b];
             const long long eu = su + c.nt[b];
             const long long P = c.P, T = c.T;
-            const int cf = static_cast<int>(((su + 1) * P - 1) / T);
-            const int cl = static_cast<int>((eu * P - 1) / T);
+            int cf, cl;
+            if (DENSE) {  // stream-K: the CTAs whose ranges meet [su, eu)
+                cf = static_cast<int>(((su + 1) * P - 1) / T);
+                cl = static_cast<int>((eu * P - 1) / T);
+            } else {      // unit-aligned ranges: the unit's own group of CTAs
+                const long long nt = p.tiles_per_unit, ua = T / nt, a = su / nt;
+                if (P >= ua) {
+                    const long long q = P / ua, r = P % ua;
+                    cf = static_cast<int>(a < r ? a * (q + 1) : r * (q + 1) + (a - r) * q);
+                    cl = cf + static_cast<int>(a < r ? q + 1 : q) - 1;
+                } else {
+                    cf = cl = static_cast<int>(blockIdx.x);
+                }
+            }
             float o[G];
             if (cf == cl) {
 #pragma unroll
@@ -463,46 +552,69 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 part[G * kHeadDim + G + row] = fle[row];
                 part[G * kHeadDim + 2 * G + row] = flr[row];
             }
-            __threadfence();
+            // Every thread's partial writes happen before thread 0's release fence (group
+            // barrier), which publishes them before the ticket; the last contributor's
+            // acquire fence and the second barrier make all partials visible to its threads.
             if (!group_sync(c, gphase, lane))
                 return false;
             if (row == 0) {
+                fence_acq_rel_gpu();
                 const int tk = atomicAdd(&p.tickets[u], 1);
                 const int is_last = (tk == cl - cf) ? 1 : 0;
-                if (is_last)
+                if (is_last) {
                     p.tickets[u] = 0;
+                    fence_acq_rel_gpu();
+                }
                 c.last_flag = is_last;
             }
             if (!group_sync(c, gphase, lane))
                 return false;
             if (!c.last_flag)
                 return true;
-            __threadfence();
+            // One-pass online merge starting from this CTA's own partial (in registers);
+            // the other contributors are read four at a time so their loads overlap.
             float M[G], Le[G], Lr[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                M[h] = -INFINITY;
-                Le[h] = Lr[h] = o[h] = 0.f;
+                M[h] = fm[h];
+                Le[h] = fle[h];
+                Lr[h] = flr[h];
+                o[h] = acc[h];
             }
-            for (int cc = cf; cc <= cl; ++cc) {
-                const long long start = static_cast<long long>(cc) * T / P;
-                const int sl = (cc == cf && start < su) ? 1 : 0;
-                const float *pc = p.partials + (2 * static_cast<size_t>(cc) + sl) * kPartialFloats(G);
+            // under stream-K, u may be the last segment of cf (slot 1); unit-aligned ranges
+            // hold one segment each (slot 0)
+            const bool cf_tail = DENSE && static_cast<long long>(cf) * T / P < su;
+            for (int c0 = cf; c0 <= cl; c0 += 4) {
+                float mc[4][G], lc[4][G], rc[4][G], ac[4][G];
+                bool use[4];
 #pragma unroll
-                for (int h = 0; h < G; ++h)
-                    M[h] = fmaxf(M[h], __ldcg(pc + G * kHeadDim + h));
-            }
-            for (int cc = cf; cc <= cl; ++cc) {
-                const long long start = static_cast<long long>(cc) * T / P;
-                const int sl = (cc == cf && start < su) ? 1 : 0;
-                const float *pc = p.partials + (2 * static_cast<size_t>(cc) + sl) * kPartialFloats(G);
+                for (int k = 0; k < 4; ++k) {
+                    const int cc = c0 + k;
+                    use[k] = cc <= cl && cc != static_cast<int>(blockIdx.x);
+                    const int sl = (cc == cf && cf_tail) ? 1 : 0;
+                    const float *pc = p.partials +
+                                      (2 * static_cast<size_t>(use[k] ? cc : blockIdx.x) + sl) *
+                                          kPartialFloats(G);
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float mc = __ldcg(pc + G * kHeadDim + h);
-                    const float w = (M[h] == -INFINITY) ? 0.f : exp2f(mc - M[h]);
-                    Le[h] += w * __ldcg(pc + G * kHeadDim + G + h);
-                    Lr[h] += w * __ldcg(pc + G * kHeadDim + 2 * G + h);
-                    o[h] += w * __ldcg(pc + h * kHeadDim + row);
+                    for (int h = 0; h < G; ++h) {
+                        mc[k][h] = use[k] ? __ldcg(pc + G * kHeadDim + h) : -INFINITY;
+                        lc[k][h] = use[k] ? __ldcg(pc + G * kHeadDim + G + h) : 0.f;
+                        rc[k][h] = use[k] ? __ldcg(pc + G * kHeadDim + 2 * G + h) : 0.f;
+                        ac[k][h] = use[k] ? __ldcg(pc + h * kHeadDim + row) : 0.f;
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        const float mn = fmaxf(M[h], mc[k][h]);
+                        const float a = (M[h] == -INFINITY) ? 0.f : exp2f(M[h] - mn);
+                        const float w = (mc[k][h] == -INFINITY) ? 0.f : exp2f(mc[k][h] - mn);
+                        Le[h] = Le[h] * a + w * lc[k][h];
+                        Lr[h] = Lr[h] * a + w * rc[k][h];
+                        o[h] = o[h] * a + w * ac[k][h];
+                        M[h] = mn;
+                    }
                 }
             }
 #pragma unroll
@@ -528,8 +640,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int h = 0; h < G; ++h)
                 acc[h] = (a_flags & kFlagFirst) ? ov[h] : fmaf(acc[h], a_alpha[h], ov[h]);
             if (a_flags & kFlagLast) {
+                if (row == 0)
+                    SFI_STAMP(6);
                 if (!finalize(a_unit, a_m, a_le, a_lr))
                     return false;
+                if (row == 0)
+                    SFI_STAMP(7);
 #pragma unroll
                 for (int h = 0; h < G; ++h)
                     acc[h] = 0.f;
@@ -544,6 +660,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 ok = false;
                 break;
             }
+            if (i == 0 && row == 0)
+                SFI_STAMP(5);
             const int u = c.meta[s].unit;
             const int tile = c.meta[s].tile;
             const int flags = c.meta[s].flags;
@@ -658,8 +776,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             a_unit = u;
             (void)tile;
         }
+        if (row == 0)
+            SFI_STAMP(8);
         if (ok && n_tiles > 0 && !correct(n_tiles - 1))
             ok = false;
+        if (row == 0)
+            SFI_STAMP(9);
         if (!ok)
             fail(c, p.err);
     }
@@ -669,6 +791,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+        if (lane == 0)
+            SFI_STAMP(10);
     }
 }
 
@@ -682,6 +806,8 @@ __global__ void __launch_bounds__(256) evidence_kernel(const float *__restrict__
                                                        const uint8_t *__restrict__ active,
                                                        int batch, int n_kv_heads, int capacity)
 {
+    pdl_trigger();
+    pdl_wait();
     const int u = blockIdx.y;
     const int b = (u / n_kv_heads) % batch;
     if (active && !active[b])
@@ -724,8 +850,9 @@ cudaError_t launch_attn_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, cons
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess)
         return e;
-    kern<<<grid, kAttnThreads, kSmemBytes, stream>>>(tm_k, tm_v, tm_q, tm_kc, tm_vc, p);
-    return cudaGetLastError();
+    e = launch_pdl(kern, dim3(grid), dim3(kAttnThreads), kSmemBytes, stream, tm_k, tm_v, tm_q, tm_kc,
+                   tm_vc, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -761,10 +888,10 @@ cudaError_t launch_evidence(const float *zbuf, const float2 *stats, float *f, co
     if (grid.x == 0)
         grid.x = 1;
     switch (group) {
-    case 1: evidence_kernel<1><<<grid, 256, 0, stream>>>(zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity); break;
-    case 2: evidence_kernel<2><<<grid, 256, 0, stream>>>(zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity); break;
-    case 4: evidence_kernel<4><<<grid, 256, 0, stream>>>(zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity); break;
-    case 8: evidence_kernel<8><<<grid, 256, 0, stream>>>(zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity); break;
+    case 1: return launch_pdl(evidence_kernel<1>, grid, dim3(256), 0, stream, zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity);
+    case 2: return launch_pdl(evidence_kernel<2>, grid, dim3(256), 0, stream, zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity);
+    case 4: return launch_pdl(evidence_kernel<4>, grid, dim3(256), 0, stream, zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity);
+    case 8: return launch_pdl(evidence_kernel<8>, grid, dim3(256), 0, stream, zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity);
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -834,5 +961,12 @@ cudaError_t launch_sparse_static(int group, const CUtensorMap &tm_k, const CUten
         return e;
     return launch_attention(false, group, tm_k, tm_v, tm_q, tm_kc, tm_vc, p, grid, stream);
 }
+
+#ifdef SFI_TRACE
+cudaError_t trace_read(unsigned long long *host, int n)
+{
+    return cudaMemcpyFromSymbol(host, g_sfi_trace, sizeof(unsigned long long) * 16 * (n < 1024 ? n : 1024));
+}
+#endif
 
 }  // namespace sfi

@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(256) append_kernel(
 {
     __shared__ int sh_ok, sh_pos, sh_page;
     const int b = blockIdx.x, tid = threadIdx.x;
+    pdl_trigger();
+    pdl_wait();
     if (active && !active[b])
         return;
     if (tid == 0) {
@@ -78,6 +80,8 @@ __global__ void __launch_bounds__(256) compact_kernel(
     const int kvh = u % n_kv_heads;
     const int b = (u / n_kv_heads) % batch;
     const int layer = u / (n_kv_heads * batch);
+    pdl_trigger();
+    pdl_wait();
     if (active && !active[b])
         return;
     const int L = min(seq_len[b], capacity);
@@ -118,11 +122,12 @@ cudaError_t launch_append(const void *k_new, const void *v_new, void *k, void *v
                           int n_kv_heads, int capacity, int page_size, int n_pages, int max_pages,
                           uint32_t *err, cudaStream_t stream)
 {
-    append_kernel<<<batch, 256, 0, stream>>>(
-        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
-        static_cast<uint4 *>(k), static_cast<uint4 *>(v), seq_len, active, page_table, n_layers,
-        batch, n_kv_heads, capacity, page_size, n_pages, max_pages, err);
-    return cudaGetLastError();
+    const cudaError_t e = launch_pdl(
+        append_kernel, dim3(batch), dim3(256), 0, stream, static_cast<const uint4 *>(k_new),
+        static_cast<const uint4 *>(v_new), static_cast<uint4 *>(k), static_cast<uint4 *>(v),
+        seq_len, active, page_table, n_layers, batch, n_kv_heads, capacity, page_size, n_pages,
+        max_pages, err);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_compact(const void *k, const void *v, void *kc, void *vc, const int32_t *sel_idx,
@@ -134,11 +139,12 @@ cudaError_t launch_compact(const void *k, const void *v, void *kc, void *vc, con
     const int units = n_layers * batch * n_kv_heads;
     const int comp_cap = n_sink + n_select;
     dim3 grid(units, (comp_cap + 127) / 128);
-    compact_kernel<<<grid, 256, 0, stream>>>(
-        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), static_cast<uint4 *>(kc),
-        static_cast<uint4 *>(vc), sel_idx, sel_cnt, rows, seq_len, active, page_table, batch,
-        n_kv_heads, capacity, page_size, n_pages, max_pages, n_sink, n_select, err);
-    return cudaGetLastError();
+    const cudaError_t e = launch_pdl(
+        compact_kernel, grid, dim3(256), 0, stream, static_cast<const uint4 *>(k),
+        static_cast<const uint4 *>(v), static_cast<uint4 *>(kc), static_cast<uint4 *>(vc), sel_idx,
+        sel_cnt, rows, seq_len, active, page_table, batch, n_kv_heads, capacity, page_size, n_pages,
+        max_pages, n_sink, n_select, err);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace sfi

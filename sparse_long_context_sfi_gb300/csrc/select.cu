@@ -78,6 +78,8 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p)
     __shared__ uint32_t sh_digit;
     __shared__ int sh_above;
 
+    pdl_trigger();
+    pdl_wait();
     const int u = blockIdx.x;
     const int b = (u / p.n_kv_heads) % p.batch;
     if (p.active && !p.active[b])
@@ -116,17 +118,24 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p)
         for (int i = tid; i < nb; i += NT)
             hist[i] = 0u;
         __syncthreads();
-        for (int base = 0; base < nC; base += NT) {
-            const int i = base + tid;
-            const bool in = i < nC;
-            const uint32_t k = in ? fz.key(i) : 0u;
-            const bool part = in && ((k & pmask) == prefix);
-            const uint32_t digit = (k >> shift) & static_cast<uint32_t>(nb - 1);
-            const unsigned act = __ballot_sync(0xffffffffu, part);
-            if (part) {
-                const unsigned peers = __match_any_sync(act, digit);
-                if (lane == __ffs(peers) - 1)
-                    atomicAdd(&hist[digit], static_cast<uint32_t>(__popc(peers)));
+        for (int base = 0; base < nC; base += 4 * NT) {
+            // four consecutive candidates per thread: their loads are in flight together
+            uint32_t k[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = base + 4 * tid + e;
+                k[e] = i < nC ? fz.key(i) : 0u;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool part = (base + 4 * tid + e < nC) && ((k[e] & pmask) == prefix);
+                const uint32_t digit = (k[e] >> shift) & static_cast<uint32_t>(nb - 1);
+                const unsigned act = __ballot_sync(0xffffffffu, part);
+                if (part) {
+                    const unsigned peers = __match_any_sync(act, digit);
+                    if (lane == __ffs(peers) - 1)
+                        atomicAdd(&hist[digit], static_cast<uint32_t>(__popc(peers)));
+                }
             }
         }
         __syncthreads();
@@ -202,8 +211,8 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p)
 
 cudaError_t launch_select(const SelectParams &p, cudaStream_t stream)
 {
-    select_kernel<<<p.n_units, NT, 0, stream>>>(p);
-    return cudaGetLastError();
+    const cudaError_t e = launch_pdl(select_kernel, dim3(p.n_units), dim3(NT), 0, stream, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace sfi

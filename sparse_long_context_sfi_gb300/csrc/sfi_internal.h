@@ -76,6 +76,9 @@ cudaError_t launch_compact(const void *k, const void *v, void *kc, void *vc,
                            int n_select, uint32_t *err, cudaStream_t stream);
 
 size_t attention_smem_bytes();
+#ifdef SFI_TRACE
+cudaError_t trace_read(unsigned long long *host, int n);
+#endif
 
 // Fast-step attention with its split-KV scratch in a library-owned device array instead of
 // a caller workspace (see sfi_sparse_decode_attn_static). p.partials and p.tickets are

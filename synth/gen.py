@@ -264,6 +264,23 @@ def boundary_mask(key, steps: int, kind: str, param: float, b: int = 0) -> np.nd
         m[t] = 1
 
 
+TRIGGER_TOKENS = (13, 30, 0, 198)   # synthetic ids standing for ".", "?", "!" and newline
+
+
+def token_stream(key, steps: int, vocab: int = 32000, mean_span: float = 18.0, b: int = 0,
+                 trigger_ids=TRIGGER_TOKENS) -> np.ndarray:
+    """int32 [steps] synthetic generated tokens: each token is a trigger id with probability
+    1/mean_span (which one: uniform), otherwise a uniform non-trigger id."""
+    u = uniform01(key, STREAM_MASK, b, np.arange(steps) + (1 << 20))
+    h = hash_at(key, STREAM_MASK, 1, b, 0, np.arange(steps), 1)
+    trig = np.asarray(trigger_ids, np.int64)
+    other = np.setdiff1d(np.arange(vocab), trig)
+    tok = other[(h % np.uint64(other.size)).astype(np.int64)]
+    is_t = u < 1.0 / mean_span
+    tok = np.where(is_t, trig[(h >> np.uint64(32)).astype(np.int64) % trig.size], tok)
+    return tok.astype(np.int32)
+
+
 def page_table(key, lengths_cap, page_size: int):
     """Seeded random page assignment. lengths_cap[b] = positions sequence b may reach.
 

@@ -86,3 +86,14 @@ def test_decode_plan_layout_matches_header(lib):
     assert C.sizeof(sfi.SfiSparseMem) == 5 * 8
     assert sfi.SfiDecodePlan.masks.offset == 64 and sfi.SfiDecodePlan.events.offset == 80
     assert C.sizeof(sfi.SfiDecodePlan) == 88
+
+
+@pytest.mark.parametrize("t_max", [0, 7, 64])
+def test_native_token_scheduler_matches_oracle(lib, t_max):
+    from synth import gen
+    key = gen.key_from_seed(11)
+    trig = np.array(gen.TRIGGER_TOKENS, np.int32)
+    for b in range(5):
+        toks = gen.token_stream(key, 500, b=b, mean_span=9.0)
+        np.testing.assert_array_equal(sfi.sfi_schedule_tokens(toks, trig, t_max),
+                                      oracle.schedule_tokens(toks, trig, t_max))

@@ -24,8 +24,11 @@ MUTANTS = {
     "prior_wrong_sign": ("const float b = c2 * rt;", "const float b = -c2 * rt;"),
     "window_off_by_one": ("int w0 = L_now - W;", "int w0 = L_now - W + 1;"),
     "candidates_include_window": ("const int n = L - W - S;", "const int n = L - S;"),
-    "tmax_strict": ("t - last >= t_max", "t - last > t_max"),
-    "first_step_not_slow": ("int s = (t == 0) ||", "int s = (t < 0) ||"),
+    "tmax_strict": ("mask[t - 1] || (t_max > 0 && t - last >= t_max)",
+                    "mask[t - 1] || (t_max > 0 && t - last > t_max)"),
+    "first_step_not_slow": ("int s = (t == 0) || mask[t - 1]", "int s = (t < 0) || mask[t - 1]"),
+    "token_trigger_off_by_one": ("if (tokens[t - 1] == trigger_ids[i])",
+                                 "if (tokens[t] == trigger_ids[i])"),
 }
 
 PIN_TESTS = [name for name in dir(pins) if name.startswith("test_")]

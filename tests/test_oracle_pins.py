@@ -267,3 +267,19 @@ def test_geometric_mask_gap_mean():
     assert gaps.min() >= 1
     # mean 18, standard deviation sqrt(1 - 1/18) * 18; allow five standard errors
     assert abs(gaps.mean() - 18) < 5 * math.sqrt(1 - 1 / 18) * 18 / math.sqrt(gaps.size)
+
+
+def test_token_schedule_hand_example_and_mask_equivalence():
+    trig = np.array([13, 0], np.int32)
+    toks = np.array([5, 13, 7, 7, 0, 9, 9, 9, 9], np.int32)
+    assert np.flatnonzero(oracle.schedule_tokens(toks, trig, 0)).tolist() == [0, 2, 5]
+    assert np.flatnonzero(oracle.schedule_tokens(toks, trig, 3)).tolist() == [0, 2, 5, 8]
+    # a trigger token at step t is exactly a boundary mask bit at t
+    key = gen.key_from_seed(7)
+    toks = gen.token_stream(key, 3000)
+    mask = np.isin(toks, np.array(gen.TRIGGER_TOKENS)).astype(np.uint8)
+    for t_max in (0, 64):
+        np.testing.assert_array_equal(oracle.schedule_tokens(toks, np.array(gen.TRIGGER_TOKENS), t_max),
+                                      oracle.schedule(mask, t_max))
+    gaps = np.diff(np.flatnonzero(mask))
+    assert abs(gaps.mean() - 18) < 5 * 18 / math.sqrt(gaps.size)
