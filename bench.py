@@ -41,7 +41,10 @@ def parse():
     ap.add_argument("--workload", default="llama8b_ctx32k_b4")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the dense-only/fast-only modes and the CPU baseline")
+                    help="skip the dense-only/fast-only modes, the CPU baseline and the other "
+                         "workloads")
+    ap.add_argument("--also", default="llama8b_ctx128k_l32,ragged_paged_b32",
+                    help="comma-separated workloads measured after the headline one")
     return ap.parse_args()
 
 
@@ -241,23 +244,12 @@ def cpu_baseline(wl):
             "seconds": float(r["seconds"].sum())}
 
 
-def main():
-    args = parse()
-    world, rank, local = dist_setup(args.gpus)
-    if args.impl == "reference":
-        run_reference(args, world, rank)
-        return
+def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=None):
+    """Time whole decode runs of one workload (CUDA-graph replays), the per-kernel durations
+    (event-instrumented replays), and optionally the dense-only / fast-only modes and the
+    end-to-end run with host buffers."""
     import torch
-
-    import __graft_entry__
-    __graft_entry__.build()
     from synth import device as sdev
-    from synth.configs import WORKLOADS
-    from synth.workload import HostWorkload
-
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    wl = HostWorkload(WORKLOADS[args.workload])
     cfg = wl.cfg
     st = sdev.make_state(wl, device=dev)
     ins = sdev.DeviceInputs(wl, cfg.steps, dev)
@@ -265,7 +257,6 @@ def main():
     out = torch.empty((cfg.steps, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
                       dtype=torch.bfloat16, device=dev)
     len0 = st.seq_len.clone()
-    stream = torch.cuda.Stream(device=dev)
 
     def capture(plan):
         g = torch.cuda.CUDAGraph()
@@ -279,41 +270,44 @@ def main():
         return g
 
     def time_graph(g, k, w):
-        for _ in range(w):
-            g.replay()
-        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(w):
+                g.replay()
+            torch.cuda.synchronize()
+            barrier(world)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(k):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
         barrier(world)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(k):
-            g.replay()
-        e1.record()
-        torch.cuda.synchronize()
-        barrier(world)
-        return e0.elapsed_time(e1)
+        return allreduce_max(e0.elapsed_time(e1), world)
 
-    plan = st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, out_fp32=False)
-    g_mix = capture(plan)
-    with torch.cuda.stream(stream):
-        with Clocks(local) as clk:
-            ms = time_graph(g_mix, args.steps, args.warmup)
-    ms = allreduce_max(ms, world)
-    torch.cuda.synchronize()
-    err = int(st.err[0])
-    tokens_per_step = cfg.batch * cfg.steps
-    value = world * tokens_per_step * args.steps / (ms / 1000.0)
-    n_slow_steps = int(slow.any(axis=1).sum())
+    res = {}
+    tokens_per_run = cfg.batch * cfg.steps
+    g_mix = capture(st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, out_fp32=False))
+    clk = Clocks(clock_index) if clock_index is not None else None
+    if clk:
+        clk.__enter__()
+    ms = time_graph(g_mix, k_steps, warmup)
+    if clk:
+        clk.__exit__()
+        res["clocks"] = clk.summary()
+    res["value"] = world * tokens_per_run * k_steps / (ms / 1000.0)
+    res["ms_per_run"] = ms / k_steps
+    res["tokens_per_run"] = tokens_per_run
+    res["slow_steps"] = int(slow.any(axis=1).sum())
+    res["launches_per_run"] = int(sum(1 + (4 if r.any() else 0) + (0 if r.all() else 1) for r in slow))
     sel_rows = (st.rows.view(cfg.n_layers, cfg.batch, cfg.n_kv_heads).float().mean(dim=(0, 2))
                 .cpu().numpy())
-    launches_per_run = int(sum(1 + (4 if r.any() else 0) + (0 if r.all() else 1) for r in slow))
 
-    # -- live kernel timing: the same run with external event nodes around each attention
-    #    kernel, replayed a few times --------------------------------------------------------
+    # live kernel timing: the same run with external event nodes around each attention kernel
     events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * cfg.steps)]
-    plan_ev = st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, out_fp32=False, events=events)
-    g_ev = capture(plan_ev)
-    reps = 5
+    g_ev = capture(st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, out_fp32=False,
+                                events=events))
+    reps = 3
     d_dense, d_sparse = [], []
     is_slow = slow.any(axis=1)
     with torch.cuda.stream(stream):
@@ -324,7 +318,7 @@ def main():
                 dt = events[2 * t].elapsed_time(events[2 * t + 1]) * 1e-3
                 (d_dense if is_slow[t] else d_sparse).append((t, dt))
     bd, bs = bytes_model(wl, slow.astype(bool), sel_rows)
-    peak, peak_kind = measured_peaks()
+    peak, _ = measured_peaks()
 
     def kstats(d, bytes_per):
         if not d:
@@ -333,98 +327,141 @@ def main():
         byt = np.array([bytes_per[x[0]] for x in d])
         avg = float(secs.mean())
         gbs = float(byt.mean() / avg / 1e9)
-        return {"launches_per_step": len(d) // reps, "avg_us": avg * 1e6,
+        return {"launches_per_run": len(d) // reps, "avg_us": avg * 1e6,
                 "bytes_per_launch": float(byt.mean()), "achieved_gbs": gbs,
-                "frac_of_peak": gbs / peak, "total_us_per_step": float(secs.sum() / reps * 1e6)}
+                "frac_of_peak": gbs / peak, "total_us_per_run": float(secs.sum() / reps * 1e6)}
 
-    kd, ks = kstats(d_dense, bd), kstats(d_sparse, bs)
-    dom_name, dom = max([("sfi_dense_decode_attn", kd), ("sfi_sparse_decode_attn", ks)],
-                        key=lambda x: -1 if x[1] is None else x[1]["total_us_per_step"])
+    res["kernels"] = {"sfi_dense_decode_attn": kstats(d_dense, bd),
+                      "sfi_sparse_decode_attn": kstats(d_sparse, bs)}
+    del g_ev
+
+    if extras:
+        # end to end through the public API with host buffers
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        hq, hk, hv, ho = pin(ins.q), pin(ins.k_new), pin(ins.v_new), pin(out)
+        hq.copy_(ins.q.cpu())
+        hk.copy_(ins.k_new.cpu())
+        hv.copy_(ins.v_new.cpu())
+        h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
+        with torch.cuda.stream(stream):
+            for i in range(warmup + k_steps):
+                if i == warmup:
+                    torch.cuda.synchronize()
+                    barrier(world)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                ins.q.copy_(hq, non_blocking=True)
+                ins.k_new.copy_(hk, non_blocking=True)
+                ins.v_new.copy_(hv, non_blocking=True)
+                g_mix.replay()
+                ho.copy_(out, non_blocking=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e1.record()
+            torch.cuda.synchronize()
+        ms_e2e = allreduce_max(e0.elapsed_time(e1), world)
+        res["e2e"] = {"value": world * tokens_per_run * k_steps / (ms_e2e / 1000.0),
+                      "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+                      "d2h_bytes_per_step": int(ho.numel() * 2), "ms_per_step": ms_e2e / k_steps}
+        # dense-only (the full-KV baseline) and fast-only
+        k2 = max(3, k_steps // 4)
+        g_dense = capture(st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, out_fp32=False,
+                                       dense_only=True))
+        ms_d = time_graph(g_dense, k2, 2)
+        del g_dense
+        fast_only = np.zeros_like(slow)
+        fast_only[0] = 1
+        g_fast = capture(st.make_plan(fast_only, ins.q, ins.k_new, ins.v_new, out,
+                                      out_fp32=False))
+        ms_f = time_graph(g_fast, k2, 2)
+        del g_fast
+        res["modes"] = {
+            "sfi_mix": {"tokens_per_s": res["value"], "ms_per_run": res["ms_per_run"],
+                        "slow_steps": res["slow_steps"]},
+            "dense_only": {"tokens_per_s": world * tokens_per_run * k2 / (ms_d / 1000.0),
+                           "ms_per_run": ms_d / k2},
+            "fast_only": {"tokens_per_s": world * tokens_per_run * k2 / (ms_f / 1000.0),
+                          "ms_per_run": ms_f / k2, "note": "one slow step at t=0"},
+        }
+        res["modes"]["sfi_vs_dense_speedup"] = (res["modes"]["sfi_mix"]["tokens_per_s"] /
+                                                res["modes"]["dense_only"]["tokens_per_s"])
+    torch.cuda.synchronize()
+    res["device_error"] = int(st.err[0])
+    res["kv_bytes"] = int(st.k.numel() * 4)
+    del g_mix
+    return res
+
+
+def workload_config(wl, res):
+    cfg = wl.cfg
+    return {"workload": cfg.name, "layers": cfg.n_layers, "batch": cfg.batch,
+            "q_heads": cfg.n_q_heads, "kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim,
+            "context": int(wl.len0.max()) if cfg.ctx_lo == cfg.ctx else f"{cfg.ctx_lo}-{cfg.ctx}",
+            "paged": bool(cfg.page_size), "decode_steps_per_step": cfg.steps,
+            "slow_steps_per_step": res["slow_steps"],
+            "budget": f"{cfg.n_sink} sinks + {cfg.n_window} window + {cfg.n_select} selected",
+            "l2": f"inputs larger than L2: every slow step streams the {res['kv_bytes'] / 1e6:.0f} MB "
+                  "KV cache; no flush"}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from synth.configs import WORKLOADS
+    from synth.workload import HostWorkload
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    wl = HostWorkload(WORKLOADS[args.workload])
+    res = measure(wl, args, world, dev, stream, args.steps, args.warmup, extras=not args.no_extras,
+                  clock_index=local)
+    torch.cuda.empty_cache()
+    others = {}
+    if not args.no_extras and args.also:
+        for name in [n for n in args.also.split(",") if n and n != args.workload]:
+            w2 = HostWorkload(WORKLOADS[name])
+            r2 = measure(w2, args, world, dev, stream, max(3, args.steps // 4), 2, extras=False)
+            others[name] = {"tokens_per_s": r2["value"], "ms_per_run": r2["ms_per_run"],
+                            "config": workload_config(w2, r2), "kernels": r2["kernels"],
+                            "device_error": r2["device_error"]}
+            torch.cuda.empty_cache()
+
+    peak, peak_kind = measured_peaks()
+    ks = res["kernels"]
+    dom_name, dom = max(ks.items(), key=lambda x: -1 if x[1] is None else x[1]["total_us_per_run"])
     traffic = traffic_record(dom_name)
     roofline = {"bound": "hbm", "achieved": dom["achieved_gbs"], "peak": peak, "unit": "GB/s",
                 "frac": dom["achieved_gbs"] / peak, "kernel": dom_name,
                 "peak_kind": f"{peak_kind} (hbm_gbs, STREAM-style copy)",
                 "bytes_per_launch": dom["bytes_per_launch"], "avg_launch_us": dom["avg_us"],
                 "traffic": None if traffic is None else traffic["dram_bytes_per_launch"]}
-
-    # -- end to end through the public API with host buffers --------------------------------
-    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-    hq, hk, hv, ho = pin(ins.q), pin(ins.k_new), pin(ins.v_new), pin(out)
-    hq.copy_(ins.q.cpu())
-    hk.copy_(ins.k_new.cpu())
-    hv.copy_(ins.v_new.cpu())
-    h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
-    d2h = ho.numel() * 2
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup + args.steps):
-            if i == args.warmup:
-                torch.cuda.synchronize()
-                barrier(world)
-                e0 = torch.cuda.Event(enable_timing=True)
-                e0.record()
-            ins.q.copy_(hq, non_blocking=True)
-            ins.k_new.copy_(hk, non_blocking=True)
-            ins.v_new.copy_(hv, non_blocking=True)
-            g_mix.replay()
-            ho.copy_(out, non_blocking=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e1.record()
-        torch.cuda.synchronize()
-    ms_e2e = allreduce_max(e0.elapsed_time(e1), world)
-    e2e = {"value": world * tokens_per_step * args.steps / (ms_e2e / 1000.0), "unit": "tokens/s",
-           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-           "ms_per_step": ms_e2e / args.steps}
-
-    # -- dense-only (full-KV baseline) and fast-only modes -----------------------------------
-    modes = {"sfi_mix": {"tokens_per_s": value, "ms_per_run": ms / args.steps,
-                         "slow_steps": n_slow_steps}}
-    if not args.no_extras:
-        k2 = max(3, args.steps // 4)
-        g_dense = capture(st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, out_fp32=False,
-                                       dense_only=True))
-        with torch.cuda.stream(stream):
-            ms_d = allreduce_max(time_graph(g_dense, k2, 2), world)
-        fast_only = np.zeros_like(slow)
-        fast_only[0] = 1
-        g_fast = capture(st.make_plan(fast_only, ins.q, ins.k_new, ins.v_new, out,
-                                      out_fp32=False))
-        with torch.cuda.stream(stream):
-            ms_f = allreduce_max(time_graph(g_fast, k2, 2), world)
-        modes["dense_only"] = {"tokens_per_s": world * tokens_per_step * k2 / (ms_d / 1000.0),
-                               "ms_per_run": ms_d / k2}
-        modes["fast_only"] = {"tokens_per_s": world * tokens_per_step * k2 / (ms_f / 1000.0),
-                              "ms_per_run": ms_f / k2, "note": "one slow step at t=0"}
-        modes["sfi_vs_dense_speedup"] = modes["sfi_mix"]["tokens_per_s"] / modes["dense_only"]["tokens_per_s"]
-    torch.cuda.synchronize()
-    err |= int(st.err[0])
-
     cpu = None
     if rank == 0 and world == 1 and not args.no_extras:
         cpu = cpu_baseline(wl)
-
     if rank == 0:
-        L0 = int(wl.len0.max())
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+            "metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_run"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded counter-based generator, Zipf(1.1) key-norm boost)",
-            "config": {"workload": cfg.name, "layers": cfg.n_layers, "batch": cfg.batch,
-                       "q_heads": cfg.n_q_heads, "kv_heads": cfg.n_kv_heads,
-                       "head_dim": cfg.head_dim, "context": L0, "decode_steps_per_step": cfg.steps,
-                       "slow_steps_per_step": n_slow_steps,
-                       "budget": f"{cfg.n_sink} sinks + {cfg.n_window} window + {cfg.n_select} selected",
-                       "l2": "inputs larger than L2: every slow step streams the "
-                             f"{st.k.numel() * 4 / 1e6:.0f} MB KV cache; no flush",
-                       "parallelism": "replicas" if world > 1 else "single"},
+            "config": dict(workload_config(wl, res),
+                           parallelism="replicas" if world > 1 else "single"),
             "roofline": roofline,
-            "kernels": {"sfi_dense_decode_attn": kd, "sfi_sparse_decode_attn": ks},
+            "kernels": ks,
             "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": launches_per_run * args.steps,
-            "clocks": clk.summary(),
-            "modes": modes,
-            "device_error": err,
+            "e2e": res.get("e2e"),
+            "gpu_launches": res["launches_per_run"] * args.steps,
+            "clocks": res.get("clocks"),
+            "modes": res.get("modes"),
+            "other_workloads": others,
+            "device_error": res["device_error"],
         }
         print(json.dumps(line))
 

@@ -233,6 +233,20 @@ def test_end_to_end_32k_batch4_sampled():
     compare_run(wl, 6, units=[0, 7, 13, 31])
 
 
+def test_end_to_end_128k_32_layers_sampled():
+    """The 128K-context, 32-layer workload at full size (17 GB of KV): sampled units over
+    the first decode steps."""
+    wl = HostWorkload(WORKLOADS["llama8b_ctx128k_l32"])
+    compare_run(wl, 4, units=[0, 8 * 17 + 5, 8 * 31 + 7])
+
+
+def test_end_to_end_ragged_paged_full_size_sampled():
+    """The ragged batch-32 paged workload at full size: sampled units (different sequence
+    lengths and per-sequence schedules) over the first decode steps."""
+    wl = HostWorkload(WORKLOADS["ragged_paged_b32"])
+    compare_run(wl, 8, units=[0, 8 * 5 + 3, 8 * 17 + 1, 8 * 31 + 7])
+
+
 # ------------------------------------------------------------------------------ error paths
 
 def test_bad_page_entry_sets_device_error_and_skips():
