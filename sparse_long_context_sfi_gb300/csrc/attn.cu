@@ -114,7 +114,7 @@ __device__ __forceinline__ void fail(Ctrl &c, uint32_t *err)
     raise_error(err, 0x4u);  // SFI_DEVERR_TIMEOUT
 }
 
-// Set / clear rows [r0, r1) of a 128-row validity mask kept in four registers.
+// Set rows [r0, r1) of a 128-row validity mask kept in four registers.
 __device__ __forceinline__ uint32_t word_bits(int r0, int r1, int w)
 {
     const int lo = min(max(r0 - 32 * w, 0), 32), hi = min(max(r1 - 32 * w, 0), 32);
@@ -129,13 +129,6 @@ __device__ __forceinline__ void mask_rows(uint32_t (&v)[4], int r0, int r1)
 #pragma unroll
     for (int w = 0; w < 4; ++w)
         v[w] |= word_bits(r0, r1, w);
-}
-
-__device__ __forceinline__ void clear_rows(uint32_t (&v)[4], int r0, int r1)
-{
-#pragma unroll
-    for (int w = 0; w < 4; ++w)
-        v[w] &= ~word_bits(r0, r1, w);
 }
 
 template <int G>
@@ -267,7 +260,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     if (warp == 0) {
         // =============================== TMA producer ===================================
-        if (lane == 0 && n_tiles > 0) {
+        // The whole warp runs the loop; each lane issues at most one TMA box per tile (a
+        // 64-column half of K or V for one page / block of rows), and lane 0 publishes the
+        // tile with a single arrive.expect_tx of the warp's summed bytes.
+        if (n_tiles > 0) {
             const uint64_t pol = policy_evict_first();
             // decode the first tile of the range
             long long g = g0;
@@ -280,6 +276,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             int t = (r - c.pre[b]) - kvh * c.nt[b];
             int seg = -1, issued = 0;
             int seg_len = 0, seg_rows_c = 0, seg_ws = 0;
+            const int my_q = lane >> 2, my_op = lane & 3;  // page / block and (K|V, half)
+            // paged dense tiles: this lane's page id, loaded one tile ahead
+            const bool paged_dense = DENSE && p.page_size != 0;
+            int my_page = 0;
+            auto load_page = [&](int bb, int tt) {
+                my_page = (tt * kTile + 16 * my_q < c.len[bb])
+                              ? __ldg(p.page_table + bb * p.max_pages + tt * 8 + my_q)
+                              : 0;
+            };
+            if (paged_dense)
+                load_page(b, t);
+            bool ok = true;
             for (int i = 0; i < n_tiles; ++i, ++g) {
                 if (i > 0 && ++t == c.nt[b]) {
                     t = 0;
@@ -294,27 +302,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                 }
                 const int s = i % kStages;
-                if (!mbar_wait(&c.empty[s], ((i / kStages) & 1) ^ 1, &c.abort)) {
-                    fail(c, p.err);
-                    break;
-                }
+                if (lane == 0)
+                    ok = mbar_wait(&c.empty[s], ((i / kStages) & 1) ^ 1, &c.abort);
                 const int u = (layer * B + b) * Hkv + kvh;
                 const bool first = (i == 0) || (t == 0);
                 const bool last = (i == n_tiles - 1) || (t == c.nt[b] - 1);
                 if (first) {
                     ++seg;
-                    if (seg >= 2 && !mbar_wait(&c.q_free[seg & 1], ((seg >> 1) - 1) & 1, &c.abort)) {
-                        fail(c, p.err);
-                        break;
-                    }
-                }
-                uint8_t *st = smem + s * kStageBytes;
-                TileMeta &mt = c.meta[s];
-                mt.unit = u;
-                mt.tile = t;
-                mt.flags = (first ? kFlagFirst : 0) | (last ? kFlagLast : 0);
-                if (first) {
-                    // per-unit quantities, read once per segment
+                    if (lane == 0 && ok && seg >= 2)
+                        ok = mbar_wait(&c.q_free[seg & 1], ((seg >> 1) - 1) & 1, &c.abort);
                     seg_len = c.len[b];
                     if (!DENSE) {
                         const int rows_c = max(0, min(__ldg(p.comp_rows + u), p.comp_cap));
@@ -323,112 +319,153 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         seg_ws = max(n_s, seg_len - p.n_window);
                     }
                 }
-                uint32_t valid[4] = {0u, 0u, 0u, 0u};
-                uint64_t *bar = &c.full[s];
-                auto issue = [&](const CUtensorMap *mk, const CUtensorMap *mv, int y, int row0,
-                                 int rows) {
-                    mbar_expect_tx(bar, 4u * static_cast<uint32_t>(rows) * 128u);
-                    uint8_t *dk = st + row0 * 128;
-                    uint8_t *dv = dk + 2 * kChunkBytes;
-                    if (DENSE) {  // streamed once per slow step: do not displace reusable lines
-                        tma_load_2d_hint(dk, mk, bar, 0, y, pol);
-                        tma_load_2d_hint(dk + kChunkBytes, mk, bar, 64, y, pol);
-                        tma_load_2d_hint(dv, mv, bar, 0, y, pol);
-                        tma_load_2d_hint(dv + kChunkBytes, mv, bar, 64, y, pol);
-                    } else {
-                        tma_load_2d(dk, mk, bar, 0, y);
-                        tma_load_2d(dk + kChunkBytes, mk, bar, 64, y);
-                        tma_load_2d(dv, mv, bar, 0, y);
-                        tma_load_2d(dv + kChunkBytes, mv, bar, 64, y);
-                    }
-                };
-                if (first) {
-                    mbar_expect_tx(bar, 2u * G * 128u);
-                    uint8_t *qb = smem + kQOff + (seg & 1) * kOpBytes;
-                    tma_load_2d(qb, &tm_q, bar, 0, u * G);
-                    tma_load_2d(qb + kOpChunk, &tm_q, bar, 64, u * G);
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+                    if (lane == 0)
+                        fail(c, p.err);
+                    break;
                 }
                 const int L = seg_len;
+                // ---- this lane's box ----------------------------------------------------
+                const CUtensorMap *map = nullptr;
+                int y = 0, row0 = 0, rows = 0, kv = 0, half = 0;
+                uint32_t valid[4] = {0u, 0u, 0u, 0u};
                 if (DENSE) {
                     const int pos0 = t * kTile;
                     const int nvalid = min(kTile, L - pos0);
-                    mask_rows(valid, 0, nvalid);
                     if (p.page_size == 0) {
-                        issue(&tm_k, &tm_v, u * p.capacity + pos0, 0, kTile);
-                    } else {
-                        const int *pt = p.page_table + b * p.max_pages + (pos0 >> 4);
-                        int page[8];
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            page[q] = (16 * q < nvalid) ? __ldg(pt + q) : 0;
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            if (16 * q >= nvalid)
-                                continue;
-                            if (page[q] < 0 || page[q] >= p.n_pages) {
-                                raise_error(p.err, 0x1u);
-                                clear_rows(valid, 16 * q, 16 * q + 16);
-                                continue;
-                            }
-                            issue(&tm_k, &tm_v, ((layer * p.n_pages + page[q]) * Hkv + kvh) * 16,
-                                  16 * q, 16);
+                        if (lane == 0)
+                            mask_rows(valid, 0, nvalid);
+                        if (lane < 4) {
+                            kv = lane >> 1;
+                            half = lane & 1;
+                            map = kv ? &tm_v : &tm_k;
+                            y = u * p.capacity + pos0;
+                            rows = kTile;
+                        }
+                    } else if (16 * my_q < nvalid) {
+                        if (my_page < 0 || my_page >= p.n_pages) {
+                            if (my_op == 0)
+                                raise_error(p.err, 0x1u);  // rows of this page stay invalid
+                        } else {
+                            kv = my_op >> 1;
+                            half = my_op & 1;
+                            map = kv ? &tm_v : &tm_k;
+                            y = ((layer * p.n_pages + my_page) * Hkv + kvh) * 16;
+                            row0 = 16 * my_q;
+                            rows = 16;
+                            if (my_op == 0)
+                                mask_rows(valid, row0, min(row0 + 16, nvalid));
                         }
                     }
                 } else {
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int R = t * kTile + 64 * h2;
-                        if (R < 64 * p.n_cbox) {
-                            const int k = R >> 6;
-                            const int vr = max(0, min(64, seg_rows_c - 64 * k));
-                            if (vr > 0) {
-                                issue(&tm_kc, &tm_vc, u * p.comp_cap + 64 * k, 64 * h2, 64);
-                                mask_rows(valid, 64 * h2, 64 * h2 + vr);
-                            }
-                            continue;
-                        }
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int j = (R + 16 * q - 64 * p.n_cbox) >> 4;
-                            if (j >= p.n_wbox)
-                                break;
-                            const int row0 = 64 * h2 + 16 * q;
-                            if (p.page_size == 0) {
-                                const int p0 = seg_ws + 16 * j;
-                                const int vr = max(0, min(16, L - p0));
-                                if (vr == 0)
-                                    continue;
-                                issue(&tm_k, &tm_v, u * p.capacity + p0, row0, 16);
+                    const int h2 = lane >> 4, j16 = lane & 15;
+                    const int R = t * kTile + 64 * h2;
+                    if (R < 64 * p.n_cbox) {
+                        const int k = R >> 6;
+                        const int vr = max(0, min(64, seg_rows_c - 64 * k));
+                        if (vr > 0 && j16 < 4) {
+                            kv = j16 >> 1;
+                            half = j16 & 1;
+                            map = kv ? &tm_vc : &tm_kc;
+                            y = u * p.comp_cap + 64 * k;
+                            row0 = 64 * h2;
+                            rows = 64;
+                            if (j16 == 0)
                                 mask_rows(valid, row0, row0 + vr);
-                            } else {
-                                const int lp = (seg_ws >> 4) + j;
-                                const int r0 = max(seg_ws - lp * 16, 0);
-                                const int r1 = min(L - lp * 16, 16);
-                                if (r1 <= r0)
-                                    continue;
+                        }
+                    } else {
+                        const int q = j16 >> 2;
+                        const int j = (R + 16 * q - 64 * p.n_cbox) >> 4;
+                        const int rr0 = 64 * h2 + 16 * q;
+                        if (j < p.n_wbox && p.page_size == 0) {
+                            const int p0 = seg_ws + 16 * j;
+                            const int vr = max(0, min(16, L - p0));
+                            if (vr > 0) {
+                                kv = my_op >> 1;
+                                half = my_op & 1;
+                                map = kv ? &tm_v : &tm_k;
+                                y = u * p.capacity + p0;
+                                row0 = rr0;
+                                rows = 16;
+                                if (my_op == 0)
+                                    mask_rows(valid, rr0, rr0 + vr);
+                            }
+                        } else if (j < p.n_wbox) {
+                            const int lp = (seg_ws >> 4) + j;
+                            const int r0 = max(seg_ws - lp * 16, 0);
+                            const int r1 = min(L - lp * 16, 16);
+                            if (r1 > r0) {
                                 const int page = __ldg(p.page_table + b * p.max_pages + lp);
                                 if (page < 0 || page >= p.n_pages) {
-                                    raise_error(p.err, 0x1u);
-                                    continue;
+                                    if (my_op == 0)
+                                        raise_error(p.err, 0x1u);
+                                } else {
+                                    kv = my_op >> 1;
+                                    half = my_op & 1;
+                                    map = kv ? &tm_v : &tm_k;
+                                    y = ((layer * p.n_pages + page) * Hkv + kvh) * 16;
+                                    row0 = rr0;
+                                    rows = 16;
+                                    if (my_op == 0)
+                                        mask_rows(valid, rr0 + r0, rr0 + r1);
                                 }
-                                issue(&tm_k, &tm_v, ((layer * p.n_pages + page) * Hkv + kvh) * 16,
-                                      row0, 16);
-                                mask_rows(valid, row0 + r0, row0 + r1);
                             }
                         }
                     }
                 }
+                // ---- publish the tile, then issue ---------------------------------------
+                uint32_t vw[4];
 #pragma unroll
                 for (int w = 0; w < 4; ++w)
-                    mt.valid[w] = valid[w];
-                mbar_arrive(bar);  // releases the metadata; completes with the copies
-                if (i == 0)
+                    vw[w] = __reduce_or_sync(0xffffffffu, valid[w]);
+                const uint32_t bytes =
+                    __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(rows) * 128u) +
+                    (first ? 2u * G * 128u : 0u);
+                uint64_t *bar = &c.full[s];
+                if (lane == 0) {
+                    TileMeta &mt = c.meta[s];
+                    mt.unit = u;
+                    mt.tile = t;
+                    mt.flags = (first ? kFlagFirst : 0) | (last ? kFlagLast : 0);
+#pragma unroll
+                    for (int w = 0; w < 4; ++w)
+                        mt.valid[w] = vw[w];
+                    mbar_arrive_expect_tx(bar, bytes);  // releases the metadata
+                }
+                __syncwarp();
+                if (first && lane < 2) {
+                    uint8_t *qb = smem + kQOff + (seg & 1) * kOpBytes;
+                    tma_load_2d(qb + lane * kOpChunk, &tm_q, bar, 64 * lane, u * G);
+                }
+                if (rows > 0) {
+                    uint8_t *dst = smem + s * kStageBytes + kv * 2 * kChunkBytes +
+                                   half * kChunkBytes + row0 * 128;
+                    if (DENSE)  // streamed once per slow step: do not displace reusable lines
+                        tma_load_2d_hint(dst, map, bar, 64 * half, y, pol);
+                    else
+                        tma_load_2d(dst, map, bar, 64 * half, y);
+                }
+                if (lane == 0 && i == 0)
                     SFI_STAMP(3);
                 ++issued;
+                if (paged_dense && i + 1 < n_tiles) {
+                    int nb = b, nt2 = t + 1;
+                    if (nt2 == c.nt[b]) {
+                        nt2 = 0;
+                        if (kvh + 1 == Hkv) {
+                            do {
+                                if (++nb == B)
+                                    nb = 0;
+                            } while (c.nt[nb] == 0);
+                        }
+                    }
+                    load_page(nb, nt2);
+                }
             }
             // Never leave a copy in flight into shared memory we are about to give up.
-            for (int j = max(0, issued - kStages); j < issued; ++j)
-                mbar_wait(&c.full[j % kStages], (j / kStages) & 1, nullptr);
+            if (lane == 0)
+                for (int j = max(0, issued - kStages); j < issued; ++j)
+                    mbar_wait(&c.full[j % kStages], (j / kStages) & 1, nullptr);
         }
     } else if (warp == 1) {
         // ================================ MMA issuer =====================================
