@@ -43,7 +43,7 @@ def parse():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the dense-only/fast-only modes, the CPU baseline and the other "
                          "workloads")
-    ap.add_argument("--also", default="llama8b_ctx128k_l32,ragged_paged_b32",
+    ap.add_argument("--also", default="llama8b_ctx128k_l32,ragged_paged_b32,longcot_ctx128k_b8_l32",
                     help="comma-separated workloads measured after the headline one")
     return ap.parse_args()
 
@@ -244,7 +244,8 @@ def cpu_baseline(wl):
             "seconds": float(r["seconds"].sum())}
 
 
-def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=None):
+def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=None,
+            dense_only_runs=0):
     """Time whole decode runs of one workload (CUDA-graph replays), the per-kernel durations
     (event-instrumented replays), and optionally the dense-only / fast-only modes and the
     end-to-end run with host buffers."""
@@ -258,16 +259,20 @@ def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=N
                       dtype=torch.bfloat16, device=dev)
     len0 = st.seq_len.clone()
 
-    def capture(plan):
+    def capture(run):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             st.seq_len.copy_(len0)
-            st.run(plan, stream=stream)            # eager warm-up: builds maps, checks args
+            run.issue(stream)                      # eager warm-up: builds maps, checks args
         stream.synchronize()
         with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
             st.seq_len.copy_(len0)
-            st.run(plan, stream=stream)
+            run.issue(stream)
         return g
+
+    def run_of(sl, **kw):
+        return sdev.DriftingRun(wl, st, sl, ins.q, ins.k_new, ins.v_new, out, ins.model,
+                                out_fp32=False, **kw)
 
     def time_graph(g, k, w):
         with torch.cuda.stream(stream):
@@ -287,7 +292,7 @@ def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=N
 
     res = {}
     tokens_per_run = cfg.batch * cfg.steps
-    g_mix = capture(st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, out_fp32=False))
+    g_mix = capture(run_of(slow))
     clk = Clocks(clock_index) if clock_index is not None else None
     if clk:
         clk.__enter__()
@@ -305,8 +310,7 @@ def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=N
 
     # live kernel timing: the same run with external event nodes around each attention kernel
     events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * cfg.steps)]
-    g_ev = capture(st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, out_fp32=False,
-                                events=events))
+    g_ev = capture(run_of(slow, events=events))
     reps = 3
     d_dense, d_sparse = [], []
     is_slow = slow.any(axis=1)
@@ -364,14 +368,12 @@ def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=N
                       "d2h_bytes_per_step": int(ho.numel() * 2), "ms_per_step": ms_e2e / k_steps}
         # dense-only (the full-KV baseline) and fast-only
         k2 = max(3, k_steps // 4)
-        g_dense = capture(st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, out_fp32=False,
-                                       dense_only=True))
+        g_dense = capture(run_of(slow, dense_only=True))
         ms_d = time_graph(g_dense, k2, 2)
         del g_dense
         fast_only = np.zeros_like(slow)
         fast_only[0] = 1
-        g_fast = capture(st.make_plan(fast_only, ins.q, ins.k_new, ins.v_new, out,
-                                      out_fp32=False))
+        g_fast = capture(run_of(fast_only))
         ms_f = time_graph(g_fast, k2, 2)
         del g_fast
         res["modes"] = {
@@ -384,6 +386,12 @@ def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=N
         }
         res["modes"]["sfi_vs_dense_speedup"] = (res["modes"]["sfi_mix"]["tokens_per_s"] /
                                                 res["modes"]["dense_only"]["tokens_per_s"])
+    if dense_only_runs:
+        g_dense = capture(run_of(slow, dense_only=True))
+        ms_d = time_graph(g_dense, dense_only_runs, 1)
+        del g_dense
+        res["dense_only"] = {"tokens_per_s": world * tokens_per_run * dense_only_runs / (ms_d / 1000.0),
+                             "ms_per_run": ms_d / dense_only_runs}
     torch.cuda.synchronize()
     res["device_error"] = int(st.err[0])
     res["kv_bytes"] = int(st.k.numel() * 4)
@@ -427,10 +435,15 @@ def main():
     if not args.no_extras and args.also:
         for name in [n for n in args.also.split(",") if n and n != args.workload]:
             w2 = HostWorkload(WORKLOADS[name])
-            r2 = measure(w2, args, world, dev, stream, max(3, args.steps // 4), 2, extras=False)
+            big = w2.cfg.n_layers * w2.cfg.batch * w2.cfg.ctx > 32 * 10 ** 6
+            r2 = measure(w2, args, world, dev, stream, 2 if big else max(3, args.steps // 4),
+                         1 if big else 2, extras=False, dense_only_runs=1 if big else 2)
             others[name] = {"tokens_per_s": r2["value"], "ms_per_run": r2["ms_per_run"],
                             "config": workload_config(w2, r2), "kernels": r2["kernels"],
                             "device_error": r2["device_error"]}
+            if "dense_only" in r2:
+                others[name]["dense_only"] = r2["dense_only"]
+                others[name]["sfi_vs_dense_speedup"] = r2["value"] / r2["dense_only"]["tokens_per_s"]
             torch.cuda.empty_cache()
 
     peak, peak_kind = measured_peaks()

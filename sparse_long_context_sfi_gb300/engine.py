@@ -102,11 +102,16 @@ class SfiState:
 
     # -- a whole run through the native driver --------------------------------------------------
     def make_plan(self, slow: np.ndarray, q, k_new, v_new, out, out_fp32=True, out_per_step=True,
-                  dense_only=False, events=None):
+                  dense_only=False, events=None, t0=0, t1=None):
         """slow: uint8 [steps][B]; q/k_new/v_new/out: device tensors with a leading step axis.
-        events: optional list of 2 * steps torch.cuda.Event(enable_timing=True), recorded
-        around each step's attention kernel."""
-        slow = np.ascontiguousarray(slow, dtype=np.uint8)
+        events: optional list of 2 * (t1 - t0) torch.cuda.Event(enable_timing=True), recorded
+        around each step's attention kernel. [t0, t1): the steps this plan covers (a run can
+        be issued as several consecutive plans)."""
+        t1 = slow.shape[0] if t1 is None else t1
+        q, k_new, v_new = q[t0:t1], k_new[t0:t1], v_new[t0:t1]
+        if out_per_step:
+            out = out[t0:t1]
+        slow = np.ascontiguousarray(slow[t0:t1], dtype=np.uint8)
         steps = slow.shape[0]
         mixed = np.array([(r.any() and not r.all()) for r in slow])
         masks = None
@@ -117,8 +122,8 @@ class SfiState:
             n_steps=steps, slow=slow.ctypes.data, q=q.data_ptr(), k_new=k_new.data_ptr(),
             v_new=v_new.data_ptr(), out=out.data_ptr(), out_fp32=1 if out_fp32 else 0,
             out_per_step=1 if out_per_step else 0, scores_f=self.scores.data_ptr(),
-            masks=None if masks is None else masks.data_ptr(), len_start=int(self.len0.max()),
-            dense_only=1 if dense_only else 0)
+            masks=None if masks is None else masks.data_ptr(),
+            len_start=int(self.len0.max()) + t0, dense_only=1 if dense_only else 0)
         ev_arr = None
         if events is not None:
             assert len(events) == 2 * steps

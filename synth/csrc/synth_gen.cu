@@ -267,3 +267,53 @@ int synth_fill_queries(void *dst, int steps, int n_layers, int batch, int n_q_he
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// Heavy-hitter drift: rewrite the K rows of listed positions of a contiguous cache
+// [Ly][B][Hkv][cap][D] with their new planted / plain content (V rows do not change).
+// pos, planted: [units][m] (pos < 0 = unused slot).
+namespace {
+
+__global__ void rewrite_k(uint4 *dst, int n_units, int m, const int32_t *pos,
+                          const uint8_t *planted, int batch, int n_kv_heads, int cap,
+                          uint64_t key, const float *ka)
+{
+    const uint64_t total = static_cast<uint64_t>(n_units) * m * 16;
+    for (uint64_t i = blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<uint64_t>(gridDim.x) * blockDim.x) {
+        const int ch = static_cast<int>(i & 15);
+        const uint64_t slot = i >> 4;
+        const int unit = static_cast<int>(slot / m);
+        const int p = pos[slot];
+        if (p < 0 || p >= cap)
+            continue;
+        const int head = unit % n_kv_heads;
+        const int b = (unit / n_kv_heads) % batch;
+        const int layer = unit / (n_kv_heads * batch);
+        uint32_t w[4];
+        for (int k = 0; k < 4; ++k) {
+            uint16_t e[2];
+            for (int j = 0; j < 2; ++j) {
+                const int d = 8 * ch + 2 * k + j;
+                float x = normal_f32(mix64(key, counter(0, layer, b, head, p, d)));
+                if (planted[slot])
+                    x = __fadd_rn(x, ka[(layer * n_kv_heads + head) * kD + d]);
+                e[j] = f32_to_bf16(x);
+            }
+            w[k] = static_cast<uint32_t>(e[0]) | (static_cast<uint32_t>(e[1]) << 16);
+        }
+        dst[(static_cast<uint64_t>(unit) * cap + p) * 16 + ch] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+}  // namespace
+
+extern "C" int synth_rewrite_k(void *dst, int n_units, int m, const int32_t *pos,
+                               const uint8_t *planted, int batch, int n_kv_heads, int cap,
+                               uint64_t key, const float *ka, void *cuda_stream)
+{
+    const uint64_t total = static_cast<uint64_t>(n_units) * m * 16;
+    rewrite_k<<<grid_for(total), 256, 0, static_cast<cudaStream_t>(cuda_stream)>>>(
+        static_cast<uint4 *>(dst), n_units, m, pos, planted, batch, n_kv_heads, cap, key, ka);
+    return static_cast<int>(cudaGetLastError());
+}

@@ -56,6 +56,45 @@ def fill_state_cache(wl: HostWorkload, state, on_device: bool = True, model=None
     return model
 
 
+def boundary_epochs(wl: HostWorkload, steps: int) -> np.ndarray:
+    """Heavy-hitter epoch of every step (uniform boundary mask): boundaries seen before t."""
+    m = wl.masks[0][:steps]
+    e = np.zeros(steps, dtype=np.int64)
+    e[1:] = np.cumsum(m[:-1])
+    return e
+
+
+class DriftingRun:
+    """Issues a decode run in segments between boundary steps; before the first step of each
+    epoch the drifting heavy-hitter keys are rewritten in place (a harness-side input edit,
+    the same one the oracle replays). The run starts by restoring epoch 0, so it can be
+    captured once and replayed."""
+
+    def __init__(self, wl: HostWorkload, state, slow, q, k_new, v_new, out, model=None,
+                 events=None, **plan_kw):
+        cfg = wl.cfg
+        self.wl, self.state, self.model = wl, state, model
+        steps = slow.shape[0]
+        self.ep = boundary_epochs(wl, steps)
+        cuts = [t for t in range(1, steps) if self.ep[t] != self.ep[t - 1]] if cfg.drift else []
+        bounds = [0] + cuts + [steps]
+        self.edits = gpu.drift_edits(wl, state.k.device) if cfg.drift else {}
+        self.plans = []
+        for a, b in zip(bounds[:-1], bounds[1:]):
+            ev = None if events is None else events[2 * a:2 * b]
+            self.plans.append((a, state.make_plan(slow, q, k_new, v_new, out, t0=a, t1=b,
+                                                  events=ev, **plan_kw)))
+
+    def issue(self, stream=None):
+        s = (torch.cuda.current_stream() if stream is None else stream).cuda_stream
+        if 0 in self.edits:
+            gpu.apply_drift(self.wl, self.state.k, self.edits[0], self.model, s)
+        for a, plan in self.plans:
+            if a > 0 and int(self.ep[a]) in self.edits:
+                gpu.apply_drift(self.wl, self.state.k, self.edits[int(self.ep[a])], self.model, s)
+            self.state.run(plan, stream=stream)
+
+
 def make_state(wl: HostWorkload, device="cuda", on_device: bool = True):
     from sparse_long_context_sfi_gb300.engine import SfiState
     state = SfiState(wl.cfg, wl.len0, device=device, page_table=wl.table, n_pages=wl.n_pages)

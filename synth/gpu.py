@@ -111,3 +111,50 @@ def page_owners(wl, device):
                 ob[pg] = b
                 olp[pg] = lp
     return torch.from_numpy(ob).to(device), torch.from_numpy(olp).to(device)
+
+
+def drift_edits(wl, device):
+    """Per boundary epoch e >= 1: device arrays (pos [U][m], planted [U][m]) listing the
+    K rows whose heavy-hitter membership changes from epoch e-1 to e."""
+    import torch
+    cfg = wl.cfg
+    U = wl.n_units
+    n_ep = wl.n_epochs()
+    per_unit = []
+    for layer in range(cfg.n_layers):
+        for b in range(cfg.batch):
+            for h in range(cfg.n_kv_heads):
+                per_unit.append([wl.hh_positions(layer, b, h, e) for e in range(n_ep)])
+    out = {}
+    # epoch e >= 1: changes from e-1 to e; key 0: back from the last epoch to epoch 0
+    for e in range(0, n_ep):
+        if e == 0 and n_ep == 1:
+            continue
+        changes = []
+        for u in range(U):
+            old = per_unit[u][e - 1] if e > 0 else per_unit[u][n_ep - 1]
+            new = per_unit[u][e]
+            ch = np.setxor1d(old, new)
+            changes.append((ch, np.isin(ch, new)))
+        m = max(1, max(len(c[0]) for c in changes))
+        pos = np.full((U, m), -1, np.int32)
+        pl = np.zeros((U, m), np.uint8)
+        for u, (ch, f) in enumerate(changes):
+            pos[u, :len(ch)] = ch
+            pl[u, :len(ch)] = f
+        out[e] = (torch.from_numpy(pos).to(device), torch.from_numpy(pl).to(device), m)
+    return out
+
+
+def apply_drift(wl, k, edit, model: "DeviceModel", stream=0):
+    """Rewrite the changed K rows of one epoch (edit from drift_edits)."""
+    cfg = wl.cfg
+    pos, pl, m = edit
+    l = lib()
+    if not hasattr(l, "_rewrite_set"):
+        l.synth_rewrite_k.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_int,
+                                      C.c_int, C.c_int, C.c_uint64, C.c_void_p, C.c_void_p]
+        l._rewrite_set = True
+    _check(l.synth_rewrite_k(k.data_ptr(), wl.n_units, m, pos.data_ptr(), pl.data_ptr(), cfg.batch,
+                             cfg.n_kv_heads, k.shape[3], int(wl.key), model.ka.data_ptr(), stream),
+           "synth_rewrite_k")

@@ -247,6 +247,32 @@ def test_end_to_end_ragged_paged_full_size_sampled():
     compare_run(wl, 8, units=[0, 8 * 5 + 3, 8 * 17 + 1, 8 * 31 + 7])
 
 
+def test_end_to_end_drifting_heavy_hitters():
+    """Long-CoT workload shape (window 128, budget 1916) scaled down, with heavy hitters
+    re-seeded at every boundary: the run is issued in segments with the key edits between
+    them, exactly as the benchmark does, and every step of every unit is checked."""
+    wl = small("longcot_ctx128k_b8_l32", ctx=3000, ctx_lo=3000, batch=2, n_layers=2, steps=40,
+               mask_param=6)
+    cfg = wl.cfg
+    assert wl.n_epochs() > 3
+    st = sdev.make_state(wl)
+    ins = sdev.DeviceInputs(wl, cfg.steps, st.k.device)
+    slow = st.schedule(wl.masks)
+    out = torch.zeros((cfg.steps, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
+                      dtype=torch.float32, device=st.k.device)
+    sdev.DriftingRun(wl, st, slow, ins.q, ins.k_new, ins.v_new, out, ins.model).issue()
+    torch.cuda.synchronize()
+    assert int(st.err[0]) == 0
+    ref = odecode.run(wl, steps=cfg.steps)
+    got = out.cpu().numpy()
+    G = cfg.group
+    for t in range(cfg.steps):
+        for u in range(st.n_units):
+            layer, b, kvh = unit_coords(cfg, u)
+            ok, err = close(got[t, layer, b, kvh * G:(kvh + 1) * G], ref["out"][t][u])
+            assert ok, f"step {t} unit {u}: max err {err}"
+
+
 # ------------------------------------------------------------------------------ error paths
 
 def test_bad_page_entry_sets_device_error_and_skips():
