@@ -364,6 +364,7 @@ sfi_status sfi_select(const sfi_kv_cache *kv, const float *scores_f, const sfi_b
     p.lambda = budget->lambda;
     p.sel_idx = mem->sel_idx;
     p.sel_cnt = mem->sel_cnt;
+    p.cache_keys = (kv->max_len - budget->n_window - budget->n_sink) <= 32768 ? 1 : 0;
     return launch_status(launch_select(p, as_stream(stream)));
 }
 

@@ -14,6 +14,9 @@ namespace {
 
 constexpr int NT = kSelectThreads;
 constexpr int kWarps = NT / 32;
+constexpr int kKeyCache = 32768;  // candidates whose keys fit in shared memory
+constexpr int kListCap = 8192;    // keys gathered for the refining passes
+constexpr int kSub = 4;           // sub-histograms (warps w with w % kSub equal share one)
 
 __device__ __forceinline__ uint32_t order_key(float x)
 {
@@ -73,10 +76,10 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *scratch, int *to
 
 __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p)
 {
-    __shared__ uint32_t hist[2048];
     __shared__ int scratch[kWarps + 1];
     __shared__ uint32_t sh_digit;
     __shared__ int sh_above;
+    __shared__ int sh_count;
 
     pdl_trigger();
     pdl_wait();
@@ -107,58 +110,127 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p)
     fz.c2 = __double2float_rn(p.lambda / Z);
     fz.inv_tau = __double2float_rn(1.0 / tau);
 
-    // ---- radix select of the K-th largest key ------------------------------------------
-    uint32_t prefix = 0, pmask = 0;
-    int krem = K;
-#pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-        const int nbits = pass < 2 ? 11 : 10;
-        const int nb = 1 << nbits;
-        for (int i = tid; i < nb; i += NT)
-            hist[i] = 0u;
-        __syncthreads();
-        for (int base = 0; base < nC; base += 4 * NT) {
-            // four consecutive candidates per thread: their loads are in flight together
-            uint32_t k[4];
+    // Keys of up to kKeyCache candidates are kept in shared memory by the first pass. The
+    // candidates that share the threshold's top 12 bits are then gathered into a list (at
+    // most kListCap keys) and the two refining passes run over that list only.
+    // Dynamic shared memory: kSub sub-histograms (one per group of warps, so fewer lanes
+    // collide on a bin), the gathered list, then the key cache when it is used.
+    extern __shared__ uint32_t dyn[];
+    const bool cached = p.cache_keys && nC <= kKeyCache;
+    uint32_t *hist = dyn;
+    uint32_t *lst = dyn + kSub * 4096;
+    uint32_t *kcache = lst + kListCap;
+    const int sub = (tid >> 5) % kSub;
+    auto key_at = [&](int i) -> uint32_t { return cached ? kcache[i] : fz.key(i); };
+    int nbins = 4096;
+    auto count = [&](bool part, uint32_t digit) {
+        if (part)
+            atomicAdd(&hist[sub * nbins + digit], 1u);
+    };
+    // the bin, scanning from the top, where the running count first reaches krem
+    auto bin_count = [&](int bin) {
+        int h = 0;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = base + 4 * tid + e;
-                k[e] = i < nC ? fz.key(i) : 0u;
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const bool part = (base + 4 * tid + e < nC) && ((k[e] & pmask) == prefix);
-                const uint32_t digit = (k[e] >> shift) & static_cast<uint32_t>(nb - 1);
-                const unsigned act = __ballot_sync(0xffffffffu, part);
-                if (part) {
-                    const unsigned peers = __match_any_sync(act, digit);
-                    if (lane == __ffs(peers) - 1)
-                        atomicAdd(&hist[digit], static_cast<uint32_t>(__popc(peers)));
-                }
-            }
-        }
-        __syncthreads();
-        // thread t owns bins nb-1-per*t ... (descending); find the bin where the count of
-        // keys above it first reaches krem
+        for (int s2 = 0; s2 < kSub; ++s2)
+            h += static_cast<int>(hist[s2 * nbins + bin]);
+        return h;
+    };
+    auto find_digit = [&](int nb, int krem_now) {
         const int per = nb / NT;
         int mine = 0;
         for (int j = 0; j < per; ++j)
-            mine += static_cast<int>(hist[nb - 1 - (per * tid + j)]);
+            mine += bin_count(nb - 1 - (per * tid + j));
         int total;
         int before = block_exclusive_scan(mine, scratch, &total);
         for (int j = 0; j < per; ++j) {
             const int bin = nb - 1 - (per * tid + j);
-            const int h = static_cast<int>(hist[bin]);
-            if (before < krem && before + h >= krem) {
+            const int h = bin_count(bin);
+            if (before < krem_now && before + h >= krem_now) {
                 sh_digit = static_cast<uint32_t>(bin);
                 sh_above = before;
             }
             before += h;
         }
         __syncthreads();
+    };
+
+    // ---- radix select of the K-th largest key ------------------------------------------
+    // pass 0: top 12 bits of every candidate
+    for (int i = tid; i < kSub * 4096; i += NT)
+        hist[i] = 0u;
+    if (tid == 0)
+        sh_count = 0;
+    __syncthreads();
+    for (int base = 0; base < nC; base += 4 * NT) {
+        // four candidates per thread, NT apart: coalesced loads, all in flight together
+        uint32_t k[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = base + e * NT + tid;
+            k[e] = i < nC ? fz.key(i) : 0u;
+            if (cached && i < nC)
+                kcache[i] = k[e];
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            count(base + e * NT + tid < nC, k[e] >> 20);
+    }
+    __syncthreads();
+    int krem = K;
+    find_digit(4096, krem);
+    const uint32_t d0 = sh_digit;
+    uint32_t prefix = d0 << 20, pmask = 0xFFF00000u;
+    krem -= sh_above;
+    const int n_lst = bin_count(static_cast<int>(d0));
+    const bool use_list = n_lst <= kListCap;
+    __syncthreads();
+    if (use_list) {
+        for (int base = 0; base < nC; base += NT) {
+            const int i = base + tid;
+            const uint32_t k = i < nC ? key_at(i) : 0u;
+            const bool in = i < nC && (k >> 20) == d0;
+            const unsigned bal = __ballot_sync(0xffffffffu, in);
+            int wbase = 0;
+            if (lane == 0 && bal)
+                wbase = atomicAdd(&sh_count, __popc(bal));
+            wbase = __shfl_sync(0xffffffffu, wbase, 0);
+            if (in)
+                lst[wbase + __popc(bal & ((1u << lane) - 1u))] = k;
+        }
+        __syncthreads();
+    }
+    // passes 1 and 2: 10-bit digits, over the gathered list (or every candidate)
+#pragma unroll 1
+    for (int pass = 1; pass < 3; ++pass) {
+        const int shift = pass == 1 ? 10 : 0;
+        nbins = 1024;
+        for (int i = tid; i < kSub * 1024; i += NT)
+            hist[i] = 0u;
+        __syncthreads();
+        if (use_list) {
+            for (int base = 0; base < n_lst; base += NT) {
+                const int i = base + tid;
+                const uint32_t k = i < n_lst ? lst[i] : 0u;
+                count(i < n_lst && (k & pmask) == prefix, (k >> shift) & 1023u);
+            }
+        } else {
+            for (int base = 0; base < nC; base += 4 * NT) {
+                uint32_t k[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = base + e * NT + tid;
+                    k[e] = i < nC ? key_at(i) : 0u;
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    count(base + e * NT + tid < nC && (k[e] & pmask) == prefix,
+                          (k[e] >> shift) & 1023u);
+            }
+        }
+        __syncthreads();
+        find_digit(1024, krem);
         prefix |= sh_digit << shift;
-        pmask |= static_cast<uint32_t>(nb - 1) << shift;
+        pmask |= 1023u << shift;
         krem -= sh_above;
         __syncthreads();
     }
@@ -166,42 +238,51 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p)
     const int need_eq = krem;     // how many keys equal to thr are taken (lowest first)
 
     // ---- ordered compaction ------------------------------------------------------------
-    int out_base = 0, eq_base = 0;
-    for (int base = 0; base < nC; base += 4 * NT) {
-        uint32_t k[4];
-        int n_eq = 0;
+    // A chosen candidate's slot = (keys > thr before it) + min(keys == thr before it,
+    // need_eq), so one block scan of packed (equal << 16 | greater) counts per chunk of
+    // 8 x NT candidates places every chosen index in ascending order.
+    int gt_base = 0, eq_base = 0;
+    for (int base = 0; base < nC; base += 8 * NT) {
+        uint32_t k[8];
+        if (cached && base + 8 * tid + 7 < nC) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(kcache + base + 8 * tid);
+            const uint4 c4 = *reinterpret_cast<const uint4 *>(kcache + base + 8 * tid + 4);
+            k[0] = a.x; k[1] = a.y; k[2] = a.z; k[3] = a.w;
+            k[4] = c4.x; k[5] = c4.y; k[6] = c4.z; k[7] = c4.w;
+        } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int i = base + 4 * tid + e;
-            k[e] = i < nC ? fz.key(i) : 0u;
-            n_eq += (i < nC && k[e] == thr) ? 1 : 0;
-        }
-        int tot_eq;
-        int eq_before = eq_base + block_exclusive_scan(n_eq, scratch, &tot_eq);
-        bool sel[4];
-        int n_sel = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int i = base + 4 * tid + e;
-            sel[e] = false;
-            if (i < nC) {
-                if (k[e] > thr) {
-                    sel[e] = true;
-                } else if (k[e] == thr) {
-                    sel[e] = eq_before < need_eq;
-                    ++eq_before;
-                }
+            for (int e = 0; e < 8; ++e) {
+                const int i = base + 8 * tid + e;
+                k[e] = i < nC ? key_at(i) : 0u;
             }
-            n_sel += sel[e] ? 1 : 0;
         }
-        int tot_sel;
-        int pos = out_base + block_exclusive_scan(n_sel, scratch, &tot_sel);
+        int n_gt = 0, n_eq = 0;
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if (sel[e])
-                out[pos++] = S + base + 4 * tid + e;
-        out_base += tot_sel;
-        eq_base += tot_eq;
+        for (int e = 0; e < 8; ++e) {
+            const bool in = base + 8 * tid + e < nC;
+            n_gt += (in && k[e] > thr) ? 1 : 0;
+            n_eq += (in && k[e] == thr) ? 1 : 0;
+        }
+        int tot;
+        const int packed = block_exclusive_scan((n_eq << 16) | n_gt, scratch, &tot);
+        int gt_before = gt_base + (packed & 0xFFFF);
+        int eq_before = eq_base + (packed >> 16);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int i = base + 8 * tid + e;
+            if (i >= nC)
+                break;
+            if (k[e] > thr) {
+                out[gt_before + min(eq_before, need_eq)] = S + i;
+                ++gt_before;
+            } else if (k[e] == thr) {
+                if (eq_before < need_eq)
+                    out[gt_before + eq_before] = S + i;
+                ++eq_before;
+            }
+        }
+        gt_base += tot & 0xFFFF;
+        eq_base += tot >> 16;
     }
     if (tid == 0)
         p.sel_cnt[u] = K;
@@ -211,7 +292,16 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p)
 
 cudaError_t launch_select(const SelectParams &p, cudaStream_t stream)
 {
-    const cudaError_t e = launch_pdl(select_kernel, dim3(p.n_units), dim3(NT), 0, stream, p);
+    const size_t smem =
+        (kSub * 4096 + kListCap + (p.cache_keys ? kKeyCache : 0)) * sizeof(uint32_t);
+    {
+        const cudaError_t a =
+            cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (a != cudaSuccess)
+            return a;
+    }
+    const cudaError_t e = launch_pdl(select_kernel, dim3(p.n_units), dim3(NT), smem, stream, p);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -52,6 +52,7 @@ struct SelectParams {
     double lambda;
     int32_t *sel_idx;           // [units][n_select]
     int32_t *sel_cnt;           // [units]
+    int cache_keys;             // candidates (host bound) fit the shared-memory key cache
 };
 
 // Launchers (return the cudaGetLastError() of the launch).
