@@ -146,13 +146,21 @@ def barrier(world):
 
 
 def allreduce_max(x: float, world: int) -> float:
+    """Slowest rank's value (timing is taken as the max over ranks)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_tokens_per_s(world: int, tokens_per_step: int, steps: int, ms_max: float) -> float:
+    """Whole-job throughput of N independent replicas: every rank's tokens over the slowest
+    rank's time."""
+    return world * tokens_per_step * steps / (ms_max / 1000.0)
 
 
 def bytes_model(wl, slow, sel_rows):
@@ -300,7 +308,7 @@ def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=N
     if clk:
         clk.__exit__()
         res["clocks"] = clk.summary()
-    res["value"] = world * tokens_per_run * k_steps / (ms / 1000.0)
+    res["value"] = aggregate_tokens_per_s(world, tokens_per_run, k_steps, ms)
     res["ms_per_run"] = ms / k_steps
     res["tokens_per_run"] = tokens_per_run
     res["slow_steps"] = int(slow.any(axis=1).sum())

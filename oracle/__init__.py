@@ -47,6 +47,12 @@ def load(path: str | None = None):
     lib.sfi_oracle_schedule.restype = None
     lib.sfi_oracle_schedule_tokens.argtypes = [i32, P, P, i32, i32, P]
     lib.sfi_oracle_schedule_tokens.restype = None
+    lib.sfi_oracle_log2f.argtypes = [C.c_float]
+    lib.sfi_oracle_log2f.restype = C.c_float
+    lib.sfi_oracle_refine_scores.argtypes = [i32, i32, i32, i32, i32, f64, i32, C.c_float, P, i32,
+                                             C.c_float, C.c_float, P, P]
+    lib.sfi_oracle_key_norms.argtypes = [i32, i32, P, P]
+    lib.sfi_oracle_key_norms.restype = None
     lib.sfi_oracle_attend_batch.argtypes = [i32, i32, i32, i32, P, P, P, P, i32, P, P, P, i32]
     return lib
 
@@ -159,6 +165,34 @@ def schedule_tokens(tokens, trigger_ids, t_max):
     lib().sfi_oracle_schedule_tokens(tokens.shape[0], _p(tokens), _p(trig), trig.shape[0], t_max,
                                      _p(slow))
     return slow
+
+
+def log2f(x: float) -> float:
+    return lib().sfi_oracle_log2f(x)
+
+
+def refine_scores(L, S, W, tau, lam, f32, geometric=False, nu=0.0, knorm=None, radius=0,
+                  gamma=1.0, mu=0.0):
+    """Refined Selector scores of the H heads of one (layer, sequence): f32 [H][L] evidence,
+    knorm [H][L] key norms (or None). Returns fp32 [H][n_C]."""
+    f32 = _c(f32, np.float32)
+    H = f32.shape[0]
+    n = max(0, L - W - S)
+    out = np.zeros((H, max(n, 1)), dtype=np.float32)
+    kn = None if knorm is None else _c(knorm, np.float32)
+    n = lib().sfi_oracle_refine_scores(H, L, S, W, tau, lam, 1 if geometric else 0, nu,
+                                       None if kn is None else _p(kn), radius, gamma, mu,
+                                       _p(f32), _p(out))
+    if n < 0:
+        raise ValueError("oracle refine failed")
+    return out[:, :n]
+
+
+def key_norms(k):
+    k = _c(k, np.uint16)
+    out = np.zeros(k.shape[0], dtype=np.float32)
+    lib().sfi_oracle_key_norms(k.shape[0], k.shape[1], _p(k), _p(out))
+    return out
 
 
 def attend_batch(q, k, v, n_rows, rows=None, want_f: bool = False, threads: int = 0):

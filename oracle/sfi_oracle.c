@@ -245,6 +245,156 @@ int sfi_oracle_fused_scores(int L, int S, int W, int tau, double lambda, const f
     return n;
 }
 
+/*
+ * log2 of an fp32 value in fp32, from the definition x = 2^e m, m in [1, 2):
+ *     log2 x = e + (2/ln 2) * atanh(t),  t = (m - 1)/(m + 1) in [0, 1/3],
+ * with atanh(t) = t + t^3/3 + ... + t^11/11 (truncation < 2e-7 relative). Every step is
+ * an IEEE round-to-nearest fp32 operation in a fixed order, so any IEEE host computes the
+ * same bits. log2(0) = -inf; negative or NaN input gives NaN.
+ */
+float sfi_oracle_log2f(float x)
+{
+    if (x != x || x < 0.0f)
+        return NAN;
+    if (x == 0.0f)
+        return -INFINITY;
+    if (isinf(x))
+        return INFINITY;
+    uint32_t u;
+    memcpy(&u, &x, sizeof u);
+    int e = (int)((u >> 23) & 0xFFu);
+    if (e == 0) { /* subnormal: scale by 2^32 first */
+        const float y = x * 4294967296.0f;
+        memcpy(&u, &y, sizeof u);
+        e = (int)((u >> 23) & 0xFFu) - 32;
+    }
+    e -= 127;
+    const uint32_t mb = (u & 0x007FFFFFu) | 0x3F800000u;
+    float m;
+    memcpy(&m, &mb, sizeof m);
+    const float t = (m - 1.0f) / (m + 1.0f);
+    const float t2 = t * t;
+    /* fl32(1/11), fl32(1/9), ..., fl32(2/ln 2) as exact literals */
+    float s = 0x1.745d18p-4f;
+    s = s * t2 + 0x1.c71c72p-4f;
+    s = s * t2 + 0x1.24924ap-3f;
+    s = s * t2 + 0x1.99999ap-3f;
+    s = s * t2 + 0x1.555556p-2f;
+    s = s * t2 + 1.0f;
+    const float two_over_ln2 = 0x1.715476p+1f;
+    return (float)e + two_over_ln2 * (t * s);
+}
+
+/*
+ * Selector refinements ([Sum 2B]): the pages name them without formulas; the readings:
+ *   prior with a key-norm term ("avoid tokens with extremely high key norms"):
+ *       rt_j = fl32(min(1, d_j/tau)) * g_j,  g_j = min(1, fl32(nu / ||k_j||))  (nu = 0: g = 1),
+ *       still divided by the closed-form Z of the plain ramp (the term only removes mass);
+ *   fusion: arithmetic s = fl32(fl32(c1 f) + fl32(c2 rt)) as sfi_oracle_fused_scores, or the
+ *       geometric (log-linear) mixture of the reverse-KL objective, scored in the log domain:
+ *       s = fl32(fl32(fl32(1 - lambda) log2 f) + fl32(fl32(lambda) log2 fl32(c2 rt / lambda)))
+ *       (lambda = 0: s = log2 f; the log score ranks like the geometric mixture);
+ *   Soft-NMS within a head: a candidate strictly below the largest score of its candidate
+ *       neighbours at distance 1..radius is scaled by gamma: s' = fl32(gamma s);
+ *   cross-head exclusivity: with T_j = s'_0j + ... + s'_(H-1)j summed in head order,
+ *       s''_hj = fl32(s'_hj - fl32(mu' fl32(T_j - s'_hj))),  mu' = fl32(mu / (H - 1)).
+ * f: fp32 [H][L] evidence of the H kv heads of one (layer, sequence); knorm: fp32 [H][L]
+ * key norms or NULL; out: fp32 [H][n_C] refined scores of candidates S .. L-W-1.
+ * Returns n_C.
+ */
+int sfi_oracle_refine_scores(int H, int L, int S, int W, int tau, double lambda, int geometric,
+                             float nu, const float *knorm, int radius, float gamma, float mu,
+                             const float *f, float *out)
+{
+    const int n = sfi_oracle_num_candidates(L, S, W);
+    if (n == 0)
+        return 0;
+    const double Z = sfi_oracle_prior_norm(n, tau);
+    const float c1 = (float)(1.0 - lambda);
+    const float c2 = (float)(lambda / Z);
+    const float inv_tau = (float)(1.0 / (double)tau);
+    const float lam_f = (float)lambda;
+    float *s = (float *)malloc(sizeof(float) * (size_t)H * n);
+    if (!s)
+        return -1;
+    for (int h = 0; h < H; ++h)
+        for (int i = 0; i < n; ++i) {
+            const int j = S + i;
+            const int d = (L - W) - j;
+            float rt = (float)d * inv_tau;
+            if (rt > 1.0f)
+                rt = 1.0f;
+            if (nu > 0.0f && knorm) {
+                float g = nu / knorm[(size_t)h * L + j];
+                if (g > 1.0f)
+                    g = 1.0f;
+                rt = rt * g;
+            }
+            const float fj = f[(size_t)h * L + j];
+            float v;
+            if (!geometric) {
+                const float a = c1 * fj;
+                const float b = c2 * rt;
+                v = a + b;
+            } else {
+                const float a = c1 * sfi_oracle_log2f(fj);
+                float b = 0.0f;
+                if (lambda > 0.0) {
+                    const float r = (c2 * rt) / lam_f;
+                    b = lam_f * sfi_oracle_log2f(r);
+                }
+                v = lambda < 1.0 ? a + b : b;
+            }
+            s[(size_t)h * n + i] = v;
+        }
+    /* Soft-NMS within each head */
+    for (int h = 0; h < H; ++h)
+        for (int i = 0; i < n; ++i) {
+            const float v = s[(size_t)h * n + i];
+            float best = -INFINITY;
+            for (int k = 1; k <= radius; ++k) {
+                if (i - k >= 0 && s[(size_t)h * n + i - k] > best)
+                    best = s[(size_t)h * n + i - k];
+                if (i + k < n && s[(size_t)h * n + i + k] > best)
+                    best = s[(size_t)h * n + i + k];
+            }
+            out[(size_t)h * n + i] = (radius > 0 && v < best) ? gamma * v : v;
+        }
+    /* cross-head exclusivity */
+    if (mu != 0.0f && H > 1) {
+        const float mu1 = (float)((double)mu / (double)(H - 1));
+        for (int i = 0; i < n; ++i) {
+            float T = 0.0f;
+            for (int h = 0; h < H; ++h)
+                T = T + out[(size_t)h * n + i];
+            for (int h = 0; h < H; ++h) {
+                const float v = out[(size_t)h * n + i];
+                const float others = T - v;
+                const float pen = mu1 * others;
+                s[(size_t)h * n + i] = v - pen;
+            }
+        }
+        memcpy(out, s, sizeof(float) * (size_t)H * n);
+    }
+    free(s);
+    return n;
+}
+
+/* Key norms ||k_j||_2 of bf16 rows: squares summed in fp32 in dimension order, then the
+ * correctly rounded fp32 square root. k: [L][D]; out: [L]. */
+void sfi_oracle_key_norms(int L, int D, const uint16_t *k, float *out)
+{
+    for (int j = 0; j < L; ++j) {
+        float acc = 0.0f;
+        for (int d = 0; d < D; ++d) {
+            const float x = (float)sfi_oracle_bf16_to_double(k[(size_t)j * D + d]);
+            const float sq = x * x;
+            acc = acc + sq;
+        }
+        out[j] = sqrtf(acc);
+    }
+}
+
 /* IEEE total order of an fp32 value as an unsigned key (NaN lowest): used so that the
  * order of scores is a total order on bit patterns. */
 static uint32_t order_key(float x)

@@ -9,6 +9,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_pins as pins
+from tests import test_oracle_refine_pins as refine_pins
 
 MUTANTS = {
     "dropped_scale": ("z[j] = dot * scale;", "z[j] = dot;"),
@@ -20,8 +21,9 @@ MUTANTS = {
     "evidence_not_averaged": ("f[j] = s / (double)G;", "f[j] = s;"),
     "tie_break_to_higher_index": ("return (x->idx > y->idx) - (x->idx < y->idx);",
                                   "return (x->idx < y->idx) - (x->idx > y->idx);"),
-    "prior_distance_off_by_one": ("const int d = (L - W) - j;", "const int d = (L - W) - j - 1;"),
-    "prior_wrong_sign": ("const float b = c2 * rt;", "const float b = -c2 * rt;"),
+    "prior_distance_off_by_one": ("const int d = (L - W) - j;\n        float rt = (float)d * inv_tau;\n        if (rt > 1.0f)\n            rt = 1.0f;\n        const float a",
+                                  "const int d = (L - W) - j - 1;\n        float rt = (float)d * inv_tau;\n        if (rt > 1.0f)\n            rt = 1.0f;\n        const float a"),
+    "prior_wrong_sign": ("const float b = c2 * rt;\n        s[i] = a + b;", "const float b = -c2 * rt;\n        s[i] = a + b;"),
     "window_off_by_one": ("int w0 = L_now - W;", "int w0 = L_now - W + 1;"),
     "candidates_include_window": ("const int n = L - W - S;", "const int n = L - S;"),
     "tmax_strict": ("mask[t - 1] || (t_max > 0 && t - last >= t_max)",
@@ -29,17 +31,25 @@ MUTANTS = {
     "first_step_not_slow": ("int s = (t == 0) || mask[t - 1]", "int s = (t < 0) || mask[t - 1]"),
     "token_trigger_off_by_one": ("if (tokens[t - 1] == trigger_ids[i])",
                                  "if (tokens[t] == trigger_ids[i])"),
+    "nms_non_strict": ("(radius > 0 && v < best)", "(radius > 0 && v <= best)"),
+    "exclusivity_wrong_sign": ("s[(size_t)h * n + i] = v - pen;", "s[(size_t)h * n + i] = v + pen;"),
+    "geometric_weights_swapped": ("const float a = c1 * sfi_oracle_log2f(fj);",
+                                  "const float a = lam_f * sfi_oracle_log2f(fj);"),
+    "key_norm_term_inverted": ("float g = nu / knorm[(size_t)h * L + j];",
+                               "float g = knorm[(size_t)h * L + j] / nu;"),
+    "log2_series_term_dropped": ("s = s * t2 + 0x1.99999ap-3f;", "s = s * t2;"),
 }
 
-PIN_TESTS = [name for name in dir(pins) if name.startswith("test_")]
+PIN_TESTS = [(pins, name) for name in dir(pins) if name.startswith("test_")] + \
+    [(refine_pins, name) for name in dir(refine_pins) if name.startswith("test_")]
 
 
 def run_pins():
     """Run every pin (with its parametrisations); return the names that failed."""
     import inspect
     failed = []
-    for name in PIN_TESTS:
-        fn = getattr(pins, name)
+    for mod, name in PIN_TESTS:
+        fn = getattr(mod, name)
         marks = getattr(fn, "pytestmark", [])
         cases = [{}]
         for m in marks:
