@@ -394,6 +394,36 @@ def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=N
         }
         res["modes"]["sfi_vs_dense_speedup"] = (res["modes"]["sfi_mix"]["tokens_per_s"] /
                                                 res["modes"]["dense_only"]["tokens_per_s"])
+    if extras:
+        # Selector refinements (Soft-NMS, cross-head exclusivity, key-norm prior term) on the
+        # last slow step's evidence, timed with events on the stream
+        import sparse_long_context_sfi_gb300 as sfi
+        st.kv.max_len = int(wl.len0.max()) + cfg.steps
+        norms = torch.zeros_like(st.scores)
+        refined = torch.empty_like(st.scores)
+        bud = sfi.SfiBudget(n_sink=cfg.n_sink, n_window=cfg.n_window, n_select=cfg.n_select,
+                            prior_tau=cfg.prior_tau, lambda_=cfg.lam, nms_radius=2,
+                            nms_gamma=0.5, excl_mu=0.3, norm_nu=float(1.5 * cfg.head_dim ** 0.5))
+        with torch.cuda.stream(stream):
+            reps = 10
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            sfi.sfi_key_norms(st.kv, norms, stream=stream)
+            sfi.sfi_refine_scores(st.kv, st.scores, norms, bud, refined, stream=stream)
+            torch.cuda.synchronize()
+            ev[0].record()
+            for _ in range(reps):
+                sfi.sfi_key_norms(st.kv, norms, stream=stream)
+            ev[1].record()
+            for _ in range(reps):
+                sfi.sfi_refine_scores(st.kv, st.scores, norms, bud, refined, stream=stream)
+            ev[2].record()
+            torch.cuda.synchronize()
+        n_pos = float(sum(int(x) + cfg.steps for x in wl.len0)) * cfg.n_layers * cfg.n_kv_heads
+        res["refinements"] = {
+            "key_norms_us": ev[0].elapsed_time(ev[1]) * 1e3 / reps,
+            "refine_us": ev[1].elapsed_time(ev[2]) * 1e3 / reps,
+            "options": "nms_radius 2, nms_gamma 0.5, excl_mu 0.3, norm_nu 1.5 sqrt(D)",
+            "key_norms_gbs": n_pos * 256 / (ev[0].elapsed_time(ev[1]) * 1e-3 / reps) / 1e9}
     if dense_only_runs:
         g_dense = capture(run_of(slow, dense_only=True))
         ms_d = time_graph(g_dense, dense_only_runs, 1)
@@ -481,6 +511,7 @@ def main():
             "gpu_launches": res["launches_per_run"] * args.steps,
             "clocks": res.get("clocks"),
             "modes": res.get("modes"),
+            "refinements": res.get("refinements"),
             "other_workloads": others,
             "device_error": res["device_error"],
         }

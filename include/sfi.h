@@ -92,6 +92,12 @@ typedef struct sfi_budget {
     int32_t n_select;
     int32_t prior_tau;
     double lambda;
+    /* Selector refinements, read by sfi_refine_scores only (each is off when zero):     */
+    int32_t nms_radius;  /* Soft-NMS: neighbours at distance 1..nms_radius in a head     */
+    float nms_gamma;     /* Soft-NMS: factor for a candidate below its neighbourhood max */
+    float excl_mu;       /* cross-head exclusivity strength in [0, 1]                    */
+    float norm_nu;       /* key-norm prior term: prior scaled by min(1, norm_nu/||k||)   */
+    int32_t geometric;   /* 1: geometric (log-linear) mixture instead of arithmetic      */
 } sfi_budget;
 
 /*
@@ -168,6 +174,36 @@ sfi_status sfi_dense_decode_attn(const sfi_kv_cache *kv, const void *q, void *ou
  */
 sfi_status sfi_select(const sfi_kv_cache *kv, const float *scores_f, const sfi_budget *budget,
                       const sfi_sparse_mem *mem, const uint8_t *active, void *stream);
+
+/*
+ * Key norms for the Selector's key-norm prior term (summary 2B: the prior counters tokens
+ * with extremely high key norms). norms: fp32 [n_layers][batch][n_kv_heads][capacity];
+ * norms[u][j] = ||k_j||_2 for j < seq_len[b] of active sequences: squares of the bf16
+ * values summed in fp32 in dimension order, then the correctly rounded square root.
+ */
+sfi_status sfi_key_norms(const sfi_kv_cache *kv, float *norms, const uint8_t *active,
+                         void *stream);
+
+/*
+ * Refined Selector scores (summary 2B: the fused scores are refined by Soft-NMS within a
+ * head and a soft cross-head competition before Top-K; the pages give no formulas, these
+ * are the library's readings). For every (layer, sequence) of an active sequence and every
+ * candidate j in [n_sink, L - n_window), all kv heads h:
+ *   rt_hj = fl32(min(1, d_j / prior_tau)), times min(1, fl32(norm_nu / key_norms[h][j]))
+ *           when norm_nu > 0 (key_norms may then not be NULL);
+ *   s_hj  = arithmetic: fl32(fl32(c1 f_hj) + fl32(c2 rt_hj))  (c1, c2 as in sfi_select), or
+ *           geometric:  fl32(c1 log2 f_hj) + fl32(lambda log2 fl32(fl32(c2 rt_hj) / lambda))
+ *           in fp32 with the library's own log2 (log-domain score of the geometric mixture);
+ *   Soft-NMS: s'_hj = fl32(nms_gamma s_hj) if s_hj is strictly below the largest s_hi of the
+ *           candidates i with 1 <= |i - j| <= nms_radius, else s_hj;
+ *   exclusivity: s''_hj = fl32(s'_hj - fl32(mu' fl32(T_j - s'_hj))), T_j = sum over heads of
+ *           s'_hj in head order, mu' = fl32(excl_mu / (n_kv_heads - 1)).
+ * refined: fp32 [units][capacity], written at the candidate positions. Select on it with
+ * sfi_select and lambda = 0 (which keeps the scores as they are). n_kv_heads <= 16.
+ */
+sfi_status sfi_refine_scores(const sfi_kv_cache *kv, const float *scores_f,
+                             const float *key_norms, const sfi_budget *budget, float *refined,
+                             const uint8_t *active, void *stream);
 
 /*
  * Pack the sparse memory (summary section 3, memory-coalesced sparse kernel): for every

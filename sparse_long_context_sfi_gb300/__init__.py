@@ -28,7 +28,8 @@ SFI_DEVERR_LENGTH = 0x8
 
 ENTRY_POINTS = (
     "sfi_status_string", "sfi_version", "sfi_workspace_bytes", "sfi_workspace_init",
-    "sfi_append_kv", "sfi_dense_decode_attn", "sfi_select", "sfi_compact",
+    "sfi_append_kv", "sfi_dense_decode_attn", "sfi_select", "sfi_compact", "sfi_key_norms",
+    "sfi_refine_scores",
     "sfi_sparse_decode_attn", "sfi_sparse_decode_attn_static", "sfi_schedule",
     "sfi_schedule_tokens", "sfi_decode_run", "sfi_read_error", "sfi_clear_error",
 )
@@ -46,7 +47,9 @@ class SfiKvCache(C.Structure):
 
 class SfiBudget(C.Structure):
     _fields_ = [("n_sink", C.c_int32), ("n_window", C.c_int32), ("n_select", C.c_int32),
-                ("prior_tau", C.c_int32), ("lambda_", C.c_double)]
+                ("prior_tau", C.c_int32), ("lambda_", C.c_double), ("nms_radius", C.c_int32),
+                ("nms_gamma", C.c_float), ("excl_mu", C.c_float), ("norm_nu", C.c_float),
+                ("geometric", C.c_int32)]
 
 
 class SfiSparseMem(C.Structure):
@@ -89,6 +92,8 @@ def lib():
             "sfi_dense_decode_attn": (C.c_int, [KV, P, P, I32, P, P, P, SZ, P]),
             "sfi_select": (C.c_int, [KV, P, BD, MEM, P, P]),
             "sfi_compact": (C.c_int, [KV, BD, MEM, P, P]),
+            "sfi_key_norms": (C.c_int, [KV, P, P, P]),
+            "sfi_refine_scores": (C.c_int, [KV, P, P, BD, P, P, P]),
             "sfi_sparse_decode_attn": (C.c_int, [KV, MEM, BD, P, P, I32, P, P, SZ, P]),
             "sfi_sparse_decode_attn_static": (C.c_int, [KV, MEM, BD, P, P, I32, P, P]),
             "sfi_schedule": (C.c_int, [I32, P, I32, P]),
@@ -166,6 +171,18 @@ def sfi_select(kv: SfiKvCache, scores_f, budget: SfiBudget, mem: SfiSparseMem, a
                stream=None):
     _check("sfi_select", lib().sfi_select(C.byref(kv), _ptr(scores_f), C.byref(budget),
                                           C.byref(mem), _ptr(active), _stream(stream)))
+
+
+def sfi_key_norms(kv: SfiKvCache, norms, active=None, stream=None):
+    _check("sfi_key_norms", lib().sfi_key_norms(C.byref(kv), _ptr(norms), _ptr(active),
+                                                _stream(stream)))
+
+
+def sfi_refine_scores(kv: SfiKvCache, scores_f, key_norms, budget: SfiBudget, refined,
+                      active=None, stream=None):
+    _check("sfi_refine_scores", lib().sfi_refine_scores(
+        C.byref(kv), _ptr(scores_f), _ptr(key_norms), C.byref(budget), _ptr(refined),
+        _ptr(active), _stream(stream)))
 
 
 def sfi_compact(kv: SfiKvCache, budget: SfiBudget, mem: SfiSparseMem, active=None, stream=None):

@@ -26,7 +26,7 @@ SYNTH_LIB = os.path.join(ROOT, "synth", "libsynth.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
-SOURCES = ["attn.cu", "select.cu", "kvops.cu", "api.cpp"]
+SOURCES = ["attn.cu", "select.cu", "refine.cu", "kvops.cu", "api.cpp"]
 
 
 def nvcc() -> str:

@@ -368,6 +368,60 @@ sfi_status sfi_select(const sfi_kv_cache *kv, const float *scores_f, const sfi_b
     return launch_status(launch_select(p, as_stream(stream)));
 }
 
+sfi_status sfi_key_norms(const sfi_kv_cache *kv, float *norms, const uint8_t *active,
+                         void *stream)
+{
+    sfi_status st = check_kv(kv);
+    if (st != SFI_OK)
+        return st;
+    if (!norms)
+        return SFI_ERR_INVALID_ARG;
+    return launch_status(launch_key_norms(kv->k, norms, kv->seq_len, active, kv->n_layers,
+                                          kv->batch, kv->n_kv_heads, kv->capacity, kv->page_size,
+                                          kv->n_pages, kv->max_pages_per_seq, kv->page_table,
+                                          kv->max_len, kv->err, as_stream(stream)));
+}
+
+sfi_status sfi_refine_scores(const sfi_kv_cache *kv, const float *scores_f,
+                             const float *key_norms, const sfi_budget *budget, float *refined,
+                             const uint8_t *active, void *stream)
+{
+    sfi_status st = check_kv(kv);
+    if (st != SFI_OK)
+        return st;
+    if ((st = check_budget(budget)) != SFI_OK)
+        return st;
+    if (!scores_f || !refined || budget->nms_radius < 0 ||
+        !(budget->nms_gamma >= 0.f && budget->nms_gamma <= 1.f) ||
+        !(budget->excl_mu >= 0.f && budget->excl_mu <= 1.f) || !(budget->norm_nu >= 0.f) ||
+        (budget->norm_nu > 0.f && !key_norms))
+        return SFI_ERR_INVALID_ARG;
+    if (kv->n_kv_heads > 16)
+        return SFI_ERR_UNSUPPORTED;
+    RefineParams p;
+    std::memset(&p, 0, sizeof p);
+    p.f = scores_f;
+    p.key_norms = key_norms;
+    p.refined = refined;
+    p.capacity = kv->capacity;
+    p.batch = kv->batch;
+    p.n_kv_heads = kv->n_kv_heads;
+    p.seq_len = kv->seq_len;
+    p.active = active;
+    p.n_sink = budget->n_sink;
+    p.n_window = budget->n_window;
+    p.prior_tau = budget->prior_tau;
+    p.lambda = budget->lambda;
+    p.geometric = budget->geometric ? 1 : 0;
+    p.norm_nu = budget->norm_nu;
+    p.nms_radius = budget->nms_radius;
+    p.nms_gamma = budget->nms_gamma;
+    p.excl_mu = budget->excl_mu;
+    const int max_cand = kv->max_len - budget->n_window - budget->n_sink;
+    return launch_status(
+        launch_refine(p, kv->n_layers * kv->batch, max_cand > 0 ? max_cand : 1, as_stream(stream)));
+}
+
 sfi_status sfi_compact(const sfi_kv_cache *kv, const sfi_budget *budget,
                        const sfi_sparse_mem *mem, const uint8_t *active, void *stream)
 {

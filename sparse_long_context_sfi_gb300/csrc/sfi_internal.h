@@ -55,7 +55,30 @@ struct SelectParams {
     int cache_keys;             // candidates (host bound) fit the shared-memory key cache
 };
 
+struct RefineParams {
+    const float *f;             // evidence [units][capacity]
+    const float *key_norms;     // [units][capacity] or null
+    float *refined;             // [units][capacity]
+    int capacity, batch, n_kv_heads;
+    const int32_t *seq_len;
+    const uint8_t *active;
+    int n_sink, n_window, prior_tau;
+    double lambda;
+    int geometric;
+    float norm_nu;
+    int nms_radius;
+    float nms_gamma;
+    float excl_mu;
+};
+
 // Launchers (return the cudaGetLastError() of the launch).
+cudaError_t launch_refine(const RefineParams &p, int n_layer_seq, int max_cand,
+                          cudaStream_t stream);
+cudaError_t launch_key_norms(const void *k, float *norms, const int32_t *seq_len,
+                             const uint8_t *active, int n_layers, int batch, int n_kv_heads,
+                             int capacity, int page_size, int n_pages, int max_pages,
+                             const int32_t *page_table, int max_len, uint32_t *err,
+                             cudaStream_t stream);
 cudaError_t launch_attention(bool dense, int group, const CUtensorMap &tm_k,
                              const CUtensorMap &tm_v, const CUtensorMap &tm_q,
                              const CUtensorMap &tm_kc, const CUtensorMap &tm_vc,

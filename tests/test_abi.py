@@ -82,7 +82,7 @@ def test_native_scheduler_matches_oracle(lib, t_max):
 def test_decode_plan_layout_matches_header(lib):
     """ctypes structs mirror the C layouts (field offsets of the 64-bit ABI)."""
     assert C.sizeof(sfi.SfiKvCache) == 10 * 4 + 5 * 8
-    assert C.sizeof(sfi.SfiBudget) == 4 * 4 + 8
+    assert C.sizeof(sfi.SfiBudget) == 4 * 4 + 8 + 5 * 4 + 4  # padded to 8
     assert C.sizeof(sfi.SfiSparseMem) == 5 * 8
     assert sfi.SfiDecodePlan.masks.offset == 64 and sfi.SfiDecodePlan.events.offset == 80
     assert C.sizeof(sfi.SfiDecodePlan) == 88
