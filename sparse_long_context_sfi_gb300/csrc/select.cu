@@ -3,9 +3,10 @@
 // s = (1 - lambda) f + lambda r, then Top-K positions, ties to the lower position.
 //
 // One CTA of 1024 threads per unit. The K-th largest score is found by an exact radix
-// select on the scores' order-preserving 32-bit keys (digits of 11, 11 and 10 bits, one
-// shared-memory histogram pass each); a final ordered pass compacts the chosen positions
-// in ascending order with block-wide scans. The fused score uses round-to-nearest
+// select on the scores' order-preserving 32-bit keys: a 12-bit digit over every candidate,
+// then two 10-bit digits over the candidates gathered from the threshold's 12-bit bin
+// (shared-memory histograms); one ordered pass then writes the chosen positions in
+// ascending order with a single block-wide scan per chunk. The fused score uses round-to-nearest
 // multiplies and adds with no contraction, so it is bit-reproducible on any IEEE host.
 #include "sfi_device.cuh"
 

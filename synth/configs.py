@@ -1,8 +1,9 @@
 """The five SFI decode-attention workloads, as plain data.
 
 Each workload is one attention layer stack decoded for a number of steps after a
-prefill. Shapes, budgets and key models follow the workload list this repository is
-measured on; the readings of unstated details are listed in the design doc.
+prefill: GQA layers with 4 query heads per kv head and head dim 128 (Llama-3-8B's 32 query
+and 8 kv heads in all but the 4K case), a sparse budget of sinks + recent window +
+selected positions, and a seeded boundary mask that decides the slow steps.
 """
 from __future__ import annotations
 
