@@ -9,6 +9,7 @@
  *                sfi_select               evidence + positional prior -> Top-K positions
  *                sfi_compact              pack sinks + selected rows contiguously
  *   fast step    sfi_sparse_decode_attn   attention over the packed rows + recent window
+ *                sfi_fast_decode_step     the append and that attention in one launch
  *   host         sfi_schedule             trigger policy: slow or fast for each step
  *
  * Conventions for every call:
@@ -227,6 +228,22 @@ sfi_status sfi_sparse_decode_attn(const sfi_kv_cache *kv, const sfi_sparse_mem *
                                   size_t ws_bytes, void *stream);
 
 /*
+ * A whole fast decode step in one launch (blog, "How SFI Works"; summary 2A "Fast Steps" and
+ * section 3): the result of sfi_append_kv(kv, k_new, v_new, active) followed by
+ * sfi_sparse_decode_attn(kv, mem, budget, q, out, ...). Each active sequence's new K and V
+ * rows (k_new/v_new: device bf16 [n_layers][batch][n_kv_heads][128]) are written at position
+ * seq_len[b] of the cache and attended as the last row of the recent window, and seq_len[b]
+ * is advanced by one. kv->max_len bounds seq_len before the append (as for sfi_append_kv);
+ * SFI_ERR_CAPACITY when max_len + 1 > capacity. Same q/out layouts, workspace and errors as
+ * sfi_sparse_decode_attn. The workspace must have been cleared by sfi_workspace_init once;
+ * calls leave its counters at zero again.
+ */
+sfi_status sfi_fast_decode_step(const sfi_kv_cache *kv, const sfi_sparse_mem *mem,
+                                const sfi_budget *budget, const void *k_new, const void *v_new,
+                                const void *q, void *out, int32_t out_fp32, const uint8_t *active,
+                                void *ws, size_t ws_bytes, void *stream);
+
+/*
  * The fast step for callers that cannot allocate device memory. The paper has no
  * counterpart of this call: it is an interface convenience. Some callers get only their
  * input and output buffers (for example a plug-in inside a host framework that owns all
@@ -269,10 +286,11 @@ sfi_status sfi_schedule_tokens(int32_t steps, const int32_t *tokens, const int32
 
 /*
  * A whole decode run on one stream (blog "How SFI Works": the two-speed loop). For each
- * step t: sfi_append_kv with row t of k_new/v_new; then, for the sequences whose slow flag
- * is set, sfi_dense_decode_attn (with evidence) -> sfi_select -> sfi_compact, and for the
- * others sfi_sparse_decode_attn. Nothing is synchronised, so the run can be captured in a
- * CUDA graph and replayed (the caller restores seq_len before each replay).
+ * step t, with row t of k_new/v_new: for the sequences whose slow flag is set,
+ * sfi_append_kv -> sfi_dense_decode_attn (with evidence) -> sfi_select -> sfi_compact; for
+ * the others sfi_fast_decode_step (append and sparse attention in one launch). Nothing is
+ * synchronised, so the run can be captured in a CUDA graph and replayed (the caller
+ * restores seq_len before each replay).
  *   slow      host uint8 [n_steps][batch], e.g. from sfi_schedule per sequence
  *   q         device bf16 [n_steps][n_layers][batch][n_q_heads][128]
  *   k_new/v_new device bf16 [n_steps][n_layers][batch][n_kv_heads][128]

@@ -30,7 +30,8 @@ ENTRY_POINTS = (
     "sfi_status_string", "sfi_version", "sfi_workspace_bytes", "sfi_workspace_init",
     "sfi_append_kv", "sfi_dense_decode_attn", "sfi_select", "sfi_compact", "sfi_key_norms",
     "sfi_refine_scores",
-    "sfi_sparse_decode_attn", "sfi_sparse_decode_attn_static", "sfi_schedule",
+    "sfi_sparse_decode_attn", "sfi_fast_decode_step", "sfi_sparse_decode_attn_static",
+    "sfi_schedule",
     "sfi_schedule_tokens", "sfi_decode_run", "sfi_read_error", "sfi_clear_error",
 )
 
@@ -95,6 +96,7 @@ def lib():
             "sfi_key_norms": (C.c_int, [KV, P, P, P]),
             "sfi_refine_scores": (C.c_int, [KV, P, P, BD, P, P, P]),
             "sfi_sparse_decode_attn": (C.c_int, [KV, MEM, BD, P, P, I32, P, P, SZ, P]),
+            "sfi_fast_decode_step": (C.c_int, [KV, MEM, BD, P, P, P, P, I32, P, P, SZ, P]),
             "sfi_sparse_decode_attn_static": (C.c_int, [KV, MEM, BD, P, P, I32, P, P]),
             "sfi_schedule": (C.c_int, [I32, P, I32, P]),
             "sfi_schedule_tokens": (C.c_int, [I32, P, P, I32, I32, P]),
@@ -195,6 +197,15 @@ def sfi_sparse_decode_attn(kv: SfiKvCache, mem: SfiSparseMem, budget: SfiBudget,
     _check("sfi_sparse_decode_attn", lib().sfi_sparse_decode_attn(
         C.byref(kv), C.byref(mem), C.byref(budget), _ptr(q), _ptr(out), 1 if out_fp32 else 0,
         _ptr(active), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def sfi_fast_decode_step(kv: SfiKvCache, mem: SfiSparseMem, budget: SfiBudget, k_new, v_new, q,
+                         out, out_fp32: bool, ws, ws_bytes: int, active=None, stream=None):
+    """Append of k_new/v_new and the fast step's attention in one launch; kv.max_len bounds
+    seq_len before the append."""
+    _check("sfi_fast_decode_step", lib().sfi_fast_decode_step(
+        C.byref(kv), C.byref(mem), C.byref(budget), _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(out),
+        1 if out_fp32 else 0, _ptr(active), _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def sfi_sparse_decode_attn_static(kv: SfiKvCache, mem: SfiSparseMem, budget: SfiBudget, q, out,

@@ -111,7 +111,7 @@ int sm_count()
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-    size_t tickets_dense, tickets_sparse, stats, part_dense, part_sparse, zbuf, total;
+    size_t tickets_dense, tickets_sparse, append_ctr, stats, part_dense, part_sparse, zbuf, total;
 };
 
 WsLayout ws_layout(const sfi_kv_cache *kv, int sms)
@@ -123,6 +123,7 @@ WsLayout ws_layout(const sfi_kv_cache *kv, int sms)
     size_t o = 0;
     w.tickets_dense = o;  o = align256(o + units * sizeof(int));
     w.tickets_sparse = o; o = align256(o + units * sizeof(int));
+    w.append_ctr = o;     o = align256(o + sizeof(int));
     w.stats = o;          o = align256(o + units * g * sizeof(float2));
     w.part_dense = o;     o = align256(o + part);
     w.part_sparse = o;    o = align256(o + part);
@@ -225,10 +226,13 @@ sfi_status dense_impl(const sfi_kv_cache *kv, const void *q, void *out, int32_t 
     return SFI_OK;
 }
 
+// The fast step; with k_new/v_new given, the append of the new rows is fused in (kv->max_len
+// then bounds the lengths before the append).
 sfi_status sparse_impl(const sfi_kv_cache *kv, const sfi_sparse_mem *mem,
                        const sfi_budget *budget, const void *q, void *out, int32_t out_fp32,
                        const uint8_t *active, void *ws, size_t ws_bytes, void *stream,
-                       cudaEvent_t e0, cudaEvent_t e1)
+                       cudaEvent_t e0, cudaEvent_t e1, const void *k_new = nullptr,
+                       const void *v_new = nullptr)
 {
     sfi_status st = check_kv(kv);
     if (st != SFI_OK)
@@ -238,6 +242,13 @@ sfi_status sparse_impl(const sfi_kv_cache *kv, const sfi_sparse_mem *mem,
     if (!mem || !mem->kc || !mem->vc || !mem->sel_cnt || !mem->rows || !q || !out ||
         !aligned16(q) || !aligned16(mem->kc) || !aligned16(mem->vc))
         return SFI_ERR_INVALID_ARG;
+    const bool fused = k_new != nullptr || v_new != nullptr;
+    if (fused) {
+        if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
+            return SFI_ERR_INVALID_ARG;
+        if (kv->max_len + 1 > kv->capacity)
+            return SFI_ERR_CAPACITY;
+    }
     const int sms = sm_count();
     if (sms <= 0)
         return SFI_ERR_CUDA;
@@ -251,6 +262,11 @@ sfi_status sparse_impl(const sfi_kv_cache *kv, const sfi_sparse_mem *mem,
     p.out_fp32 = out_fp32 ? 1 : 0;
     p.partials = reinterpret_cast<float *>(base + w.part_sparse);
     p.tickets = reinterpret_cast<int *>(base + w.tickets_sparse);
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_cache = kv->k;
+    p.v_cache = kv->v;
+    p.append_counter = reinterpret_cast<int *>(base + w.append_ctr);
     p.comp_rows = mem->rows;
     p.sel_cnt = mem->sel_cnt;
     p.comp_cap = budget->n_sink + budget->n_select;
@@ -266,8 +282,20 @@ sfi_status sparse_impl(const sfi_kv_cache *kv, const sfi_sparse_mem *mem,
         !make_map(&tkc, mem->kc, static_cast<uint64_t>(units) * p.comp_cap, 64u) ||
         !make_map(&tvc, mem->vc, static_cast<uint64_t>(units) * p.comp_cap, 64u))
         return SFI_ERR_CUDA;
+    // Few units: a cluster of up to 8 CTAs per unit (one unit per cluster, partials merged
+    // in distributed shared memory). Otherwise one CTA per SM over contiguous tile ranges.
+    int cluster = 1;
+    if (units * 2 <= sms) {
+        long long cmax = sms / units;
+        cmax = cmax < 8 ? cmax : 8;
+        cmax = cmax < p.tiles_per_unit ? cmax : p.tiles_per_unit;
+        if (cmax >= 2)
+            cluster = sparse_cluster_size(g, static_cast<int>(units), static_cast<int>(cmax));
+    }
+    p.cluster = cluster;
     const long long t_upper = units * p.tiles_per_unit;
-    const int grid = static_cast<int>(t_upper < sms ? t_upper : sms);
+    const int grid = cluster > 1 ? static_cast<int>(units) * cluster
+                                 : static_cast<int>(t_upper < sms ? t_upper : sms);
     if (e0 && record_event(e0, as_stream(stream)) != cudaSuccess)
         return SFI_ERR_CUDA;
     if (launch_attention(false, g, tk, tv, tq, tkc, tvc, p, grid, as_stream(stream)) != cudaSuccess)
@@ -364,7 +392,6 @@ sfi_status sfi_select(const sfi_kv_cache *kv, const float *scores_f, const sfi_b
     p.lambda = budget->lambda;
     p.sel_idx = mem->sel_idx;
     p.sel_cnt = mem->sel_cnt;
-    p.cache_keys = (kv->max_len - budget->n_window - budget->n_sink) <= 32768 ? 1 : 0;
     return launch_status(launch_select(p, as_stream(stream)));
 }
 
@@ -447,6 +474,17 @@ sfi_status sfi_sparse_decode_attn(const sfi_kv_cache *kv, const sfi_sparse_mem *
 {
     return sparse_impl(kv, mem, budget, q, out, out_fp32, active, ws, ws_bytes, stream, nullptr,
                        nullptr);
+}
+
+sfi_status sfi_fast_decode_step(const sfi_kv_cache *kv, const sfi_sparse_mem *mem,
+                                const sfi_budget *budget, const void *k_new, const void *v_new,
+                                const void *q, void *out, int32_t out_fp32, const uint8_t *active,
+                                void *ws, size_t ws_bytes, void *stream)
+{
+    if (!k_new || !v_new)
+        return SFI_ERR_INVALID_ARG;
+    return sparse_impl(kv, mem, budget, q, out, out_fp32, active, ws, ws_bytes, stream, nullptr,
+                       nullptr, k_new, v_new);
 }
 
 sfi_status sfi_sparse_decode_attn_static(const sfi_kv_cache *kv, const sfi_sparse_mem *mem,
@@ -538,11 +576,15 @@ sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
             return SFI_ERR_INVALID_ARG;
         const uint8_t *m_slow = mixed ? plan->masks + static_cast<size_t>(t) * 2 * B : nullptr;
         const uint8_t *m_fast = mixed ? m_slow + B : nullptr;
+        const void *k_new = static_cast<const char *>(plan->k_new) + t * kv_step * 2;
+        const void *v_new = static_cast<const char *>(plan->v_new) + t * kv_step * 2;
+        // The slow sequences' rows are appended here; the fast ones' inside the fast step.
         k.max_len = plan->len_start + t;
-        st = sfi_append_kv(&k, static_cast<const char *>(plan->k_new) + t * kv_step * 2,
-                           static_cast<const char *>(plan->v_new) + t * kv_step * 2, nullptr, stream);
-        if (st != SFI_OK)
-            return st;
+        if (plan->dense_only || n_slow > 0) {
+            st = sfi_append_kv(&k, k_new, v_new, plan->dense_only ? nullptr : m_slow, stream);
+            if (st != SFI_OK)
+                return st;
+        }
         k.max_len = plan->len_start + t + 1;
         const void *q = static_cast<const char *>(plan->q) + t * q_step * 2;
         void *out = static_cast<char *>(plan->out) + t * o_step;
@@ -562,8 +604,10 @@ sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
                 return st;
         }
         if (n_slow < B) {
+            k.max_len = plan->len_start + t;  // the fused append's bound before appending
             if ((st = sparse_impl(&k, mem, budget, q, out, plan->out_fp32, m_fast, ws, ws_bytes,
-                                  stream, n_slow > 0 ? nullptr : e0, n_slow > 0 ? nullptr : e1)) != SFI_OK)
+                                  stream, n_slow > 0 ? nullptr : e0, n_slow > 0 ? nullptr : e1,
+                                  k_new, v_new)) != SFI_OK)
                 return st;
         }
     }

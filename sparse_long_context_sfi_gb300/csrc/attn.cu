@@ -45,7 +45,7 @@ constexpr int kFlagLast = 2;    // last tile of a segment
 // Optional per-CTA timeline for tuning (compile with -DSFI_TRACE): globaltimer stamps at
 // fixed checkpoints, read back through sfi_trace_read. Off in normal builds.
 #ifdef SFI_TRACE
-__device__ unsigned long long g_sfi_trace[1024][16];
+__device__ unsigned long long g_sfi_trace[1024][32];
 #define SFI_STAMP(slot) (g_sfi_trace[blockIdx.x & 1023][(slot)] = global_timer_ns())
 #define SFI_TRACE_SET(slot, v) (g_sfi_trace[blockIdx.x & 1023][(slot)] = (v))
 #else
@@ -66,12 +66,16 @@ struct Ctrl {
     uint64_t s_full[2], s_free[2], p_full[2], o_full[2], o_free[2], q_free[2];
     uint64_t gsync;             // softmax-group barrier (one arrive per warp)
     uint64_t drain;             // MMA drain on exit
+    uint64_t unit_meta;         // clustered: this CTA's unit and tile slice are known
+    uint64_t cl_ready;          // clustered: every CTA of the cluster has its partial in place
+    uint64_t cl_done;           // clustered: every CTA has finished reading the partials
     TileMeta meta[kStages];
     float red_max[2][4][8];
     float red_sum[4][16];
     uint32_t tmem_base;
     int abort;
     int last_flag;
+    int cl_tiles, cl_t0, cl_live, cl_rows, cl_sel;  // clustered: slice of the unit's tiles
     int P;
     long long T, TL, g0, g1;
     int nt[kMaxBatch];
@@ -175,6 +179,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         mbar_init(&c.gsync, 4);
         mbar_init(&c.drain, 1);
+        mbar_init(&c.unit_meta, 1);
+        mbar_init(&c.cl_ready, static_cast<uint32_t>(p.cluster > 1 ? p.cluster : 1));
+        mbar_init(&c.cl_done, static_cast<uint32_t>(p.cluster > 1 ? p.cluster : 1));
         mbar_fence_init();
         tma_prefetch_map(&tm_k);
         tma_prefetch_map(&tm_v);
@@ -184,6 +191,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tma_prefetch_map(&tm_vc);
         }
         c.abort = 0;
+        c.cl_live = 0;
     }
     if (warp == 1) {
         tmem_alloc(&c.tmem_base, kTmemCols);
@@ -193,65 +201,127 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int i = tid; i < 4 * kOpBytes / 16; i += kAttnThreads)
         reinterpret_cast<uint4 *>(smem + kQOff)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
+    // Clustered fast step: one unit per cluster, its tiles split evenly over the cluster's
+    // CTAs, which merge their partials through distributed shared memory. The cluster
+    // barrier publishes the mbarrier initialisation and the TMEM base cluster-wide.
+    const bool clustered = !DENSE && p.cluster > 1;
+    const bool fused = !DENSE && p.k_new != nullptr;
+    if (clustered) {
+        tc_fence_before();
+        cluster_sync_all();
+        tc_fence_after();
+    }
 
     // ---- tile space: per-sequence tile counts and this CTA's range --------------------
     pdl_wait();
     if (threadIdx.x == 0)
         SFI_STAMP(1);
-    for (int b = tid; b < B; b += kAttnThreads) {
-        const int L = p.seq_len[b];
-        int act = p.active ? p.active[b] : 1;
-        if (act && (L < 0 || L > p.max_len || L > p.capacity)) {
-            raise_error(p.err, 0x8u);  // SFI_DEVERR_LENGTH
-            act = 0;
+    long long g0 = 0, g1 = 0;
+    int n_tiles = 0;
+    if (!clustered) {
+        for (int b = tid; b < B; b += kAttnThreads) {
+            const int L0 = p.seq_len[b];
+            const int L = fused ? L0 + 1 : L0;  // with the fused append: the new row included
+            int act = p.active ? p.active[b] : 1;
+            if (act && (L0 < 0 || L0 > p.max_len || L > p.capacity)) {
+                raise_error(p.err, 0x8u);  // SFI_DEVERR_LENGTH
+                act = 0;
+            }
+            c.nt[b] = (act && L > 0) ? (DENSE ? (L + kTile - 1) / kTile : p.tiles_per_unit) : 0;
+            c.len[b] = L;
         }
-        c.nt[b] = (act && L > 0) ? (DENSE ? (L + kTile - 1) / kTile : p.tiles_per_unit) : 0;
-        c.len[b] = L;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        long long acc = 0;
-        for (int b = 0; b < B; ++b) {
-            c.pre[b] = static_cast<int>(acc * Hkv);
-            acc += c.nt[b];
-        }
-        c.TL = acc * Hkv;
-        c.T = c.TL * p.n_layers;
-        c.P = static_cast<int>(c.T < gridDim.x ? c.T : gridDim.x);
-        const long long P = c.P > 0 ? c.P : 1;
-        if (DENSE) {
-            // stream-K: equal contiguous tile ranges (balances ragged lengths)
-            c.g0 = static_cast<long long>(blockIdx.x) * c.T / P;
-            c.g1 = static_cast<long long>(blockIdx.x + 1) * c.T / P;
-        } else {
-            // every unit has the same tile count: ranges never straddle two units
-            const long long nt = p.tiles_per_unit, ua = c.T / nt, cta = blockIdx.x;
-            if (P >= ua) {
-                const long long q = P / ua, r = P % ua;
-                long long a, k, nc;
-                if (cta < r * (q + 1)) {
-                    a = cta / (q + 1);
-                    k = cta % (q + 1);
-                    nc = q + 1;
-                } else {
-                    a = r + (cta - r * (q + 1)) / q;
-                    k = (cta - r * (q + 1)) % q;
-                    nc = q;
-                }
-                c.g0 = a * nt + k * nt / nc;
-                c.g1 = a * nt + (k + 1) * nt / nc;
+        __syncthreads();
+        if (tid == 0) {
+            long long acc = 0;
+            for (int b = 0; b < B; ++b) {
+                c.pre[b] = static_cast<int>(acc * Hkv);
+                acc += c.nt[b];
+            }
+            c.TL = acc * Hkv;
+            c.T = c.TL * p.n_layers;
+            c.P = static_cast<int>(c.T < gridDim.x ? c.T : gridDim.x);
+            const long long P = c.P > 0 ? c.P : 1;
+            if (DENSE) {
+                // stream-K: equal contiguous tile ranges (balances ragged lengths)
+                c.g0 = static_cast<long long>(blockIdx.x) * c.T / P;
+                c.g1 = static_cast<long long>(blockIdx.x + 1) * c.T / P;
             } else {
-                c.g0 = (cta * ua / P) * nt;
-                c.g1 = ((cta + 1) * ua / P) * nt;
+                // every unit has the same tile count: ranges never straddle two units
+                const long long nt = p.tiles_per_unit, ua = c.T / nt, cta = blockIdx.x;
+                if (P >= ua) {
+                    const long long q = P / ua, r = P % ua;
+                    long long a, k, nc;
+                    if (cta < r * (q + 1)) {
+                        a = cta / (q + 1);
+                        k = cta % (q + 1);
+                        nc = q + 1;
+                    } else {
+                        a = r + (cta - r * (q + 1)) / q;
+                        k = (cta - r * (q + 1)) % q;
+                        nc = q;
+                    }
+                    c.g0 = a * nt + k * nt / nc;
+                    c.g1 = a * nt + (k + 1) * nt / nc;
+                } else {
+                    c.g0 = (cta * ua / P) * nt;
+                    c.g1 = ((cta + 1) * ua / P) * nt;
+                }
             }
         }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // CTAs beyond the tile count (short contexts) only tear down.
+        g0 = c.g0;
+        g1 = c.g1;
+        n_tiles = static_cast<int>(blockIdx.x) < c.P ? static_cast<int>(g1 - g0) : 0;
+    } else {
+        // The producer warp reads the unit's length, flag, packed rows and selection count
+        // in one round and publishes them; the other roles wait for that.
+        if (warp == 0) {
+            const int u = static_cast<int>(blockIdx.x) / p.cluster;
+            const int rank = static_cast<int>(blockIdx.x) % p.cluster;
+            const int b = (u / Hkv) % B;
+            int v = 0;
+            if (lane == 0)
+                v = p.seq_len[b];
+            else if (lane == 1)
+                v = p.active ? p.active[b] : 1;
+            else if (lane == 2)
+                v = p.comp_rows[u];
+            else if (lane == 3)
+                v = p.sel_cnt[u];
+            const int L0 = __shfl_sync(0xffffffffu, v, 0);
+            const int act = __shfl_sync(0xffffffffu, v, 1);
+            const int rows = __shfl_sync(0xffffffffu, v, 2);
+            const int sel = __shfl_sync(0xffffffffu, v, 3);
+            const int L = fused ? L0 + 1 : L0;
+            bool live = act != 0;
+            if (live && (L0 < 0 || L0 > p.max_len || L > p.capacity)) {
+                if (lane == 0)
+                    raise_error(p.err, 0x8u);  // SFI_DEVERR_LENGTH
+                live = false;
+            }
+            live = live && L > 0;
+            if (lane == 0) {
+                const int nt = p.tiles_per_unit, C = p.cluster;
+                c.cl_t0 = rank * nt / C;
+                c.cl_tiles = live ? (rank + 1) * nt / C - rank * nt / C : 0;
+                c.cl_live = live ? 1 : 0;
+                c.cl_rows = rows;
+                c.cl_sel = sel;
+                c.len[0] = L;
+                mbar_arrive(&c.unit_meta);
+            }
+        }
+        if (mbar_wait(&c.unit_meta, 0, &c.abort)) {
+            n_tiles = c.cl_tiles;
+            g0 = c.cl_t0;
+            g1 = g0 + n_tiles;
+        } else {
+            fail(c, p.err);
+        }
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    // CTAs beyond the tile count (short contexts) only tear down.
-    const long long g0 = c.g0, g1 = c.g1;
-    const int n_tiles = static_cast<int>(blockIdx.x) < c.P ? static_cast<int>(g1 - g0) : 0;
     if (tid == 0) {
         SFI_STAMP(2);
         SFI_TRACE_SET(12, n_tiles);
@@ -267,13 +337,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const uint64_t pol = policy_evict_first();
             // decode the first tile of the range
             long long g = g0;
-            int layer = static_cast<int>(g / c.TL);
-            int r = static_cast<int>(g - static_cast<long long>(layer) * c.TL);
-            int b = 0;
-            while (b + 1 < B && (c.nt[b] == 0 || c.pre[b] + Hkv * c.nt[b] <= r))
-                ++b;
-            int kvh = (r - c.pre[b]) / c.nt[b];
-            int t = (r - c.pre[b]) - kvh * c.nt[b];
+            int layer, b, kvh, t;
+            if (clustered) {  // a slice of one unit's tiles
+                const int u0 = static_cast<int>(blockIdx.x) / p.cluster;
+                layer = u0 / (Hkv * B);
+                b = (u0 / Hkv) % B;
+                kvh = u0 % Hkv;
+                t = static_cast<int>(g0);
+            } else {
+                layer = static_cast<int>(g / c.TL);
+                const int r = static_cast<int>(g - static_cast<long long>(layer) * c.TL);
+                b = 0;
+                while (b + 1 < B && (c.nt[b] == 0 || c.pre[b] + Hkv * c.nt[b] <= r))
+                    ++b;
+                kvh = (r - c.pre[b]) / c.nt[b];
+                t = (r - c.pre[b]) - kvh * c.nt[b];
+            }
+            auto ntiles_of = [&](int bb) { return clustered ? p.tiles_per_unit : c.nt[bb]; };
             int seg = -1, issued = 0;
             int seg_len = 0, seg_rows_c = 0, seg_ws = 0;
             const int my_q = lane >> 2, my_op = lane & 3;  // page / block and (K|V, half)
@@ -287,9 +367,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             };
             if (paged_dense)
                 load_page(b, t);
+            // Fused append: this lane's 128-byte half of unit u's new K or V row goes to cache
+            // row `dst_row` (of the tensor maps' row view) before the lane's own TMA box, which
+            // covers that row, reads it back through the async proxy.
+            auto append_half = [&](int uu, int kvsel, int hf, long long dst_row) {
+                const uint4 *src = static_cast<const uint4 *>(kvsel ? p.v_new : p.k_new) +
+                                   static_cast<size_t>(uu) * 16 + hf * 8;
+                uint4 *dst = static_cast<uint4 *>(kvsel ? p.v_cache : p.k_cache) +
+                             static_cast<size_t>(dst_row) * 16 + hf * 8;
+                uint4 x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    x[e] = src[e];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    dst[e] = x[e];
+                fence_proxy_async_global();
+            };
             bool ok = true;
             for (int i = 0; i < n_tiles; ++i, ++g) {
-                if (i > 0 && ++t == c.nt[b]) {
+                if (i > 0 && ++t == ntiles_of(b)) {
                     t = 0;
                     if (++kvh == Hkv) {
                         kvh = 0;
@@ -298,7 +395,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                 b = 0;
                                 ++layer;
                             }
-                        } while (c.nt[b] == 0);
+                        } while (ntiles_of(b) == 0);
                     }
                 }
                 const int s = i % kStages;
@@ -306,15 +403,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     ok = mbar_wait(&c.empty[s], ((i / kStages) & 1) ^ 1, &c.abort);
                 const int u = (layer * B + b) * Hkv + kvh;
                 const bool first = (i == 0) || (t == 0);
-                const bool last = (i == n_tiles - 1) || (t == c.nt[b] - 1);
+                const bool last = (i == n_tiles - 1) || (t == ntiles_of(b) - 1);
                 if (first) {
                     ++seg;
                     if (lane == 0 && ok && seg >= 2)
                         ok = mbar_wait(&c.q_free[seg & 1], ((seg >> 1) - 1) & 1, &c.abort);
-                    seg_len = c.len[b];
+                    seg_len = clustered ? c.len[0] : c.len[b];
                     if (!DENSE) {
-                        const int rows_c = max(0, min(__ldg(p.comp_rows + u), p.comp_cap));
-                        const int n_s = max(0, rows_c - max(0, __ldg(p.sel_cnt + u)));
+                        const int rows_c = max(0, min(clustered ? c.cl_rows : __ldg(p.comp_rows + u),
+                                                      p.comp_cap));
+                        const int n_s = max(0, rows_c - max(0, clustered ? c.cl_sel : __ldg(p.sel_cnt + u)));
                         seg_rows_c = rows_c;
                         seg_ws = max(n_s, seg_len - p.n_window);
                     }
@@ -387,6 +485,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                 y = u * p.capacity + p0;
                                 row0 = rr0;
                                 rows = 16;
+                                if (fused && L - 1 < p0 + 16)  // the box holds the new row
+                                    append_half(u, kv, half, static_cast<long long>(y) + (L - 1 - p0));
                                 if (my_op == 0)
                                     mask_rows(valid, rr0, rr0 + vr);
                             }
@@ -406,6 +506,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                     y = ((layer * p.n_pages + page) * Hkv + kvh) * 16;
                                     row0 = rr0;
                                     rows = 16;
+                                    if (fused && L - 1 < lp * 16 + 16)  // the page holds the new row
+                                        append_half(u, kv, half, static_cast<long long>(y) + (L - 1 - lp * 16));
                                     if (my_op == 0)
                                         mask_rows(valid, rr0 + r0, rr0 + r1);
                                 }
@@ -467,6 +569,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int j = max(0, issued - kStages); j < issued; ++j)
                     mbar_wait(&c.full[j % kStages], (j / kStages) & 1, nullptr);
         }
+        // Fused append: this CTA has read seq_len (set-up); the last CTA of the grid to get
+        // here advances the length of every sequence whose new row was appended.
+        if (fused) {
+            int is_last = 0;
+            if (lane == 0)
+                is_last = atomic_add_acq_rel_gpu(p.append_counter, 1) == static_cast<int>(gridDim.x) - 1;
+            if (__shfl_sync(0xffffffffu, is_last, 0)) {
+                int32_t *len = const_cast<int32_t *>(p.seq_len);
+                for (int bb = lane; bb < B; bb += 32) {
+                    const int L0 = len[bb];
+                    const int act = p.active ? p.active[bb] : 1;
+                    if (act && L0 >= 0 && L0 <= p.max_len && L0 + 1 <= p.capacity)
+                        len[bb] = L0 + 1;
+                }
+                if (lane == 0)
+                    *p.append_counter = 0;
+            }
+        }
     } else if (warp == 1) {
         // ================================ MMA issuer =====================================
         if (lane == 0 && n_tiles > 0) {
@@ -518,10 +638,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     umma_bf16(tmem + bb * 16, a, bd, idesc_s, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&c.s_full[bb]);
+                if (i == 0)
+                    SFI_STAMP(11);
                 if (flags & kFlagLast)
                     umma_commit(&c.q_free[seg & 1]);
                 if (i > 0 && !pv(i - 1))
                     ok = false;
+                if (i == 1)
+                    SFI_STAMP(15);
             }
             if (ok && !pv(n_tiles - 1))
                 ok = false;
@@ -541,12 +665,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         float m_run[G], le[G], lr[G], acc[G];
         // the tile waiting for its O^T accumulation
         float a_alpha[G], a_m[G], a_le[G], a_lr[G];
+        // clustered: this CTA's (max, sum) of its slice, with acc[] its unnormalised output
+        float fin_m[G], fin_lr[G];
         int a_flags = 0, a_unit = 0;
         bool ok = true;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             m_run[h] = -INFINITY;
             le[h] = lr[h] = acc[h] = 0.f;
+            fin_m[h] = -INFINITY;
+            fin_lr[h] = 0.f;
         }
 
         auto finalize = [&](int u, const float (&fm)[G], const float (&fle)[G],
@@ -594,6 +722,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // acquire fence and the second barrier make all partials visible to its threads.
             if (!group_sync(c, gphase, lane))
                 return false;
+            if (row == 0)
+                SFI_STAMP(24);
             if (row == 0) {
                 fence_acq_rel_gpu();
                 const int tk = atomicAdd(&p.tickets[u], 1);
@@ -603,11 +733,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     fence_acq_rel_gpu();
                 }
                 c.last_flag = is_last;
+                SFI_STAMP(25);
             }
             if (!group_sync(c, gphase, lane))
                 return false;
             if (!c.last_flag)
                 return true;
+            if (row == 0)
+                SFI_STAMP(26);
             // One-pass online merge starting from this CTA's own partial (in registers);
             // the other contributors are read four at a time so their loads overlap.
             float M[G], Le[G], Lr[G];
@@ -654,6 +787,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                 }
             }
+            if (row == 0)
+                SFI_STAMP(27);
 #pragma unroll
             for (int h = 0; h < G; ++h)
                 o[h] = Lr[h] > 0.f ? o[h] / Lr[h] : 0.f;
@@ -679,6 +814,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (a_flags & kFlagLast) {
                 if (row == 0)
                     SFI_STAMP(6);
+                if (clustered) {  // merged across the cluster after the loop
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        fin_m[h] = a_m[h];
+                        fin_lr[h] = a_lr[h];
+                    }
+                    return true;
+                }
                 if (!finalize(a_unit, a_m, a_le, a_lr))
                     return false;
                 if (row == 0)
@@ -699,6 +842,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             if (i == 0 && row == 0)
                 SFI_STAMP(5);
+            if (i == 1 && row == 0)
+                SFI_STAMP(16);
             const int u = c.meta[s].unit;
             const int tile = c.meta[s].tile;
             const int flags = c.meta[s].flags;
@@ -716,6 +861,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&c.s_free[bb]);
+            if (i == 0 && row == 0)
+                SFI_STAMP(13);
+            if (i == 1 && row == 0)
+                SFI_STAMP(17);
             float z[G];
 #pragma unroll
             for (int h = 0; h < G; ++h)
@@ -741,6 +890,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 ok = false;
                 break;
             }
+            if (i == 0 && row == 0)
+                SFI_STAMP(14);
+            if (i == 1 && row == 0)
+                SFI_STAMP(18);
             float alpha[G];
             uint8_t *pb = smem + kPOff + bb * kOpBytes;
 #pragma unroll
@@ -769,10 +922,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     reinterpret_cast<uint4 *>(vrow + kChunkBytes)[k] = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
+            if (i == 1 && row == 0)
+                SFI_STAMP(19);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&c.p_full[bb]);
+            if (i == 1 && row == 0)
+                SFI_STAMP(20);
             float fm[G], fle[G], flr[G];
             if (flags & kFlagLast) {
 #pragma unroll
@@ -799,6 +956,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 ok = false;
                 break;
             }
+            if (i == 1 && row == 0)
+                SFI_STAMP(21);
             // this tile now waits for its accumulation
 #pragma unroll
             for (int h = 0; h < G; ++h) {
@@ -819,6 +978,79 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             ok = false;
         if (row == 0)
             SFI_STAMP(9);
+        if (clustered && c.cl_live) {
+            // ---- merge the cluster's partials through distributed shared memory ----------
+            // Every CTA of a live cluster takes part, even after a failed wait, so that no
+            // peer waits for it; outputs are written only when everything succeeded. The
+            // partial goes to this CTA's stage-0 buffer, idle now: acc [G][128], m [G], l [G].
+            const int C = p.cluster;
+            const int rank = static_cast<int>(blockIdx.x) % C;
+            const int u = static_cast<int>(blockIdx.x) / C;
+            float *part = reinterpret_cast<float *>(smem);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                part[h * kHeadDim + row] = acc[h];
+                if (row == h) {
+                    part[G * kHeadDim + h] = fin_m[h];
+                    part[G * kHeadDim + G + h] = fin_lr[h];
+                }
+            }
+            bool good = group_sync(c, gphase, lane) && ok;  // all four warps' writes are done
+            if (row == 0)
+                for (int r = 0; r < C; ++r)
+                    mbar_arrive_cluster(map_to_rank(&c.cl_ready, static_cast<uint32_t>(r)));
+            good = mbar_wait_cluster(&c.cl_ready, 0, kWaitTimeoutNs) && good;
+            if (row == 0)
+                SFI_STAMP(24);
+            if (good) {
+                // this CTA finishes dims [d0, d0 + nd) of every head
+                const int d0 = rank * kHeadDim / C, nd = (rank + 1) * kHeadDim / C - d0;
+                for (int o = row; o < nd * G; o += 4 * 32) {
+                    const int h = o % G, d = d0 + o / G;
+                    float mr[8], lrr[8], ar[8];
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        if (r < C) {
+                            const uint32_t base = map_to_rank(part, static_cast<uint32_t>(r));
+                            mr[r] = ld_cluster_f32(base + 4u * (G * kHeadDim + h));
+                            lrr[r] = ld_cluster_f32(base + 4u * (G * kHeadDim + G + h));
+                            ar[r] = ld_cluster_f32(base + 4u * (h * kHeadDim + d));
+                        }
+                    }
+                    float M = -INFINITY;
+#pragma unroll
+                    for (int r = 0; r < 8; ++r)
+                        if (r < C)
+                            M = fmaxf(M, mr[r]);
+                    float Lr = 0.f, O = 0.f;
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        if (r < C) {
+                            const float w = (mr[r] == -INFINITY) ? 0.f : exp2f(mr[r] - M);
+                            Lr = fmaf(w, lrr[r], Lr);
+                            O = fmaf(w, ar[r], O);
+                        }
+                    }
+                    const float v = Lr > 0.f ? O / Lr : 0.f;
+                    const size_t idx = (static_cast<size_t>(u) * G + h) * kHeadDim + d;
+                    if (p.out_fp32)
+                        static_cast<float *>(p.out)[idx] = v;
+                    else
+                        static_cast<__nv_bfloat16 *>(p.out)[idx] = __float2bfloat16_rn(v);
+                }
+            }
+            // Peers may read this CTA's partial until each has said it is done; the CTA
+            // stays resident (its shared memory valid) until then.
+            good = group_sync(c, gphase, lane) && good;
+            if (row == 0)
+                for (int r = 0; r < C; ++r)
+                    mbar_arrive_cluster(map_to_rank(&c.cl_done, static_cast<uint32_t>(r)));
+            good = mbar_wait_cluster(&c.cl_done, 0, 8 * kWaitTimeoutNs) && good;
+            if (row == 0)
+                SFI_STAMP(25);
+            if (!good)
+                ok = false;
+        }
         if (!ok)
             fail(c, p.err);
     }
@@ -887,12 +1119,79 @@ cudaError_t launch_attn_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, cons
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess)
         return e;
-    e = launch_pdl(kern, dim3(grid), dim3(kAttnThreads), kSmemBytes, stream, tm_k, tm_v, tm_q, tm_kc,
-                   tm_vc, p);
+    const int cluster = (!DENSE && p.cluster > 1) ? p.cluster : 1;
+    if (grid % cluster != 0)
+        return cudaErrorInvalidValue;
+    e = launch_pdl_cluster(kern, dim3(grid), dim3(kAttnThreads), kSmemBytes, cluster, stream, tm_k,
+                           tm_v, tm_q, tm_kc, tm_vc, p);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// Clusters of `cluster` sparse-kernel CTAs that can be resident at once on this device.
+template <int G>
+int max_active_clusters_t(int cluster)
+{
+    auto kern = attn_kernel<G, false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(cluster) * 64u);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    cfg.attrs = a;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+int max_active_clusters(int group, int cluster)
+{
+    switch (group) {
+    case 1: return max_active_clusters_t<1>(cluster);
+    case 2: return max_active_clusters_t<2>(cluster);
+    case 4: return max_active_clusters_t<4>(cluster);
+    case 8: return max_active_clusters_t<8>(cluster);
+    default: return 0;
+    }
+}
+
+constexpr int kMaxDevicesCached = 64;
+std::mutex g_cluster_mu;
+int g_cluster_fit[kMaxDevicesCached][4][9];  // max active clusters + 1 (0 = not yet queried)
+
 }  // namespace
+
+int sparse_cluster_size(int group, int units, int max_cluster)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesCached)
+        return 1;
+    const int gi = group == 1 ? 0 : group == 2 ? 1 : group == 4 ? 2 : 3;
+    for (int C = max_cluster < 8 ? max_cluster : 8; C >= 2; --C) {
+        int n;
+        {
+            std::lock_guard<std::mutex> lock(g_cluster_mu);
+            n = g_cluster_fit[dev][gi][C] - 1;
+        }
+        if (n < 0) {
+            n = max_active_clusters(group, C);
+            std::lock_guard<std::mutex> lock(g_cluster_mu);
+            g_cluster_fit[dev][gi][C] = n + 1;
+        }
+        if (n >= units)
+            return C;
+    }
+    return 1;
+}
 
 size_t attention_smem_bytes() { return kSmemBytes; }
 
@@ -1002,7 +1301,7 @@ cudaError_t launch_sparse_static(int group, const CUtensorMap &tm_k, const CUten
 #ifdef SFI_TRACE
 cudaError_t trace_read(unsigned long long *host, int n)
 {
-    return cudaMemcpyFromSymbol(host, g_sfi_trace, sizeof(unsigned long long) * 16 * (n < 1024 ? n : 1024));
+    return cudaMemcpyFromSymbol(host, g_sfi_trace, sizeof(unsigned long long) * 32 * (n < 1024 ? n : 1024));
 }
 #endif
 

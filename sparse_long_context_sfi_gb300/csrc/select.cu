@@ -15,7 +15,6 @@ namespace {
 
 constexpr int NT = kSelectThreads;
 constexpr int kWarps = NT / 32;
-constexpr int kKeyCache = 32768;  // candidates whose keys fit in shared memory
 constexpr int kListCap = 8192;    // keys gathered for the refining passes
 constexpr int kSub = 4;           // sub-histograms (warps w with w % kSub equal share one)
 
@@ -75,7 +74,9 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *scratch, int *to
     return r;
 }
 
-__global__ void __launch_bounds__(NT) select_kernel(const SelectParams p)
+// At most 56 registers per thread: a 1024-thread CTA then takes 7/8 of the register file
+// instead of all of it, so a launch under a profiler, which may need a few more, still fits.
+__global__ void __maxnreg__(56) select_kernel(const SelectParams p)
 {
     __shared__ int scratch[kWarps + 1];
     __shared__ uint32_t sh_digit;
@@ -111,18 +112,16 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p)
     fz.c2 = __double2float_rn(p.lambda / Z);
     fz.inv_tau = __double2float_rn(1.0 / tau);
 
-    // Keys of up to kKeyCache candidates are kept in shared memory by the first pass. The
-    // candidates that share the threshold's top 12 bits are then gathered into a list (at
-    // most kListCap keys) and the two refining passes run over that list only.
+    // The candidates that share the threshold's top 12 bits are gathered into a list (at
+    // most kListCap keys) and the two refining passes run over that list only. Keys are
+    // recomputed from the evidence on every pass (L2-resident after the first).
     // Dynamic shared memory: kSub sub-histograms (one per group of warps, so fewer lanes
-    // collide on a bin), the gathered list, then the key cache when it is used.
+    // collide on a bin), then the gathered list.
     extern __shared__ uint32_t dyn[];
-    const bool cached = p.cache_keys && nC <= kKeyCache;
     uint32_t *hist = dyn;
     uint32_t *lst = dyn + kSub * 4096;
-    uint32_t *kcache = lst + kListCap;
     const int sub = (tid >> 5) % kSub;
-    auto key_at = [&](int i) -> uint32_t { return cached ? kcache[i] : fz.key(i); };
+    auto key_at = [&](int i) -> uint32_t { return fz.key(i); };
     int nbins = 4096;
     auto count = [&](bool part, uint32_t digit) {
         if (part)
@@ -169,8 +168,6 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p)
         for (int e = 0; e < 4; ++e) {
             const int i = base + e * NT + tid;
             k[e] = i < nC ? fz.key(i) : 0u;
-            if (cached && i < nC)
-                kcache[i] = k[e];
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e)
@@ -245,17 +242,10 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p)
     int gt_base = 0, eq_base = 0;
     for (int base = 0; base < nC; base += 8 * NT) {
         uint32_t k[8];
-        if (cached && base + 8 * tid + 7 < nC) {
-            const uint4 a = *reinterpret_cast<const uint4 *>(kcache + base + 8 * tid);
-            const uint4 c4 = *reinterpret_cast<const uint4 *>(kcache + base + 8 * tid + 4);
-            k[0] = a.x; k[1] = a.y; k[2] = a.z; k[3] = a.w;
-            k[4] = c4.x; k[5] = c4.y; k[6] = c4.z; k[7] = c4.w;
-        } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int i = base + 8 * tid + e;
-                k[e] = i < nC ? key_at(i) : 0u;
-            }
+        for (int e = 0; e < 8; ++e) {
+            const int i = base + 8 * tid + e;
+            k[e] = i < nC ? key_at(i) : 0u;
         }
         int n_gt = 0, n_eq = 0;
 #pragma unroll
@@ -294,7 +284,7 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p)
 cudaError_t launch_select(const SelectParams &p, cudaStream_t stream)
 {
     const size_t smem =
-        (kSub * 4096 + kListCap + (p.cache_keys ? kKeyCache : 0)) * sizeof(uint32_t);
+        (kSub * 4096 + kListCap) * sizeof(uint32_t);
     {
         const cudaError_t a =
             cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -33,6 +33,13 @@ struct AttnParams {
     int n_cbox;                 // 64-row boxes of the packed region per unit
     int n_wbox;                 // 16-row boxes of the window region per unit
     int tiles_per_unit;         // sparse: ceil((64 n_cbox + 16 n_wbox) / 128)
+    int cluster;                // sparse: CTAs per unit in one thread-block cluster (1 = none)
+    // sparse step with the append fused in (k_new != null): each active sequence's new K/V
+    // rows are written at position seq_len[b] and attended, and the last CTA to have read
+    // seq_len advances it.
+    const void *k_new, *v_new;  // bf16 [units][128]
+    void *k_cache, *v_cache;    // the cache the tensor maps view
+    int *append_counter;        // CTAs that have read seq_len; zero between launches
     // outputs and workspace
     void *out;
     int out_fp32;
@@ -52,7 +59,6 @@ struct SelectParams {
     double lambda;
     int32_t *sel_idx;           // [units][n_select]
     int32_t *sel_cnt;           // [units]
-    int cache_keys;             // candidates (host bound) fit the shared-memory key cache
 };
 
 struct RefineParams {
@@ -83,6 +89,9 @@ cudaError_t launch_attention(bool dense, int group, const CUtensorMap &tm_k,
                              const CUtensorMap &tm_v, const CUtensorMap &tm_q,
                              const CUtensorMap &tm_kc, const CUtensorMap &tm_vc,
                              const AttnParams &p, int grid, cudaStream_t stream);
+// Largest cluster size (<= max_cluster) for which `units` clusters of the sparse kernel can
+// be resident at once (1 when none above 1 fits).
+int sparse_cluster_size(int group, int units, int max_cluster);
 cudaError_t launch_evidence(const float *zbuf, const float2 *stats, float *f,
                             const int32_t *seq_len, const uint8_t *active, int n_layers,
                             int batch, int n_kv_heads, int group, int capacity, int max_len,

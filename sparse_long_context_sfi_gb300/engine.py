@@ -14,7 +14,8 @@ import torch
 
 from . import (SfiBudget, SfiDecodePlan, SfiKvCache, SfiSparseMem, sfi_append_kv, sfi_compact,
                sfi_decode_run, sfi_dense_decode_attn, sfi_schedule, sfi_select,
-               sfi_sparse_decode_attn, sfi_workspace_bytes, sfi_workspace_init)
+               sfi_fast_decode_step, sfi_sparse_decode_attn, sfi_workspace_bytes,
+               sfi_workspace_init)
 
 
 class SfiState:
@@ -76,12 +77,14 @@ class SfiState:
         return np.stack([sfi_schedule(masks[b], self.cfg.t_max) for b in range(self.cfg.batch)], 1)
 
     # -- one decode step through the individual calls -----------------------------------------
-    def step(self, q, k_new, v_new, slow_b: np.ndarray, out, out_fp32=True, stream=None):
-        """q [Ly][B][Hq][D] bf16, k_new/v_new [Ly][B][Hkv][D] bf16 (device); slow_b [B] bool."""
+    def step(self, q, k_new, v_new, slow_b: np.ndarray, out, out_fp32=True, stream=None,
+             fused=True):
+        """q [Ly][B][Hq][D] bf16, k_new/v_new [Ly][B][Hkv][D] bf16 (device); slow_b [B] bool.
+        fused: the fast sequences' append runs inside sfi_fast_decode_step (as in the native
+        driver); otherwise every row is appended first and the fast step is
+        sfi_sparse_decode_attn."""
         kv = self.kv
-        kv.max_len = int(self.len0.max()) + self.t
-        sfi_append_kv(kv, k_new, v_new, stream=stream)
-        kv.max_len = int(self.len0.max()) + self.t + 1
+        bound = int(self.len0.max()) + self.t
         slow_b = np.asarray(slow_b, bool)
         mixed = slow_b.any() and not slow_b.all()
         if mixed:
@@ -89,14 +92,26 @@ class SfiState:
             a_slow, a_fast = m[0], m[1]
         else:
             a_slow = a_fast = None
+        kv.max_len = bound
+        if not fused:
+            sfi_append_kv(kv, k_new, v_new, stream=stream)
+        elif slow_b.any():
+            sfi_append_kv(kv, k_new, v_new, active=a_slow, stream=stream)
+        kv.max_len = bound + 1
         if slow_b.any():
             sfi_dense_decode_attn(kv, q, out, out_fp32, self.scores, self.ws, self.ws_bytes,
                                   active=a_slow, stream=stream)
             sfi_select(kv, self.scores, self.budget, self.mem, active=a_slow, stream=stream)
             sfi_compact(kv, self.budget, self.mem, active=a_slow, stream=stream)
         if not slow_b.all():
-            sfi_sparse_decode_attn(kv, self.mem, self.budget, q, out, out_fp32, self.ws,
-                                   self.ws_bytes, active=a_fast, stream=stream)
+            if fused:
+                kv.max_len = bound
+                sfi_fast_decode_step(kv, self.mem, self.budget, k_new, v_new, q, out, out_fp32,
+                                     self.ws, self.ws_bytes, active=a_fast, stream=stream)
+                kv.max_len = bound + 1
+            else:
+                sfi_sparse_decode_attn(kv, self.mem, self.budget, q, out, out_fp32, self.ws,
+                                       self.ws_bytes, active=a_fast, stream=stream)
         self.t += 1
         return mixed and (a_slow, a_fast)
 

@@ -142,14 +142,16 @@ def test_dense_bf16_output():
 
 # ------------------------------------------------------------------------------ fast step
 
+@pytest.mark.parametrize("fused", [True, False], ids=["fused_append", "append_then_sparse"])
 @pytest.mark.parametrize("case", [
     dict(name="gqa4_ctx4k_hh"),
-    dict(name="llama8b_ctx32k_b4", ctx=5000, batch=2),
+    dict(name="llama8b_ctx32k_b4", ctx=5000, batch=2),               # clusters of 8 CTAs
     dict(name="llama8b_ctx32k_b4", ctx=150, batch=2),                # n_C < K: all selected
     dict(name="llama8b_ctx32k_b4", ctx=40, batch=1),                 # window clipped at sinks
+    dict(name="llama8b_ctx32k_b4", ctx=1300, batch=3, n_layers=5),   # 120 units: tile ranges
     dict(name="ragged_paged_b32", batch=4, ctx=2500, ctx_lo=700),    # paged window
 ])
-def test_sparse_step_vs_oracle(case):
+def test_sparse_step_vs_oracle(case, fused):
     """Slow step at t=0, then fast steps: each fast output equals attention over sinks +
     the (GPU-selected) memory + the sliding window."""
     case = dict(case)
@@ -163,7 +165,7 @@ def test_sparse_step_vs_oracle(case):
     sel = None
     for t in range(n):
         slow = np.full(cfg.batch, t == 0)
-        st.step(ins.q[t], ins.k_new[t], ins.v_new[t], slow, outs[t])
+        st.step(ins.q[t], ins.k_new[t], ins.v_new[t], slow, outs[t], fused=fused)
         if t == 0:
             torch.cuda.synchronize()
             sel = [st.sel_idx[u, :int(st.sel_cnt[u])].cpu().numpy() for u in range(st.n_units)]
@@ -182,6 +184,40 @@ def test_sparse_step_vs_oracle(case):
             o, _ = oracle.attend(q, k, v, rows)
             ok, err = close(outs[t, layer, b, kvh * G:(kvh + 1) * G], o)
             assert ok, f"unit {u} step {t}: sparse max err {err}"
+
+
+@pytest.mark.parametrize("case", [
+    dict(name="llama8b_ctx32k_b4", ctx=3000, batch=2),               # clusters of 8 CTAs
+    dict(name="llama8b_ctx32k_b4", ctx=1300, batch=3, n_layers=5),   # 120 units: tile ranges
+    dict(name="ragged_paged_b32", batch=5, ctx=2500, ctx_lo=700),    # paged, mixed steps
+])
+def test_fused_fast_step_equals_append_then_sparse(case):
+    """sfi_fast_decode_step against sfi_append_kv + sfi_sparse_decode_attn on two copies of
+    the same state: the caches and lengths bit for bit, the outputs within the tolerance
+    (the merge order of split units may differ between launches)."""
+    case = dict(case)
+    wl = small(case.pop("name"), steps=12, **case)
+    cfg = wl.cfg
+    n = 12
+    a = sdev.make_state(wl, on_device=True)
+    b = sdev.make_state(wl, on_device=True)
+    ins = sdev.DeviceInputs(wl, n, a.k.device)
+    shape = (cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim)
+    oa = torch.zeros(shape, dtype=torch.float32, device=a.k.device)
+    ob = torch.zeros_like(oa)
+    rng = np.random.default_rng(5)
+    for t in range(n):
+        slow = np.full(cfg.batch, t == 0) if t < 2 or cfg.batch < 3 else rng.random(cfg.batch) < 0.3
+        a.step(ins.q[t], ins.k_new[t], ins.v_new[t], slow, oa, fused=True)
+        b.step(ins.q[t], ins.k_new[t], ins.v_new[t], slow, ob, fused=False)
+        torch.cuda.synchronize()
+        assert int(a.err[0]) == 0 and int(b.err[0]) == 0
+        assert torch.equal(a.seq_len, b.seq_len)
+        ok, err = close(oa.cpu().numpy(), ob.cpu().numpy())
+        assert ok, f"step {t}: fused vs separate max err {err}"
+    assert torch.equal(a.k, b.k) and torch.equal(a.v, b.v)
+    want = torch.from_numpy((wl.len0 + n).astype(np.int32))
+    assert torch.equal(a.seq_len.cpu(), want)
 
 
 # ------------------------------------------------------------------ whole decode, end to end
