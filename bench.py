@@ -164,8 +164,9 @@ def aggregate_tokens_per_s(world: int, tokens_per_step: int, steps: int, ms_max:
 
 
 def bytes_model(wl, slow, sel_rows):
-    """Algorithmic bytes of every step's attention kernel: dense = KV rows + logits; sparse =
-    packed rows + window rows (each 512 B of K+V), plus q/out (small)."""
+    """Algorithmic bytes of every step's attention kernel: dense = KV rows + logits; sparse
+    (the fused fast step) = packed rows + window rows (each 512 B of K+V) + the appended row
+    (512 B read from the new-token buffer, 512 B written to the cache), plus q/out (small)."""
     cfg = wl.cfg
     per_unit_q = cfg.group * 256 + cfg.group * 128 * 2
     units_per_seq = cfg.n_layers * cfg.n_kv_heads
@@ -183,7 +184,8 @@ def bytes_model(wl, slow, sel_rows):
             n_s = np.minimum(cfg.n_sink, L)
             win = L - np.maximum(n_s, L - cfg.n_window)
             rows = ((sel_rows + win) * fast).sum() * units_per_seq
-            sparse.append(rows * BYTES_PER_ROW + fast.sum() * units_per_seq * per_unit_q)
+            sparse.append(rows * BYTES_PER_ROW +
+                          fast.sum() * units_per_seq * (per_unit_q + 2 * BYTES_PER_ROW))
         else:
             sparse.append(0)
     return np.array(dense, float), np.array(sparse, float)
@@ -312,36 +314,58 @@ def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=N
     res["ms_per_run"] = ms / k_steps
     res["tokens_per_run"] = tokens_per_run
     res["slow_steps"] = int(slow.any(axis=1).sum())
-    res["launches_per_run"] = int(sum(1 + (4 if r.any() else 0) + (0 if r.all() else 1) for r in slow))
+    # slow step: append, dense, evidence, select, compact; fast step: one fused kernel
+    res["launches_per_run"] = int(sum((5 if r.any() else 0) + (0 if r.all() else 1) for r in slow))
     sel_rows = (st.rows.view(cfg.n_layers, cfg.batch, cfg.n_kv_heads).float().mean(dim=(0, 2))
                 .cpu().numpy())
 
-    # live kernel timing: the same run with external event nodes around each attention kernel
-    events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * cfg.steps)]
+    # live kernel timing: the same run with external event nodes around each slow step's
+    # dense kernel, and around each maximal stretch of consecutive fast steps (whose fused
+    # fast-step kernels run back to back, overlapped by programmatic dependent launch; the
+    # stretch's time divided by its launches is their average duration there)
+    is_slow = slow.any(axis=1)
+    events = [None] * (2 * cfg.steps)
+    groups = []                                    # (first, last) step of each fast stretch
+    t = 0
+    while t < cfg.steps:
+        if is_slow[t]:
+            events[2 * t] = torch.cuda.Event(enable_timing=True)
+            events[2 * t + 1] = torch.cuda.Event(enable_timing=True)
+            t += 1
+            continue
+        t1 = t
+        while t1 + 1 < cfg.steps and not is_slow[t1 + 1]:
+            t1 += 1
+        events[2 * t] = torch.cuda.Event(enable_timing=True)
+        events[2 * t1 + 1] = torch.cuda.Event(enable_timing=True)
+        groups.append((t, t1))
+        t = t1 + 1
     g_ev = capture(run_of(slow, events=events))
     reps = 3
-    d_dense, d_sparse = [], []
-    is_slow = slow.any(axis=1)
+    d_dense, d_sparse = [], []                     # (steps, seconds)
     with torch.cuda.stream(stream):
         for _ in range(reps):
             g_ev.replay()
             torch.cuda.synchronize()
-            for t in range(cfg.steps):
-                dt = events[2 * t].elapsed_time(events[2 * t + 1]) * 1e-3
-                (d_dense if is_slow[t] else d_sparse).append((t, dt))
+            for t in np.nonzero(is_slow)[0]:
+                d_dense.append(([int(t)], events[2 * t].elapsed_time(events[2 * t + 1]) * 1e-3))
+            for a, b in groups:
+                d_sparse.append((list(range(a, b + 1)),
+                                 events[2 * a].elapsed_time(events[2 * b + 1]) * 1e-3))
     bd, bs = bytes_model(wl, slow.astype(bool), sel_rows)
     peak, _ = measured_peaks()
 
     def kstats(d, bytes_per):
         if not d:
             return None
-        secs = np.array([x[1] for x in d])
-        byt = np.array([bytes_per[x[0]] for x in d])
-        avg = float(secs.mean())
-        gbs = float(byt.mean() / avg / 1e9)
-        return {"launches_per_run": len(d) // reps, "avg_us": avg * 1e6,
-                "bytes_per_launch": float(byt.mean()), "achieved_gbs": gbs,
-                "frac_of_peak": gbs / peak, "total_us_per_run": float(secs.sum() / reps * 1e6)}
+        n = sum(len(x[0]) for x in d)
+        secs = float(sum(x[1] for x in d))
+        byt = float(sum(bytes_per[i] for x in d for i in x[0]))
+        avg = secs / n
+        gbs = byt / secs / 1e9
+        return {"launches_per_run": n // reps, "avg_us": avg * 1e6, "bytes_per_launch": byt / n,
+                "achieved_gbs": gbs, "frac_of_peak": gbs / peak,
+                "total_us_per_run": secs / reps * 1e6}
 
     res["kernels"] = {"sfi_dense_decode_attn": kstats(d_dense, bd),
                       "sfi_sparse_decode_attn": kstats(d_sparse, bs)}

@@ -303,7 +303,8 @@ sfi_status sfi_schedule_tokens(int32_t steps, const int32_t *tokens, const int32
  *             baseline the pages compare against); slow is ignored
  *   events    optional host array of 2 * n_steps cudaEvent_t (as void*): events[2t] and
  *             events[2t+1] are recorded (external, so they survive graph capture) right
- *             before and after step t's attention kernel; NULL = none
+ *             before and after step t's attention kernel (the fused fast step's kernel on
+ *             fast steps); NULL = none, and NULL entries are skipped
  */
 typedef struct sfi_decode_plan {
     int32_t n_steps;

@@ -392,6 +392,12 @@ sfi_status sfi_select(const sfi_kv_cache *kv, const float *scores_f, const sfi_b
     p.lambda = budget->lambda;
     p.sel_idx = mem->sel_idx;
     p.sel_cnt = mem->sel_cnt;
+    p.err = kv->err;
+    // Stage in shared memory when every unit's candidates (with up to 3 values of alignment
+    // slack on either side) fit, and the copy's tail stays inside the unit's row.
+    const long long bound = static_cast<long long>(kv->max_len) - budget->n_window - budget->n_sink;
+    p.staged = (aligned16(scores_f) && bound + 3 <= kStageCap &&
+                static_cast<long long>(kv->max_len) - budget->n_window + 3 <= kv->capacity) ? 1 : 0;
     return launch_status(launch_select(p, as_stream(stream)));
 }
 

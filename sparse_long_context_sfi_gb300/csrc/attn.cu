@@ -135,6 +135,18 @@ __device__ __forceinline__ void mask_rows(uint32_t (&v)[4], int r0, int r1)
         v[w] |= word_bits(r0, r1, w);
 }
 
+// a[i] for a small register array without dynamic indexing (which would move the array to
+// local memory)
+template <int G>
+__device__ __forceinline__ float pick(const float (&a)[G], int i)
+{
+    float v = a[0];
+#pragma unroll
+    for (int h = 1; h < G; ++h)
+        v = (i == h) ? a[h] : v;
+    return v;
+}
+
 template <int G>
 __device__ __forceinline__ void store_out(const AttnParams &p, int u, int d, const float (&o)[G])
 {
@@ -241,32 +253,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             c.T = c.TL * p.n_layers;
             c.P = static_cast<int>(c.T < gridDim.x ? c.T : gridDim.x);
             const long long P = c.P > 0 ? c.P : 1;
-            if (DENSE) {
-                // stream-K: equal contiguous tile ranges (balances ragged lengths)
-                c.g0 = static_cast<long long>(blockIdx.x) * c.T / P;
-                c.g1 = static_cast<long long>(blockIdx.x + 1) * c.T / P;
-            } else {
-                // every unit has the same tile count: ranges never straddle two units
-                const long long nt = p.tiles_per_unit, ua = c.T / nt, cta = blockIdx.x;
-                if (P >= ua) {
-                    const long long q = P / ua, r = P % ua;
-                    long long a, k, nc;
-                    if (cta < r * (q + 1)) {
-                        a = cta / (q + 1);
-                        k = cta % (q + 1);
-                        nc = q + 1;
-                    } else {
-                        a = r + (cta - r * (q + 1)) / q;
-                        k = (cta - r * (q + 1)) % q;
-                        nc = q;
-                    }
-                    c.g0 = a * nt + k * nt / nc;
-                    c.g1 = a * nt + (k + 1) * nt / nc;
-                } else {
-                    c.g0 = (cta * ua / P) * nt;
-                    c.g1 = ((cta + 1) * ua / P) * nt;
-                }
-            }
+            // stream-K: equal contiguous tile ranges (balances ragged lengths and unit counts
+            // that are not a multiple of the CTA count)
+            c.g0 = static_cast<long long>(blockIdx.x) * c.T / P;
+            c.g1 = static_cast<long long>(blockIdx.x + 1) * c.T / P;
         }
         tc_fence_before();
         __syncthreads();
@@ -367,23 +357,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             };
             if (paged_dense)
                 load_page(b, t);
-            // Fused append: this lane's 128-byte half of unit u's new K or V row goes to cache
-            // row `dst_row` (of the tensor maps' row view) before the lane's own TMA box, which
-            // covers that row, reads it back through the async proxy.
-            auto append_half = [&](int uu, int kvsel, int hf, long long dst_row) {
-                const uint4 *src = static_cast<const uint4 *>(kvsel ? p.v_new : p.k_new) +
-                                   static_cast<size_t>(uu) * 16 + hf * 8;
-                uint4 *dst = static_cast<uint4 *>(kvsel ? p.v_cache : p.k_cache) +
-                             static_cast<size_t>(dst_row) * 16 + hf * 8;
-                uint4 x[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    x[e] = src[e];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    dst[e] = x[e];
-                fence_proxy_async_global();
+            // Fused append: unit uu's new K and V rows go to cache position pos, 16 bytes per
+            // lane (lanes 0-15 K, 16-31 V); each lane then fences its write against the async
+            // proxy and the warp synchronises, so every later TMA box of this warp that covers
+            // the row reads the new data. Issued right after the segment's first TMA (or before
+            // it, when the first tile itself holds the row), well ahead of the box that reads it.
+            auto append_row = [&](int uu, int ll, int bb, int kk, int pos) {
+                long long row;
+                bool good = true;
+                if (p.page_size == 0) {
+                    row = static_cast<long long>(uu) * p.capacity + pos;
+                } else {
+                    const int page = __ldg(p.page_table + bb * p.max_pages + (pos >> 4));
+                    good = page >= 0 && page < p.n_pages;
+                    if (!good && lane == 0)
+                        raise_error(p.err, 0x1u);  // SFI_DEVERR_PAGE_RANGE
+                    row = ((static_cast<long long>(ll) * p.n_pages + page) * Hkv + kk) * 16 + (pos & 15);
+                }
+                if (good) {
+                    const int kvsel = lane >> 4, chunk = lane & 15;
+                    const uint4 x = static_cast<const uint4 *>(kvsel ? p.v_new : p.k_new)
+                        [static_cast<size_t>(uu) * 16 + chunk];
+                    static_cast<uint4 *>(kvsel ? p.v_cache : p.k_cache)[row * 16 + chunk] = x;
+                    fence_proxy_async_global();
+                }
+                __syncwarp();
             };
+            int app_tile = -1;       // tile of the current segment that holds the new row
+            bool appended = false;
             bool ok = true;
             for (int i = 0; i < n_tiles; ++i, ++g) {
                 if (i > 0 && ++t == ntiles_of(b)) {
@@ -415,6 +416,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const int n_s = max(0, rows_c - max(0, clustered ? c.cl_sel : __ldg(p.sel_cnt + u)));
                         seg_rows_c = rows_c;
                         seg_ws = max(n_s, seg_len - p.n_window);
+                    }
+                    if (fused) {
+                        const int Ln = seg_len - 1;  // position of the new row
+                        const int jn = p.page_size == 0 ? ((Ln - seg_ws) >> 4)
+                                                        : ((Ln >> 4) - (seg_ws >> 4));
+                        const int t_new = (64 * p.n_cbox + 16 * jn) / kTile;
+                        const int t_end = min(ntiles_of(b) - 1, t + (n_tiles - 1 - i));
+                        app_tile = (seg_len >= 1 && t_new >= t && t_new <= t_end) ? t_new : -1;
+                        appended = false;
                     }
                 }
                 if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
@@ -485,8 +495,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                 y = u * p.capacity + p0;
                                 row0 = rr0;
                                 rows = 16;
-                                if (fused && L - 1 < p0 + 16)  // the box holds the new row
-                                    append_half(u, kv, half, static_cast<long long>(y) + (L - 1 - p0));
                                 if (my_op == 0)
                                     mask_rows(valid, rr0, rr0 + vr);
                             }
@@ -506,14 +514,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                     y = ((layer * p.n_pages + page) * Hkv + kvh) * 16;
                                     row0 = rr0;
                                     rows = 16;
-                                    if (fused && L - 1 < lp * 16 + 16)  // the page holds the new row
-                                        append_half(u, kv, half, static_cast<long long>(y) + (L - 1 - lp * 16));
                                     if (my_op == 0)
                                         mask_rows(valid, rr0 + r0, rr0 + r1);
                                 }
                             }
                         }
                     }
+                }
+                if (fused && app_tile == t && !appended) {  // this tile holds the new row
+                    append_row(u, layer, b, kvh, L - 1);
+                    appended = true;
                 }
                 // ---- publish the tile, then issue ---------------------------------------
                 uint32_t vw[4];
@@ -546,6 +556,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         tma_load_2d_hint(dst, map, bar, 64 * half, y, pol);
                     else
                         tma_load_2d(dst, map, bar, 64 * half, y);
+                }
+                if (fused && app_tile >= 0 && !appended) {  // a later tile holds the new row
+                    append_row(u, layer, b, kvh, L - 1);
+                    appended = true;
                 }
                 if (lane == 0 && i == 0)
                     SFI_STAMP(3);
@@ -683,20 +697,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const long long su = layer * c.TL + c.pre[b] + static_cast<long long>(kvh) * c.nt[b];
             const long long eu = su + c.nt[b];
             const long long P = c.P, T = c.T;
-            int cf, cl;
-            if (DENSE) {  // stream-K: the CTAs whose ranges meet [su, eu)
-                cf = static_cast<int>(((su + 1) * P - 1) / T);
-                cl = static_cast<int>((eu * P - 1) / T);
-            } else {      // unit-aligned ranges: the unit's own group of CTAs
-                const long long nt = p.tiles_per_unit, ua = T / nt, a = su / nt;
-                if (P >= ua) {
-                    const long long q = P / ua, r = P % ua;
-                    cf = static_cast<int>(a < r ? a * (q + 1) : r * (q + 1) + (a - r) * q);
-                    cl = cf + static_cast<int>(a < r ? q + 1 : q) - 1;
-                } else {
-                    cf = cl = static_cast<int>(blockIdx.x);
-                }
-            }
+            // the CTAs whose stream-K ranges meet [su, eu)
+            const int cf = static_cast<int>(((su + 1) * P - 1) / T);
+            const int cl = static_cast<int>((eu * P - 1) / T);
             float o[G];
             if (cf == cl) {
 #pragma unroll
@@ -704,7 +707,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     o[h] = flr[h] > 0.f ? acc[h] / flr[h] : 0.f;
                 store_out<G>(p, u, row, o);
                 if (DENSE && row < G)
-                    p.stats[u * G + row] = make_float2(fm[row], fle[row]);
+                    p.stats[u * G + row] = make_float2(pick<G>(fm, row), pick<G>(fle, row));
                 return true;
             }
             const int slot = (su <= g0) ? 0 : 1;
@@ -713,9 +716,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int h = 0; h < G; ++h)
                 part[h * kHeadDim + row] = acc[h];
             if (row < G) {
-                part[G * kHeadDim + row] = fm[row];
-                part[G * kHeadDim + G + row] = fle[row];
-                part[G * kHeadDim + 2 * G + row] = flr[row];
+                part[G * kHeadDim + row] = pick<G>(fm, row);
+                part[G * kHeadDim + G + row] = pick<G>(fle, row);
+                part[G * kHeadDim + 2 * G + row] = pick<G>(flr, row);
             }
             // Every thread's partial writes happen before thread 0's release fence (group
             // barrier), which publishes them before the ticket; the last contributor's
@@ -751,9 +754,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 Lr[h] = flr[h];
                 o[h] = acc[h];
             }
-            // under stream-K, u may be the last segment of cf (slot 1); unit-aligned ranges
-            // hold one segment each (slot 0)
-            const bool cf_tail = DENSE && static_cast<long long>(cf) * T / P < su;
+            // u may be the last segment of cf's range (slot 1)
+            const bool cf_tail = static_cast<long long>(cf) * T / P < su;
             for (int c0 = cf; c0 <= cl; c0 += 4) {
                 float mc[4][G], lc[4][G], rc[4][G], ac[4][G];
                 bool use[4];
@@ -794,7 +796,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 o[h] = Lr[h] > 0.f ? o[h] / Lr[h] : 0.f;
             store_out<G>(p, u, row, o);
             if (DENSE && row < G)
-                p.stats[u * G + row] = make_float2(M[row], Le[row]);
+                p.stats[u * G + row] = make_float2(pick<G>(M, row), pick<G>(Le, row));
             return true;
         };
 

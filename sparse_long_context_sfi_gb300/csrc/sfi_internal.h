@@ -59,7 +59,12 @@ struct SelectParams {
     double lambda;
     int32_t *sel_idx;           // [units][n_select]
     int32_t *sel_cnt;           // [units]
+    int staged;                 // candidates' evidence copied to shared memory (see kStageCap)
+    uint32_t *err;              // device error word
 };
+// The Selector stages a unit's evidence in shared memory when it has at most this many
+// candidates (plus alignment slack); larger units stream it from global memory.
+constexpr int kStageCap = 36864;
 
 struct RefineParams {
     const float *f;             // evidence [units][capacity]

@@ -119,8 +119,8 @@ class SfiState:
     def make_plan(self, slow: np.ndarray, q, k_new, v_new, out, out_fp32=True, out_per_step=True,
                   dense_only=False, events=None, t0=0, t1=None):
         """slow: uint8 [steps][B]; q/k_new/v_new/out: device tensors with a leading step axis.
-        events: optional list of 2 * (t1 - t0) torch.cuda.Event(enable_timing=True), recorded
-        around each step's attention kernel. [t0, t1): the steps this plan covers (a run can
+        events: optional list of 2 * (t1 - t0) torch.cuda.Event(enable_timing=True) or None,
+        recorded before (2 t) and after (2 t + 1) step t's attention kernel (None: not recorded). [t0, t1): the steps this plan covers (a run can
         be issued as several consecutive plans)."""
         t1 = slow.shape[0] if t1 is None else t1
         q, k_new, v_new = q[t0:t1], k_new[t0:t1], v_new[t0:t1]
@@ -143,9 +143,11 @@ class SfiState:
         if events is not None:
             assert len(events) == 2 * steps
             for e in events:          # make sure the driver-level event objects exist
-                e.record()
+                if e is not None:
+                    e.record()
             torch.cuda.synchronize()
-            ev_arr = (C.c_void_p * (2 * steps))(*[e.cuda_event for e in events])
+            ev_arr = (C.c_void_p * (2 * steps))(*[None if e is None else e.cuda_event
+                                                  for e in events])
             plan.events = C.cast(ev_arr, C.c_void_p)
         plan._keep = (slow, masks, q, k_new, v_new, out, ev_arr, events)
         return plan
