@@ -285,7 +285,7 @@ sfi_status sparse_impl(const sfi_kv_cache *kv, const sfi_sparse_mem *mem,
     // Few units: a cluster of up to 8 CTAs per unit (one unit per cluster, partials merged
     // in distributed shared memory). Otherwise one CTA per SM over contiguous tile ranges.
     int cluster = 1;
-    if (units * 2 <= sms) {
+    if (units * 2 <= sms && g <= 4) {
         long long cmax = sms / units;
         cmax = cmax < 8 ? cmax : 8;
         cmax = cmax < p.tiles_per_unit ? cmax : p.tiles_per_unit;

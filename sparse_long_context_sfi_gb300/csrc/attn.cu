@@ -68,7 +68,7 @@ struct Ctrl {
     uint64_t drain;             // MMA drain on exit
     uint64_t unit_meta;         // clustered: this CTA's unit and tile slice are known
     uint64_t cl_ready;          // clustered: every CTA of the cluster has its partial in place
-    uint64_t cl_done;           // clustered: every CTA has finished reading the partials
+    uint64_t app_ready;         // clustered, fused append: the new row is in the cache
     TileMeta meta[kStages];
     float red_max[2][4][8];
     float red_sum[4][16];
@@ -76,6 +76,7 @@ struct Ctrl {
     int abort;
     int last_flag;
     int cl_tiles, cl_t0, cl_live, cl_rows, cl_sel;  // clustered: slice of the unit's tiles
+    int cl_app_tile;            // clustered, fused append: tile holding the new row, or -1
     int P;
     long long T, TL, g0, g1;
     int nt[kMaxBatch];
@@ -192,8 +193,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_init(&c.gsync, 4);
         mbar_init(&c.drain, 1);
         mbar_init(&c.unit_meta, 1);
+        mbar_init(&c.app_ready, 1);
         mbar_init(&c.cl_ready, static_cast<uint32_t>(p.cluster > 1 ? p.cluster : 1));
-        mbar_init(&c.cl_done, static_cast<uint32_t>(p.cluster > 1 ? p.cluster : 1));
         mbar_fence_init();
         tma_prefetch_map(&tm_k);
         tma_prefetch_map(&tm_v);
@@ -204,6 +205,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         c.abort = 0;
         c.cl_live = 0;
+        c.cl_app_tile = -1;
     }
     if (warp == 1) {
         tmem_alloc(&c.tmem_base, kTmemCols);
@@ -295,12 +297,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             live = live && L > 0;
             if (lane == 0) {
                 const int nt = p.tiles_per_unit, C = p.cluster;
-                c.cl_t0 = rank * nt / C;
-                c.cl_tiles = live ? (rank + 1) * nt / C - rank * nt / C : 0;
+                const int t0 = rank * nt / C, t1 = (rank + 1) * nt / C;
+                c.cl_t0 = t0;
+                c.cl_tiles = live ? t1 - t0 : 0;
                 c.cl_live = live ? 1 : 0;
                 c.cl_rows = rows;
                 c.cl_sel = sel;
                 c.len[0] = L;
+                // the tile of the unit's window that holds the new row (position L - 1)
+                int app = -1;
+                if (fused && live) {
+                    const int rows_c = max(0, min(rows, p.comp_cap));
+                    const int n_s = max(0, rows_c - max(0, sel));
+                    const int ws = max(n_s, L - p.n_window);
+                    const int jn = p.page_size == 0 ? ((L - 1 - ws) >> 4) : (((L - 1) >> 4) - (ws >> 4));
+                    const int t_new = (64 * p.n_cbox + 16 * jn) / kTile;
+                    app = (t_new >= t0 && t_new < t1) ? t_new : -1;
+                }
+                c.cl_app_tile = app;
                 mbar_arrive(&c.unit_meta);
             }
         }
@@ -424,6 +438,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const int t_new = (64 * p.n_cbox + 16 * jn) / kTile;
                         const int t_end = min(ntiles_of(b) - 1, t + (n_tiles - 1 - i));
                         app_tile = (seg_len >= 1 && t_new >= t && t_new <= t_end) ? t_new : -1;
+                        if (clustered)
+                            app_tile = c.cl_app_tile;
                         appended = false;
                     }
                 }
@@ -522,7 +538,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                 }
                 if (fused && app_tile == t && !appended) {  // this tile holds the new row
-                    append_row(u, layer, b, kvh, L - 1);
+                    if (clustered) {  // written by softmax warp 2 at the start: wait for it
+                        bool w = true;
+                        if (lane == 0)
+                            w = mbar_wait(&c.app_ready, 0, &c.abort);
+                        if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) {
+                            if (lane == 0)
+                                fail(c, p.err);
+                            break;
+                        }
+                    } else {
+                        append_row(u, layer, b, kvh, L - 1);
+                    }
                     appended = true;
                 }
                 // ---- publish the tile, then issue ---------------------------------------
@@ -557,7 +584,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     else
                         tma_load_2d(dst, map, bar, 64 * half, y);
                 }
-                if (fused && app_tile >= 0 && !appended) {  // a later tile holds the new row
+                if (fused && !clustered && app_tile >= 0 && !appended) {  // a later tile holds it
                     append_row(u, layer, b, kvh, L - 1);
                     appended = true;
                 }
@@ -603,66 +630,88 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
     } else if (warp == 1) {
         // ================================ MMA issuer =====================================
+        // One thread issues, in tile order, S(i) = K_i Q^T once tile i has landed and its S
+        // buffer is free, and O(i) = V_i^T P_i^T once the softmax has written P_i: whichever
+        // is ready first, so a slow softmax on one tile does not hold back the next S.
         if (lane == 0 && n_tiles > 0) {
             constexpr uint32_t idesc_s = idesc_bf16(kTile, kOpRows, false, false);
             constexpr uint32_t idesc_o = idesc_bf16(kTile, kOpRows, true, false);
-            int seg = -1;
+            int seg = -1, ns = 0, np = 0;
             bool ok = true;
-            auto pv = [&](int j) -> bool {
-                const int s = j % kStages, bb = j & 1, use = j >> 1;
-                if (!mbar_wait(&c.p_full[bb], use & 1, &c.abort))
-                    return false;
-                if (!mbar_wait(&c.o_free[bb], (use & 1) ^ 1, &c.abort))
-                    return false;
-                tc_fence_after();
-                const uint32_t va = smem_u32(smem + s * kStageBytes + 2 * kChunkBytes);
-                const uint32_t pa = smem_u32(smem + kPOff + bb * kOpBytes);
+            uint32_t idle = 0;
+            uint64_t idle_t0 = 0;
+            while (np < n_tiles) {
+                bool prog = false;
+                if (ns < n_tiles) {
+                    const int s = ns % kStages, bb = ns & 1, use = ns >> 1;
+                    if (mbar_test_wait(&c.full[s], (ns / kStages) & 1) &&
+                        mbar_test_wait(&c.s_free[bb], (use & 1) ^ 1)) {
+                        if (ns == 0)
+                            SFI_STAMP(4);
+                        const int flags = c.meta[s].flags;
+                        if (flags & kFlagFirst)
+                            ++seg;
+                        tc_fence_after();
+                        const uint32_t ka = smem_u32(smem + s * kStageBytes);
+                        const uint32_t qa = smem_u32(smem + kQOff + (seg & 1) * kOpBytes);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t a = smem_desc_sw128(va + kk * 2048, kChunkBytes, 1024);
-                    const uint64_t bd = smem_desc_sw128(pa + (kk >> 2) * kOpChunk + (kk & 3) * 32, 16, 1024);
-                    umma_bf16(tmem + 32 + bb * 16, a, bd, idesc_o, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t a = smem_desc_sw128(ka + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024);
+                            const uint64_t bd = smem_desc_sw128(qa + (kk >> 2) * kOpChunk + (kk & 3) * 32, 16, 1024);
+                            umma_bf16(tmem + bb * 16, a, bd, idesc_s, kk > 0 ? 1u : 0u);
+                        }
+                        umma_commit(&c.s_full[bb]);
+                        if (ns == 0)
+                            SFI_STAMP(11);
+                        if (flags & kFlagLast)
+                            umma_commit(&c.q_free[seg & 1]);
+                        ++ns;
+                        prog = true;
+                    }
                 }
-                umma_commit(&c.o_full[bb]);
-                umma_commit(&c.empty[s]);
-                return true;
-            };
-            for (int i = 0; i < n_tiles && ok; ++i) {
-                const int s = i % kStages, bb = i & 1, use = i >> 1;
-                if (!mbar_wait(&c.full[s], (i / kStages) & 1, &c.abort)) {
-                    ok = false;
-                    break;
-                }
-                if (i == 0)
-                    SFI_STAMP(4);
-                const int flags = c.meta[s].flags;
-                if (flags & kFlagFirst)
-                    ++seg;
-                if (!mbar_wait(&c.s_free[bb], (use & 1) ^ 1, &c.abort)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t ka = smem_u32(smem + s * kStageBytes);
-                const uint32_t qa = smem_u32(smem + kQOff + (seg & 1) * kOpBytes);
+                if (np < ns) {
+                    const int s = np % kStages, bb = np & 1, use = np >> 1;
+                    if (mbar_test_wait(&c.p_full[bb], use & 1) &&
+                        mbar_test_wait(&c.o_free[bb], (use & 1) ^ 1)) {
+                        tc_fence_after();
+                        const uint32_t va = smem_u32(smem + s * kStageBytes + 2 * kChunkBytes);
+                        const uint32_t pa = smem_u32(smem + kPOff + bb * kOpBytes);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t a = smem_desc_sw128(ka + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(qa + (kk >> 2) * kOpChunk + (kk & 3) * 32, 16, 1024);
-                    umma_bf16(tmem + bb * 16, a, bd, idesc_s, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t a = smem_desc_sw128(va + kk * 2048, kChunkBytes, 1024);
+                            const uint64_t bd = smem_desc_sw128(pa + (kk >> 2) * kOpChunk + (kk & 3) * 32, 16, 1024);
+                            umma_bf16(tmem + 32 + bb * 16, a, bd, idesc_o, kk > 0 ? 1u : 0u);
+                        }
+                        umma_commit(&c.o_full[bb]);
+                        umma_commit(&c.empty[s]);
+                        if (np == 0)
+                            SFI_STAMP(15);
+                        ++np;
+                        prog = true;
+                    }
                 }
-                umma_commit(&c.s_full[bb]);
-                if (i == 0)
-                    SFI_STAMP(11);
-                if (flags & kFlagLast)
-                    umma_commit(&c.q_free[seg & 1]);
-                if (i > 0 && !pv(i - 1))
-                    ok = false;
-                if (i == 1)
-                    SFI_STAMP(15);
+                if (prog) {
+                    idle = 0;
+                    continue;
+                }
+                // nothing ready: yield the issue slot briefly; give up after kWaitTimeoutNs
+                // without progress, or as soon as another role has given up
+                if (idle > 8u)
+                    __nanosleep(20);
+                if ((++idle & 63u) == 0u) {
+                    if (c.abort) {
+                        ok = false;
+                        break;
+                    }
+                    const uint64_t now = global_timer_ns();
+                    if (idle == 64u)
+                        idle_t0 = now;
+                    else if (now - idle_t0 > kWaitTimeoutNs) {
+                        ok = false;
+                        break;
+                    }
+                }
             }
-            if (ok && !pv(n_tiles - 1))
-                ok = false;
             if (!ok)
                 fail(c, p.err);
             // All MMAs of this thread are complete once `drain` fires.
@@ -689,6 +738,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             le[h] = lr[h] = acc[h] = 0.f;
             fin_m[h] = -INFINITY;
             fin_lr[h] = 0.f;
+        }
+
+        if (clustered && fused && warp == 2 && c.cl_app_tile >= 0) {
+            // Clustered fused append, off the producer's path: the unit's new K and V rows go
+            // to cache position L - 1 (16 bytes per lane: lanes 0-15 K, 16-31 V); each lane
+            // fences its write against the async proxy before the warp signals app_ready, on
+            // which the producer waits before loading the box that covers the row.
+            const int u = static_cast<int>(blockIdx.x) / p.cluster;
+            const int b = (u / Hkv) % B, layer = u / (Hkv * B), kvh = u % Hkv;
+            const int pos = c.len[0] - 1;
+            long long r = static_cast<long long>(u) * p.capacity + pos;
+            bool good = true;
+            if (p.page_size != 0) {
+                const int page = __ldg(p.page_table + b * p.max_pages + (pos >> 4));
+                good = page >= 0 && page < p.n_pages;
+                if (!good && lane == 0)
+                    raise_error(p.err, 0x1u);  // SFI_DEVERR_PAGE_RANGE
+                r = ((static_cast<long long>(layer) * p.n_pages + page) * Hkv + kvh) * 16 + (pos & 15);
+            }
+            if (good) {
+                const int kvsel = lane >> 4, chunk = lane & 15;
+                const uint4 x = static_cast<const uint4 *>(kvsel ? p.v_new : p.k_new)
+                    [static_cast<size_t>(u) * 16 + chunk];
+                static_cast<uint4 *>(kvsel ? p.v_cache : p.k_cache)[r * 16 + chunk] = x;
+                fence_proxy_async_global();
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&c.app_ready);
         }
 
         auto finalize = [&](int u, const float (&fm)[G], const float (&fle)[G],
@@ -982,72 +1060,68 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             SFI_STAMP(9);
         if (clustered && c.cl_live) {
             // ---- merge the cluster's partials through distributed shared memory ----------
-            // Every CTA of a live cluster takes part, even after a failed wait, so that no
-            // peer waits for it; outputs are written only when everything succeeded. The
-            // partial goes to this CTA's stage-0 buffer, idle now: acc [G][128], m [G], l [G].
-            const int C = p.cluster;
+            // CTA r owns dims [r 128/C, (r+1) 128/C). Every CTA pushes, with remote stores,
+            // its (max, sum) and its unnormalised outputs of each owner's dims into that
+            // owner's receive area (the second Q buffer: a clustered CTA has one segment and
+            // uses only the first), then one lane per owner arrives on the owner's cl_ready
+            // with release semantics. An owner that has seen all C arrivals merges from its
+            // own shared memory; after that no peer touches it, so it may exit. Every CTA of
+            // a live cluster pushes and arrives even after a failed wait, so no peer waits for
+            // it; outputs are written only when everything succeeded.
+            const int C = p.cluster;           // 2, 4 or 8 (group <= 4: see the host)
+            const int nd = kHeadDim / C;       // dims per owner
             const int rank = static_cast<int>(blockIdx.x) % C;
             const int u = static_cast<int>(blockIdx.x) / C;
-            float *part = reinterpret_cast<float *>(smem);
+            float *recv = reinterpret_cast<float *>(smem + kQOff + kOpBytes);
+            // receive layout: acc [src][G][nd], then stats [src][G][2] (max, sum)
+            const int acc_floats = C * G * nd;
+            {
+                const int owner = row / nd, j = row - owner * nd;
+                const uint32_t base = map_to_rank(recv, static_cast<uint32_t>(owner));
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                part[h * kHeadDim + row] = acc[h];
-                if (row == h) {
-                    part[G * kHeadDim + h] = fin_m[h];
-                    part[G * kHeadDim + G + h] = fin_lr[h];
+                for (int h = 0; h < G; ++h)
+                    st_cluster_f32(base + 4u * ((rank * G + h) * nd + j), acc[h]);
+                if (row < C * G) {  // (max, sum) of head h to owner row / G
+                    const int ow = row / G, h = row - ow * G;
+                    const uint32_t b2 = map_to_rank(recv, static_cast<uint32_t>(ow));
+                    const int o2 = acc_floats + (rank * G + h) * 2;
+                    st_cluster_f32(b2 + 4u * o2, pick<G>(fin_m, h));
+                    st_cluster_f32(b2 + 4u * (o2 + 1), pick<G>(fin_lr, h));
                 }
             }
-            bool good = group_sync(c, gphase, lane) && ok;  // all four warps' writes are done
             if (row == 0)
-                for (int r = 0; r < C; ++r)
-                    mbar_arrive_cluster(map_to_rank(&c.cl_ready, static_cast<uint32_t>(r)));
-            good = mbar_wait_cluster(&c.cl_ready, 0, kWaitTimeoutNs) && good;
+                SFI_STAMP(26);
+            bool good = group_sync(c, gphase, lane) && ok;  // every thread's pushes are issued
+            if (row < C)  // lanes 0..C-1 of one warp, one owner each, in parallel
+                mbar_arrive_cluster(map_to_rank(&c.cl_ready, static_cast<uint32_t>(row)));
+            if (row == 0)
+                SFI_STAMP(28);
+            // A peer arrives within its own bounded waits even when it fails; this limit is
+            // well above those, so no CTA leaves while a live peer may still push to it.
+            good = mbar_wait_cluster(&c.cl_ready, 0, 8 * kWaitTimeoutNs) && good;
             if (row == 0)
                 SFI_STAMP(24);
             if (good) {
-                // this CTA finishes dims [d0, d0 + nd) of every head
-                const int d0 = rank * kHeadDim / C, nd = (rank + 1) * kHeadDim / C - d0;
                 for (int o = row; o < nd * G; o += 4 * 32) {
-                    const int h = o % G, d = d0 + o / G;
-                    float mr[8], lrr[8], ar[8];
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) {
-                        if (r < C) {
-                            const uint32_t base = map_to_rank(part, static_cast<uint32_t>(r));
-                            mr[r] = ld_cluster_f32(base + 4u * (G * kHeadDim + h));
-                            lrr[r] = ld_cluster_f32(base + 4u * (G * kHeadDim + G + h));
-                            ar[r] = ld_cluster_f32(base + 4u * (h * kHeadDim + d));
-                        }
-                    }
+                    const int h = o / nd, j = o - h * nd;
                     float M = -INFINITY;
-#pragma unroll
-                    for (int r = 0; r < 8; ++r)
-                        if (r < C)
-                            M = fmaxf(M, mr[r]);
+                    for (int q = 0; q < C; ++q)
+                        M = fmaxf(M, recv[acc_floats + (q * G + h) * 2]);
                     float Lr = 0.f, O = 0.f;
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) {
-                        if (r < C) {
-                            const float w = (mr[r] == -INFINITY) ? 0.f : exp2f(mr[r] - M);
-                            Lr = fmaf(w, lrr[r], Lr);
-                            O = fmaf(w, ar[r], O);
-                        }
+                    for (int q = 0; q < C; ++q) {
+                        const float mq = recv[acc_floats + (q * G + h) * 2];
+                        const float w = (mq == -INFINITY) ? 0.f : exp2f(mq - M);
+                        Lr = fmaf(w, recv[acc_floats + (q * G + h) * 2 + 1], Lr);
+                        O = fmaf(w, recv[(q * G + h) * nd + j], O);
                     }
                     const float v = Lr > 0.f ? O / Lr : 0.f;
-                    const size_t idx = (static_cast<size_t>(u) * G + h) * kHeadDim + d;
+                    const size_t idx = (static_cast<size_t>(u) * G + h) * kHeadDim + rank * nd + j;
                     if (p.out_fp32)
                         static_cast<float *>(p.out)[idx] = v;
                     else
                         static_cast<__nv_bfloat16 *>(p.out)[idx] = __float2bfloat16_rn(v);
                 }
             }
-            // Peers may read this CTA's partial until each has said it is done; the CTA
-            // stays resident (its shared memory valid) until then.
-            good = group_sync(c, gphase, lane) && good;
-            if (row == 0)
-                for (int r = 0; r < C; ++r)
-                    mbar_arrive_cluster(map_to_rank(&c.cl_done, static_cast<uint32_t>(r)));
-            good = mbar_wait_cluster(&c.cl_done, 0, 8 * kWaitTimeoutNs) && good;
             if (row == 0)
                 SFI_STAMP(25);
             if (!good)
@@ -1178,7 +1252,9 @@ int sparse_cluster_size(int group, int units, int max_cluster)
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesCached)
         return 1;
     const int gi = group == 1 ? 0 : group == 2 ? 1 : group == 4 ? 2 : 3;
-    for (int C = max_cluster < 8 ? max_cluster : 8; C >= 2; --C) {
+    for (int C = 8; C >= 2; C >>= 1) {  // powers of two: each CTA owns 128 / C dims
+        if (C > max_cluster)
+            continue;
         int n;
         {
             std::lock_guard<std::mutex> lock(g_cluster_mu);

@@ -94,8 +94,8 @@ cudaError_t launch_attention(bool dense, int group, const CUtensorMap &tm_k,
                              const CUtensorMap &tm_v, const CUtensorMap &tm_q,
                              const CUtensorMap &tm_kc, const CUtensorMap &tm_vc,
                              const AttnParams &p, int grid, cudaStream_t stream);
-// Largest cluster size (<= max_cluster) for which `units` clusters of the sparse kernel can
-// be resident at once (1 when none above 1 fits).
+// Largest cluster size (8, 4 or 2, at most max_cluster) for which `units` clusters of the
+// sparse kernel can be resident at once (1 when none fits).
 int sparse_cluster_size(int group, int units, int max_cluster);
 cudaError_t launch_evidence(const float *zbuf, const float2 *stats, float *f,
                             const int32_t *seq_len, const uint8_t *active, int n_layers,
