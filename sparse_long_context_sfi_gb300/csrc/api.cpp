@@ -396,8 +396,17 @@ sfi_status sfi_select(const sfi_kv_cache *kv, const float *scores_f, const sfi_b
     // Stage in shared memory when every unit's candidates (with up to 3 values of alignment
     // slack on either side) fit, and the copy's tail stays inside the unit's row.
     const long long bound = static_cast<long long>(kv->max_len) - budget->n_window - budget->n_sink;
-    p.staged = (aligned16(scores_f) && bound + 3 <= kStageCap &&
-                static_cast<long long>(kv->max_len) - budget->n_window + 3 <= kv->capacity) ? 1 : 0;
+    const bool stageable = aligned16(scores_f) &&
+                           static_cast<long long>(kv->max_len) - budget->n_window + 3 <= kv->capacity;
+    p.staged = (stageable && bound + 3 <= kStageCap) ? 1 : 0;
+    // A unit's candidates split over a cluster of CTAs (each stages its share) when they fit.
+    p.cluster = 1;
+    if (stageable) {
+        const int C = select_cluster_size(4);
+        const long long ctas = static_cast<long long>(p.n_units) * C;
+        if (C > 1 && (bound + C - 1) / C <= select_cluster_key_cap() && ctas <= 2LL * sm_count())
+            p.cluster = C;  // at most about two waves of CTAs
+    }
     return launch_status(launch_select(p, as_stream(stream)));
 }
 
@@ -662,6 +671,11 @@ sfi_status sfi_clear_error(const sfi_kv_cache *kv, void *stream)
 int sfi_trace_read(unsigned long long *host, int n_ctas)
 {
     return static_cast<int>(sfi::trace_read(host, n_ctas));
+}
+
+int sfi_trace_read_select(unsigned long long *host, int n_ctas)
+{
+    return static_cast<int>(sfi::trace_read_select(host, n_ctas));
 }
 #endif
 

@@ -77,19 +77,29 @@ __global__ void __launch_bounds__(256) refine_kernel(const RefineParams p)
     const int L = min(p.seq_len[b], p.capacity);
     const int nC = max(0, L - p.n_window - p.n_sink);
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    // fp64 is slow here: one thread computes the constants for the block
+    __shared__ float sh_c[5];
+    if (threadIdx.x == 0) {
+        const int tau = p.prior_tau;
+        const double Z = (nC >= tau) ? (tau + 1) * 0.5 + static_cast<double>(nC - tau)
+                                     : static_cast<double>(nC) * (nC + 1) / (2.0 * tau);
+        sh_c[0] = __double2float_rn(1.0 - p.lambda);
+        sh_c[1] = __double2float_rn(p.lambda / Z);
+        sh_c[2] = __double2float_rn(1.0 / tau);
+        sh_c[3] = __double2float_rn(p.lambda);
+        sh_c[4] = H > 1 ? __double2float_rn(static_cast<double>(p.excl_mu) / (H - 1)) : 0.f;
+    }
+    __syncthreads();
     if (i >= nC)
         return;
-    const int tau = p.prior_tau;
-    const double Z = (nC >= tau) ? (tau + 1) * 0.5 + static_cast<double>(nC - tau)
-                                 : static_cast<double>(nC) * (nC + 1) / (2.0 * tau);
     Fused fz;
     fz.p = &p;
     fz.L = L;
     fz.nC = nC;
-    fz.c1 = __double2float_rn(1.0 - p.lambda);
-    fz.c2 = __double2float_rn(p.lambda / Z);
-    fz.inv_tau = __double2float_rn(1.0 / tau);
-    fz.lam = __double2float_rn(p.lambda);
+    fz.c1 = sh_c[0];
+    fz.c2 = sh_c[1];
+    fz.inv_tau = sh_c[2];
+    fz.lam = sh_c[3];
     const int u0 = lb * H;  // units of this (layer, sequence) are u0 .. u0 + H - 1
     float sp[kMaxHeads];
     for (int h = 0; h < H; ++h) {
@@ -104,7 +114,7 @@ __global__ void __launch_bounds__(256) refine_kernel(const RefineParams p)
         sp[h] = (p.nms_radius > 0 && v < best) ? __fmul_rn(p.nms_gamma, v) : v;
     }
     if (p.excl_mu != 0.f && H > 1) {
-        const float mu1 = __double2float_rn(static_cast<double>(p.excl_mu) / (H - 1));
+        const float mu1 = sh_c[4];
         float T = 0.f;
         for (int h = 0; h < H; ++h)
             T = __fadd_rn(T, sp[h]);

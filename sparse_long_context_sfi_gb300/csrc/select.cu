@@ -11,9 +11,12 @@
 // any IEEE host.
 //
 // When the unit's candidates fit (up to kStageCap evidence values), the evidence is first
-// copied into shared memory with bulk asynchronous copies and every pass reads it there;
+// copied into shared memory (16-byte loads from every thread, all in flight together),
+// turned into keys in place by the first pass, and every later pass reads the keys there;
 // otherwise the passes stream it from global memory (L2-resident after the first) with
 // eight loads per thread in flight.
+#include <mutex>
+
 #include "sfi_device.cuh"
 
 namespace sfi {
@@ -23,6 +26,16 @@ constexpr int NT = kSelectThreads;
 constexpr int kWarps = NT / 32;
 constexpr int kListCap = 8192;    // keys gathered for the refining passes
 constexpr int kBatch = 8;         // candidates per thread per streaming step
+
+// Optional per-CTA timeline for tuning (compile with -DSFI_TRACE), read back through
+// sfi_trace_read_select. Off in normal builds.
+#ifdef SFI_TRACE
+__device__ unsigned long long g_sel_trace[1024][16];
+#define SEL_STAMP(slot) \
+    do { if (threadIdx.x == 0) g_sel_trace[blockIdx.x & 1023][(slot)] = global_timer_ns(); } while (0)
+#else
+#define SEL_STAMP(slot) ((void)0)
+#endif
 
 __device__ __forceinline__ uint32_t order_key(float x)
 {
@@ -43,6 +56,18 @@ struct Fuse {
         return order_key(s);
     }
 };
+
+// Constants of the fused score for nC candidates (the prior's closed-form normaliser Z in
+// fp64, then rounded once): c[0] = fl32(1 - lambda), c[1] = fl32(lambda / Z),
+// c[2] = fl32(1 / tau).
+__device__ __forceinline__ void prior_consts(int nC, int tau, double lambda, float *c)
+{
+    const double Z = (nC >= tau) ? (tau + 1) * 0.5 + static_cast<double>(nC - tau)
+                                 : static_cast<double>(nC) * (nC + 1) / (2.0 * tau);
+    c[0] = __double2float_rn(1.0 - lambda);
+    c[1] = __double2float_rn(lambda / Z);
+    c[2] = __double2float_rn(1.0 / tau);
+}
 
 // Block-wide exclusive scan of one int per thread; returns the exclusive prefix and
 // writes the block total to *total. Uses `scratch` (>= kWarps + 1 ints).
@@ -80,17 +105,6 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *scratch, int *to
     return r;
 }
 
-// 1-D bulk copy global -> this CTA's shared memory, completing on `bar` (transaction
-// bytes). Both addresses 16-byte aligned, size a multiple of 16.
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
 // Dynamic shared memory: nsub sub-histograms of 4096 bins (warps w with w % nsub equal
 // share one, so fewer lanes collide on a bin), the gathered list, then (staged mode) the
 // evidence of the unit's candidates.
@@ -100,24 +114,62 @@ size_t select_smem_bytes(bool staged)
            (staged ? static_cast<size_t>(kStageCap) * sizeof(float) : 0);
 }
 
+// Exclusive scan over the warps of the block of one (a, b) pair per warp, given by lane 0;
+// returns the pair of the warps before this one (in every lane) and writes the totals.
+// Uses `scratch` (>= 2 kWarps + 2 ints).
+__device__ __forceinline__ int2 warp_totals_exclusive_scan(int a, int b, int *scratch, int2 *total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+        scratch[warp] = a;
+        scratch[kWarps + warp] = b;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int x = lane < kWarps ? scratch[lane] : 0;
+        const int y = lane < kWarps ? scratch[kWarps + lane] : 0;
+        int xi = x, yi = y;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int xu = __shfl_up_sync(0xffffffffu, xi, o);
+            const int yu = __shfl_up_sync(0xffffffffu, yi, o);
+            if (lane >= o) {
+                xi += xu;
+                yi += yu;
+            }
+        }
+        __syncwarp();
+        if (lane < kWarps) {
+            scratch[lane] = xi - x;
+            scratch[kWarps + lane] = yi - y;
+        }
+        if (lane == kWarps - 1) {
+            scratch[2 * kWarps] = xi;
+            scratch[2 * kWarps + 1] = yi;
+        }
+    }
+    __syncthreads();
+    const int2 r = make_int2(scratch[warp], scratch[kWarps + warp]);
+    *total = make_int2(scratch[2 * kWarps], scratch[2 * kWarps + 1]);
+    __syncthreads();
+    return r;
+}
+
 // At most 56 registers per thread: a 1024-thread CTA then takes 7/8 of the register file
 // instead of all of it, so a launch under a profiler, which may need a few more, still fits.
 __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
 {
-    __shared__ int scratch[kWarps + 1];
+    __shared__ int scratch[2 * kWarps + 2];
     __shared__ uint32_t sh_digit;
     __shared__ int sh_above;
     __shared__ int sh_count;
-    __shared__ __align__(8) uint64_t stage_bar;
+    __shared__ float sh_c[3];
 
     pdl_trigger();
+    SEL_STAMP(0);
     const int tid = threadIdx.x, lane = tid & 31;
-    if (tid == 0) {
-        mbar_init(&stage_bar, 1);
-        mbar_fence_init();
-    }
-    __syncthreads();
     pdl_wait();
+    SEL_STAMP(8);
     const int u = blockIdx.x;
     const int b = (u / p.n_kv_heads) % p.batch;
     if (p.active && !p.active[b])
@@ -137,12 +189,10 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
     const float *fg = p.f + static_cast<size_t>(u) * p.capacity + S;
     Fuse fz;
     fz.n = nC;
-    const int tau = p.prior_tau;
-    const double Z = (nC >= tau) ? (tau + 1) * 0.5 + static_cast<double>(nC - tau)
-                                 : static_cast<double>(nC) * (nC + 1) / (2.0 * tau);
-    fz.c1 = __double2float_rn(1.0 - p.lambda);
-    fz.c2 = __double2float_rn(p.lambda / Z);
-    fz.inv_tau = __double2float_rn(1.0 / tau);
+    // fp64 is slow here: one thread computes the prior's constants, published by the
+    // barrier that ends the staging
+    if (tid == 0)
+        prior_consts(nC, p.prior_tau, p.lambda, sh_c);
 
     extern __shared__ __align__(16) uint32_t dyn[];
     const int nsub = p.staged ? 2 : 4;
@@ -158,29 +208,44 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(fg);
     const int off = p.staged ? static_cast<int>((a0 & 15u) >> 2) : 0;
     const bool staged = p.staged && off + nC <= kStageCap;
-    if (staged && tid == 0) {
-        const char *src = reinterpret_cast<const char *>(fg - off);
-        const uint32_t bytes = static_cast<uint32_t>(((off + nC) * 4 + 15) & ~15);
-        mbar_arrive_expect_tx(&stage_bar, bytes);
-        constexpr uint32_t kChunk = 16384;
-        for (uint32_t o = 0; o < bytes; o += kChunk)
-            bulk_load(reinterpret_cast<char *>(fs) + o, src + o,
-                      bytes - o < kChunk ? bytes - o : kChunk, &stage_bar);
+    if (staged) {
+        // every thread copies its 16-byte pieces; all loads are in flight before any store
+        const uint4 *src = reinterpret_cast<const uint4 *>(fg - off);
+        uint4 *dst = reinterpret_cast<uint4 *>(fs);
+        const int n16 = ((off + nC) * 4 + 15) >> 4;
+        for (int b0 = 0; b0 < n16; b0 += 8 * NT) {
+            uint4 x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int i = b0 + e * NT + tid;
+                if (i < n16)
+                    x[e] = src[i];
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int i = b0 + e * NT + tid;
+                if (i < n16)
+                    dst[i] = x[e];
+            }
+        }
     }
     for (int i = tid; i < nsub * 4096; i += NT)
         hist[i] = 0u;
     if (tid == 0)
         sh_count = 0;
-    if (staged && !mbar_wait(&stage_bar, 0, nullptr)) {
-        // gave up: report, let the copies land (bounded again) and leave
-        raise_error(p.err, 0x4u);  // SFI_DEVERR_TIMEOUT
-        mbar_wait(&stage_bar, 0, nullptr);
-        return;
-    }
     __syncthreads();
+    SEL_STAMP(1);
+    fz.c1 = sh_c[0];
+    fz.c2 = sh_c[1];
+    fz.inv_tau = sh_c[2];
 
-    auto fval = [&](int i) -> float { return staged ? fs[off + i] : __ldg(fg + i); };
-    auto key_at = [&](int i) -> uint32_t { return fz.key(fval(i), i); };
+    // staged mode: pass 0 turns each staged evidence value into its key in place, and the
+    // later passes read the keys; streaming mode recomputes keys from global memory
+    uint32_t *ks = reinterpret_cast<uint32_t *>(fs) + off;
+    bool keys_ready = false;
+    auto key_at = [&](int i) -> uint32_t {
+        return keys_ready ? ks[i] : fz.key(staged ? fs[off + i] : __ldg(fg + i), i);
+    };
     int nbins = 4096;
     auto count = [&](bool part, uint32_t digit) {
         if (part)
@@ -213,11 +278,19 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
     };
     // keys of candidates base + e * NT + tid, e < kBatch (all loads in flight together)
     auto load_batch = [&](int base, uint32_t (&k)[kBatch]) {
+        if (keys_ready) {
+#pragma unroll
+            for (int e = 0; e < kBatch; ++e) {
+                const int i = base + e * NT + tid;
+                k[e] = i < nC ? ks[i] : 0u;
+            }
+            return;
+        }
         float v[kBatch];
 #pragma unroll
         for (int e = 0; e < kBatch; ++e) {
             const int i = base + e * NT + tid;
-            v[e] = i < nC ? fval(i) : 0.f;
+            v[e] = i < nC ? (staged ? fs[off + i] : __ldg(fg + i)) : 0.f;
         }
 #pragma unroll
         for (int e = 0; e < kBatch; ++e)
@@ -230,12 +303,19 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
         uint32_t k[kBatch];
         load_batch(base, k);
 #pragma unroll
-        for (int e = 0; e < kBatch; ++e)
-            count(base + e * NT + tid < nC, k[e] >> 20);
+        for (int e = 0; e < kBatch; ++e) {
+            const int i = base + e * NT + tid;
+            if (staged && i < nC)
+                ks[i] = k[e];  // each thread overwrites only values it has read itself
+            count(i < nC, k[e] >> 20);
+        }
     }
     __syncthreads();
+    keys_ready = staged;
+    SEL_STAMP(2);
     int krem = K;
     find_digit(4096, krem);
+    SEL_STAMP(3);
     const uint32_t d0 = sh_digit;
     uint32_t prefix = d0 << 20, pmask = 0xFFF00000u;
     krem -= sh_above;
@@ -260,6 +340,7 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
         }
         __syncthreads();
     }
+    SEL_STAMP(4);
     // passes 1 and 2: 10-bit digits, over the gathered list (or every candidate)
 #pragma unroll 1
     for (int pass = 1; pass < 3; ++pass) {
@@ -290,58 +371,345 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
         pmask |= 1023u << shift;
         krem -= sh_above;
         __syncthreads();
+        SEL_STAMP(4 + pass);
     }
     const uint32_t thr = prefix;  // exact key of the K-th largest score
     const int need_eq = krem;     // how many keys equal to thr are taken (lowest first)
 
+    SEL_STAMP(9);
     // ---- ordered compaction ------------------------------------------------------------
     // A chosen candidate's slot = (keys > thr before it) + min(keys == thr before it,
-    // need_eq), so one block scan of packed (equal << 16 | greater) counts per chunk of
-    // 8 x NT candidates places every chosen index in ascending order.
-    int gt_base = 0, eq_base = 0;
-    for (int base = 0; base < nC; base += 8 * NT) {
-        uint32_t k[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int i = base + 8 * tid + e;
-            k[e] = i < nC ? key_at(i) : 0u;
-        }
+    // need_eq). Warp w takes one contiguous range of candidates, 32 per step (lane =
+    // candidate): ballots count its greater and equal keys; one scan over the warps gives
+    // every warp its starting counts; a second pass over its keys writes the chosen
+    // positions in ascending order.
+    {
+        const int warp = tid >> 5;
+        const unsigned lt_mask = (1u << lane) - 1u;
+        const int span = (nC + kWarps * 32 - 1) / (kWarps * 32) * 32;  // per warp
+        const int w0 = warp * span, w1 = min(nC, w0 + span);
         int n_gt = 0, n_eq = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const bool in = base + 8 * tid + e < nC;
-            n_gt += (in && k[e] > thr) ? 1 : 0;
-            n_eq += (in && k[e] == thr) ? 1 : 0;
+        for (int i0 = w0; i0 < w1; i0 += 32) {
+            const int i = i0 + lane;
+            const bool in = i < w1;
+            const uint32_t k = in ? key_at(i) : 0u;
+            n_gt += __popc(__ballot_sync(0xffffffffu, in && k > thr));
+            n_eq += __popc(__ballot_sync(0xffffffffu, in && k == thr));
         }
-        int tot;
-        const int packed = block_exclusive_scan((n_eq << 16) | n_gt, scratch, &tot);
-        int gt_before = gt_base + (packed & 0xFFFF);
-        int eq_before = eq_base + (packed >> 16);
+        SEL_STAMP(10);
+        int2 tot;
+        const int2 before = warp_totals_exclusive_scan(n_gt, n_eq, scratch, &tot);
+        SEL_STAMP(11);
+        int gt_before = before.x, eq_before = before.y;
+        for (int i0 = w0; i0 < w1; i0 += 32) {
+            const int i = i0 + lane;
+            const bool in = i < w1;
+            const uint32_t k = in ? key_at(i) : 0u;
+            const unsigned gm = __ballot_sync(0xffffffffu, in && k > thr);
+            const unsigned em = __ballot_sync(0xffffffffu, in && k == thr);
+            const int g_lt = gt_before + __popc(gm & lt_mask);
+            const int e_lt = eq_before + __popc(em & lt_mask);
+            if ((gm >> lane) & 1u)
+                out[g_lt + min(e_lt, need_eq)] = S + i;
+            else if (((em >> lane) & 1u) && e_lt < need_eq)
+                out[g_lt + e_lt] = S + i;
+            gt_before += __popc(gm);
+            eq_before += __popc(em);
+        }
+    }
+    if (tid == 0) {
+        p.sel_cnt[u] = K;
+        SEL_STAMP(7);
+    }
+#ifdef SFI_TRACE
+    if (tid == 0)
+        g_sel_trace[blockIdx.x & 1023][12] = static_cast<unsigned long long>(n_lst);
+#endif
+}
+
+// ---------------------------------------------------------------------------------------
+// Clustered Selector: the C CTAs of a cluster share one unit. CTA r stages the evidence of
+// candidates [r nC / C, (r+1) nC / C) in its shared memory, turns it into keys, and builds
+// a local histogram per radix pass; after one cluster barrier every CTA sums all C local
+// histograms through distributed shared memory and finds the same digit. Histograms are
+// double-buffered, so a CTA that has passed pass p's barrier never overwrites a buffer a peer
+// may still read. The ordered output exchanges each CTA's (greater, equal) counts the same
+// way. Every CTA of a cluster runs every barrier: the only early exits (inactive sequence,
+// all candidates kept) are taken by all of them together.
+
+constexpr int kClusterKeyCap = 33280;  // candidates per CTA (a 131K context in 4 CTAs)
+
+size_t select_cluster_smem_bytes()
+{
+    // keys: up to kClusterKeyCap candidates, 3 words of alignment slack before them and up
+    // to 3 after (the copy is whole 16-byte pieces)
+    return (3 * 4096 + kClusterKeyCap + 8) * sizeof(uint32_t);
+}
+
+__global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
+{
+    __shared__ int scratch[2 * kWarps + 2];
+    __shared__ uint32_t sh_digit;
+    __shared__ int sh_above;
+    __shared__ int sh_counts[2];  // this CTA's (greater, equal) keys for the ordered output
+    __shared__ float sh_c[3];
+
+    pdl_trigger();
+    SEL_STAMP(0);
+    pdl_wait();
+    SEL_STAMP(8);
+    const int C = p.cluster;
+    const int rank = static_cast<int>(blockIdx.x) % C;
+    const int u = static_cast<int>(blockIdx.x) / C;
+    const int b = (u / p.n_kv_heads) % p.batch;
+    if (p.active && !p.active[b])
+        return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int L = min(p.seq_len[b], p.capacity);
+    const int S = p.n_sink, W = p.n_window;
+    const int nC = max(0, L - W - S);
+    const int K = min(p.n_select, nC);
+    const int c0 = static_cast<int>(static_cast<long long>(rank) * nC / C);
+    const int c1 = static_cast<int>(static_cast<long long>(rank + 1) * nC / C);
+    const int nloc = c1 - c0;
+    int32_t *out = p.sel_idx + static_cast<size_t>(u) * p.n_select;
+    if (K == nC) {  // every candidate is kept (includes K == 0)
+        for (int i = c0 + tid; i < c1; i += NT)
+            out[i] = S + i;
+        if (tid == 0 && rank == 0)
+            p.sel_cnt[u] = nC;
+        return;
+    }
+    Fuse fz;
+    fz.n = nC;
+    // fp64 is slow here: one thread computes the prior's constants, published by the
+    // barrier that ends the staging
+    if (tid == 0)
+        prior_consts(nC, p.prior_tau, p.lambda, sh_c);
+
+    extern __shared__ __align__(16) uint32_t dyn[];
+    uint32_t *hbuf0 = dyn, *hbuf1 = dyn + 4096;  // local histograms, by pass parity
+    uint32_t *gsum = dyn + 2 * 4096;             // the cluster's sums
+    uint32_t *kraw = dyn + 3 * 4096;             // staged evidence, then keys
+
+    // ---- stage this CTA's candidates (16-byte loads, all in flight together) ------------
+    const float *fg = p.f + static_cast<size_t>(u) * p.capacity + S + c0;
+    const int off = static_cast<int>((reinterpret_cast<uintptr_t>(fg) & 15u) >> 2);
+    {
+        const uint4 *src = reinterpret_cast<const uint4 *>(fg - off);
+        uint4 *dst = reinterpret_cast<uint4 *>(kraw);
+        const int n16 = ((off + nloc) * 4 + 15) >> 4;
+        for (int b0 = 0; b0 < n16; b0 += 4 * NT) {
+            uint4 x[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int i = base + 8 * tid + e;
-            if (i >= nC)
-                break;
-            if (k[e] > thr) {
-                out[gt_before + min(eq_before, need_eq)] = S + i;
-                ++gt_before;
-            } else if (k[e] == thr) {
-                if (eq_before < need_eq)
-                    out[gt_before + eq_before] = S + i;
-                ++eq_before;
+            for (int e = 0; e < 4; ++e) {
+                const int i = b0 + e * NT + tid;
+                if (i < n16)
+                    x[e] = src[i];
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = b0 + e * NT + tid;
+                if (i < n16)
+                    dst[i] = x[e];
             }
         }
-        gt_base += tot & 0xFFFF;
-        eq_base += tot >> 16;
     }
-    if (tid == 0)
+    for (int i = tid; i < 4096; i += NT)
+        hbuf0[i] = 0u;
+    __syncthreads();
+    SEL_STAMP(1);
+    fz.c1 = sh_c[0];
+    fz.c2 = sh_c[1];
+    fz.inv_tau = sh_c[2];
+    uint32_t *ks = kraw + off;  // ks[i] = key of candidate c0 + i
+
+    // ---- pass 0: keys in place, top-12-bit histogram --------------------------------------
+    for (int i = tid; i < nloc; i += NT) {
+        const uint32_t k = fz.key(__uint_as_float(ks[i]), c0 + i);
+        ks[i] = k;
+        atomicAdd(&hbuf0[k >> 20], 1u);
+    }
+    // digit of the cluster histogram (nb bins) where the running count from the top first
+    // reaches krem; every CTA computes the same one
+    auto merged_digit = [&](const uint32_t *mine, int nb, int krem_now) {
+        cluster_sync_all();  // every CTA's local histogram of this pass is complete
+        for (int bin = tid; bin < nb; bin += NT) {
+            uint32_t h = 0;
+            for (int r = 0; r < C; ++r)
+                h += ld_cluster_u32(map_to_rank(mine + bin, static_cast<uint32_t>(r)));
+            gsum[bin] = h;
+        }
+        __syncthreads();
+        const int per = nb / NT;
+        int mine_cnt = 0;
+        for (int j = 0; j < per; ++j)
+            mine_cnt += static_cast<int>(gsum[nb - 1 - (per * tid + j)]);
+        int total;
+        int before = block_exclusive_scan(mine_cnt, scratch, &total);
+        for (int j = 0; j < per; ++j) {
+            const int bin = nb - 1 - (per * tid + j);
+            const int h = static_cast<int>(gsum[bin]);
+            if (before < krem_now && before + h >= krem_now) {
+                sh_digit = static_cast<uint32_t>(bin);
+                sh_above = before;
+            }
+            before += h;
+        }
+        __syncthreads();
+    };
+    int krem = K;
+    SEL_STAMP(2);
+    merged_digit(hbuf0, 4096, krem);
+    SEL_STAMP(3);
+    uint32_t prefix = sh_digit << 20, pmask = 0xFFF00000u;
+    krem -= sh_above;
+    // passes 1 and 2: 10-bit digits over this CTA's keys that share the prefix
+#pragma unroll 1
+    for (int pass = 1; pass < 3; ++pass) {
+        const int shift = pass == 1 ? 10 : 0;
+        uint32_t *hb = (pass & 1) ? hbuf1 : hbuf0;
+        for (int i = tid; i < 1024; i += NT)
+            hb[i] = 0u;
+        __syncthreads();
+        for (int i = tid; i < nloc; i += NT) {
+            const uint32_t k = ks[i];
+            if ((k & pmask) == prefix)
+                atomicAdd(&hb[(k >> shift) & 1023u], 1u);
+        }
+        merged_digit(hb, 1024, krem);
+        prefix |= sh_digit << shift;
+        pmask |= 1023u << shift;
+        krem -= sh_above;
+        __syncthreads();
+        SEL_STAMP(4 + pass);
+    }
+    const uint32_t thr = prefix;  // exact key of the K-th largest score
+    const int need_eq = krem;     // how many keys equal to thr are taken (lowest first)
+
+    // ---- ordered compaction (as in select_kernel, offset by the CTAs before this one) ----
+    const unsigned lt_mask = (1u << lane) - 1u;
+    const int span = (nloc + kWarps * 32 - 1) / (kWarps * 32) * 32;
+    const int w0 = warp * span, w1 = min(nloc, w0 + span);
+    int n_gt = 0, n_eq = 0;
+    for (int i0 = w0; i0 < w1; i0 += 32) {
+        const int i = i0 + lane;
+        const bool in = i < w1;
+        const uint32_t k = in ? ks[i] : 0u;
+        n_gt += __popc(__ballot_sync(0xffffffffu, in && k > thr));
+        n_eq += __popc(__ballot_sync(0xffffffffu, in && k == thr));
+    }
+    int2 tot;
+    const int2 before = warp_totals_exclusive_scan(n_gt, n_eq, scratch, &tot);
+    if (tid == 0) {
+        sh_counts[0] = tot.x;
+        sh_counts[1] = tot.y;
+    }
+    SEL_STAMP(10);
+    cluster_sync_all();  // every CTA's counts are in place
+    SEL_STAMP(11);
+    int gt_before = before.x, eq_before = before.y;
+    for (int r = 0; r < rank; ++r) {
+        gt_before += static_cast<int>(ld_cluster_u32(map_to_rank(&sh_counts[0], static_cast<uint32_t>(r))));
+        eq_before += static_cast<int>(ld_cluster_u32(map_to_rank(&sh_counts[1], static_cast<uint32_t>(r))));
+    }
+    for (int i0 = w0; i0 < w1; i0 += 32) {
+        const int i = i0 + lane;
+        const bool in = i < w1;
+        const uint32_t k = in ? ks[i] : 0u;
+        const unsigned gm = __ballot_sync(0xffffffffu, in && k > thr);
+        const unsigned em = __ballot_sync(0xffffffffu, in && k == thr);
+        const int g_lt = gt_before + __popc(gm & lt_mask);
+        const int e_lt = eq_before + __popc(em & lt_mask);
+        if ((gm >> lane) & 1u)
+            out[g_lt + min(e_lt, need_eq)] = S + c0 + i;
+        else if (((em >> lane) & 1u) && e_lt < need_eq)
+            out[g_lt + e_lt] = S + c0 + i;
+        gt_before += __popc(gm);
+        eq_before += __popc(em);
+    }
+    if (tid == 0 && rank == 0)
         p.sel_cnt[u] = K;
+    SEL_STAMP(9);
+    cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
+    SEL_STAMP(7);
 }
+
+template <typename Kern>
+int max_select_clusters(Kern kern, int cluster, size_t smem)
+{
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(cluster) * 64u);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    cfg.attrs = a;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+std::mutex g_sel_mu;
+int g_sel_fit[64][9];  // max active clusters + 1 (0 = not yet queried)
 
 }  // namespace
 
+int select_cluster_size(int max_cluster)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 1;
+    for (int C = 4; C >= 2; C >>= 1) {
+        if (C > max_cluster)
+            continue;
+        int n;
+        {
+            std::lock_guard<std::mutex> lock(g_sel_mu);
+            n = g_sel_fit[dev][C] - 1;
+        }
+        if (n < 0) {
+            n = max_select_clusters(select_cluster_kernel, C, select_cluster_smem_bytes());
+            std::lock_guard<std::mutex> lock(g_sel_mu);
+            g_sel_fit[dev][C] = n + 1;
+        }
+        if (n >= 1)
+            return C;
+    }
+    return 1;
+}
+
+int select_cluster_key_cap() { return kClusterKeyCap; }
+
+#ifdef SFI_TRACE
+cudaError_t trace_read_select(unsigned long long *host, int n)
+{
+    return cudaMemcpyFromSymbol(host, g_sel_trace, sizeof(unsigned long long) * 16 * (n < 1024 ? n : 1024));
+}
+#endif
+
 cudaError_t launch_select(const SelectParams &p, cudaStream_t stream)
 {
+    if (p.cluster > 1) {
+        const size_t smem = select_cluster_smem_bytes();
+        const cudaError_t a = cudaFuncSetAttribute(select_cluster_kernel,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem));
+        if (a != cudaSuccess)
+            return a;
+        const cudaError_t e = launch_pdl_cluster(select_cluster_kernel, dim3(p.n_units * p.cluster),
+                                                 dim3(NT), smem, p.cluster, stream, p);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
     const size_t smem = select_smem_bytes(p.staged != 0);
     {
         const cudaError_t a =

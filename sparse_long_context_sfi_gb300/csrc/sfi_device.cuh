@@ -382,6 +382,13 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t cluster_addr, float v)
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr)
 {
     float v;

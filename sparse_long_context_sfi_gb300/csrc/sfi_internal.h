@@ -60,6 +60,7 @@ struct SelectParams {
     int32_t *sel_idx;           // [units][n_select]
     int32_t *sel_cnt;           // [units]
     int staged;                 // candidates' evidence copied to shared memory (see kStageCap)
+    int cluster;                // > 1: CTAs per unit in one cluster (select_cluster_size)
     uint32_t *err;              // device error word
 };
 // The Selector stages a unit's evidence in shared memory when it has at most this many
@@ -102,6 +103,11 @@ cudaError_t launch_evidence(const float *zbuf, const float2 *stats, float *f,
                             int batch, int n_kv_heads, int group, int capacity, int max_len,
                             cudaStream_t stream);
 cudaError_t launch_select(const SelectParams &p, cudaStream_t stream);
+// Clustered Selector: the largest cluster size (4 or 2, at most max_cluster) that can be
+// launched on this device (1 when none can); and the most candidates one of its CTAs can
+// stage.
+int select_cluster_size(int max_cluster);
+int select_cluster_key_cap();
 cudaError_t launch_append(const void *k_new, const void *v_new, void *k, void *v,
                           int32_t *seq_len, const uint8_t *active, const int32_t *page_table,
                           int n_layers, int batch, int n_kv_heads, int capacity, int page_size,
@@ -116,6 +122,7 @@ cudaError_t launch_compact(const void *k, const void *v, void *kc, void *vc,
 size_t attention_smem_bytes();
 #ifdef SFI_TRACE
 cudaError_t trace_read(unsigned long long *host, int n);
+cudaError_t trace_read_select(unsigned long long *host, int n);
 #endif
 
 // Fast-step attention with its split-KV scratch in a library-owned device array instead of
