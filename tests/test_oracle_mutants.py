@@ -9,6 +9,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_pins as pins
+from tests import test_golden as golden
 from tests import test_oracle_refine_pins as refine_pins
 
 MUTANTS = {
@@ -41,7 +42,8 @@ MUTANTS = {
 }
 
 PIN_TESTS = [(pins, name) for name in dir(pins) if name.startswith("test_")] + \
-    [(refine_pins, name) for name in dir(refine_pins) if name.startswith("test_")]
+    [(refine_pins, name) for name in dir(refine_pins) if name.startswith("test_")] + \
+    [(golden, name) for name in dir(golden) if name.startswith("test_")]
 
 
 def run_pins():
