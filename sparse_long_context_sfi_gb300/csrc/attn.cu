@@ -161,7 +161,7 @@ __device__ __forceinline__ void store_out(const AttnParams &p, int u, int d, con
     }
 }
 
-template <int G, bool DENSE>
+template <int G, bool DENSE, bool CL>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
@@ -218,7 +218,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // Clustered fast step: one unit per cluster, its tiles split evenly over the cluster's
     // CTAs, which merge their partials through distributed shared memory. The cluster
     // barrier publishes the mbarrier initialisation and the TMEM base cluster-wide.
-    const bool clustered = !DENSE && p.cluster > 1;
+    // CL: the clustered fast step, compiled as its own instance (launched only with
+    // p.cluster > 1), so neither instance carries the other's code paths
+    constexpr bool clustered = !DENSE && CL;
     const bool fused = !DENSE && p.k_new != nullptr;
     if (clustered) {
         tc_fence_before();
@@ -338,6 +340,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // 64-column half of K or V for one page / block of rows), and lane 0 publishes the
         // tile with a single arrive.expect_tx of the warp's summed bytes.
         if (n_tiles > 0) {
+            if (lane == 0)
+                SFI_STAMP(22);
             const uint64_t pol = policy_evict_first();
             // decode the first tile of the range
             long long g = g0;
@@ -416,6 +420,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const int s = i % kStages;
                 if (lane == 0)
                     ok = mbar_wait(&c.empty[s], ((i / kStages) & 1) ^ 1, &c.abort);
+                if (lane == 0 && i == 0)
+                    SFI_STAMP(23);
                 const int u = (layer * B + b) * Hkv + kvh;
                 const bool first = (i == 0) || (t == 0);
                 const bool last = (i == n_tiles - 1) || (t == ntiles_of(b) - 1);
@@ -443,6 +449,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         appended = false;
                     }
                 }
+                if (lane == 0 && i == 0)
+                    SFI_STAMP(29);
                 if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
                     if (lane == 0)
                         fail(c, p.err);
@@ -552,6 +560,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                     appended = true;
                 }
+                if (lane == 0 && i == 0)
+                    SFI_STAMP(30);
                 // ---- publish the tile, then issue ---------------------------------------
                 uint32_t vw[4];
 #pragma unroll
@@ -570,6 +580,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     for (int w = 0; w < 4; ++w)
                         mt.valid[w] = vw[w];
                     mbar_arrive_expect_tx(bar, bytes);  // releases the metadata
+                    if (i == 0)
+                        SFI_STAMP(31);
                 }
                 __syncwarp();
                 if (first && lane < 2) {
@@ -1191,11 +1203,11 @@ cudaError_t launch_attn_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, cons
                           const CUtensorMap &tm_kc, const CUtensorMap &tm_vc, const AttnParams &p,
                           int grid, cudaStream_t stream)
 {
-    auto kern = attn_kernel<G, DENSE>;
+    const int cluster = (!DENSE && p.cluster > 1) ? p.cluster : 1;
+    auto kern = cluster > 1 ? attn_kernel<G, false, true> : attn_kernel<G, DENSE, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess)
         return e;
-    const int cluster = (!DENSE && p.cluster > 1) ? p.cluster : 1;
     if (grid % cluster != 0)
         return cudaErrorInvalidValue;
     e = launch_pdl_cluster(kern, dim3(grid), dim3(kAttnThreads), kSmemBytes, cluster, stream, tm_k,
@@ -1207,7 +1219,7 @@ cudaError_t launch_attn_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, cons
 template <int G>
 int max_active_clusters_t(int cluster)
 {
-    auto kern = attn_kernel<G, false>;
+    auto kern = attn_kernel<G, false, true>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
