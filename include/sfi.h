@@ -21,8 +21,10 @@
  *   - Kernels that find bad device-side data (a page-table entry out of range, an append
  *     past capacity, a bounded wait that gave up) set bits in the caller's device error
  *     word `err` and skip the bad access; they never trap. Read it with sfi_read_error.
- *   - The library keeps no state between calls except a per-device table of resolved
- *     driver entry points; calls sharing one workspace must not overlap on the GPU.
+ *   - The library keeps no state between calls except per-device tables (the resolved
+ *     driver entry point, cluster occupancy), the scratch of
+ *     sfi_sparse_decode_attn_static and the one-shot sfi_test_inject_stall flag; calls
+ *     sharing one workspace must not overlap on the GPU.
  *   - Shapes: head_dim must be 128; group = n_q_heads / n_kv_heads must be 1, 2, 4 or 8;
  *     batch <= 256. Query head h belongs to kv head h / group. A "unit" is one
  *     (layer, sequence, kv head), numbered u = (layer * batch + b) * n_kv_heads + kv_head.
@@ -332,6 +334,18 @@ sfi_status sfi_read_error(const sfi_kv_cache *kv, uint32_t *bits, void *stream);
 
 /* Clear the device error word (asynchronous). */
 sfi_status sfi_clear_error(const sfi_kv_cache *kv, void *stream);
+
+/*
+ * Test hook for the bounded waits (no counterpart in the paper). With on != 0, the next
+ * attention launch (sfi_dense_decode_attn, sfi_sparse_decode_attn, sfi_fast_decode_step or
+ * one inside sfi_decode_run) makes its first CTA expect 16 bytes more on its first tile's
+ * barrier than the copies deliver, so that barrier never completes: the waits on it give up
+ * after about a second, SFI_DEVERR_TIMEOUT is set in the error word, the kernel drains its
+ * copies and MMAs, frees its tensor memory and returns, and the context stays usable
+ * (re-initialise the workspace before further use, as after any timeout). One-shot; process
+ * wide. Not for production use.
+ */
+sfi_status sfi_test_inject_stall(int32_t on);
 
 #ifdef __cplusplus
 }

@@ -33,6 +33,7 @@ ENTRY_POINTS = (
     "sfi_sparse_decode_attn", "sfi_fast_decode_step", "sfi_sparse_decode_attn_static",
     "sfi_schedule",
     "sfi_schedule_tokens", "sfi_decode_run", "sfi_read_error", "sfi_clear_error",
+    "sfi_test_inject_stall",
 )
 
 
@@ -103,6 +104,7 @@ def lib():
             "sfi_decode_run": (C.c_int, [KV, BD, MEM, C.POINTER(SfiDecodePlan), P, SZ, P]),
             "sfi_read_error": (C.c_int, [KV, C.POINTER(C.c_uint32), P]),
             "sfi_clear_error": (C.c_int, [KV, P]),
+            "sfi_test_inject_stall": (C.c_int, [I32]),
         }
         for name, (res, args) in sig.items():
             f = getattr(l, name)
@@ -256,3 +258,9 @@ def sfi_read_error(kv: SfiKvCache, stream=None) -> int:
 
 def sfi_clear_error(kv: SfiKvCache, stream=None):
     _check("sfi_clear_error", lib().sfi_clear_error(C.byref(kv), _stream(stream)))
+
+
+def sfi_test_inject_stall(on: bool = True):
+    """Test hook: the next attention launch waits on a barrier that never completes, so its
+    bounded waits give up and report SFI_DEVERR_TIMEOUT."""
+    _check("sfi_test_inject_stall", lib().sfi_test_inject_stall(1 if on else 0))

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -148,6 +149,9 @@ cudaError_t record_event(cudaEvent_t e, cudaStream_t s)
 
 sfi_status launch_status(cudaError_t e) { return e == cudaSuccess ? SFI_OK : SFI_ERR_CUDA; }
 
+// One-shot test hook of sfi_test_inject_stall: consumed by the next attention launch.
+std::atomic<int> g_test_stall{0};
+
 void fill_common(AttnParams &p, const sfi_kv_cache *kv, const uint8_t *active)
 {
     std::memset(&p, 0, sizeof p);
@@ -197,6 +201,7 @@ sfi_status dense_impl(const sfi_kv_cache *kv, const void *q, void *out, int32_t 
     p.out = out;
     p.out_fp32 = out_fp32 ? 1 : 0;
     p.zbuf = scores_f ? reinterpret_cast<float *>(base + w.zbuf) : nullptr;
+    p.test_stall = g_test_stall.exchange(0);
     p.stats = reinterpret_cast<float2 *>(base + w.stats);
     p.partials = reinterpret_cast<float *>(base + w.part_dense);
     p.tickets = reinterpret_cast<int *>(base + w.tickets_dense);
@@ -267,6 +272,7 @@ sfi_status sparse_impl(const sfi_kv_cache *kv, const sfi_sparse_mem *mem,
     p.k_cache = kv->k;
     p.v_cache = kv->v;
     p.append_counter = reinterpret_cast<int *>(base + w.append_ctr);
+    p.test_stall = g_test_stall.exchange(0);
     p.comp_rows = mem->rows;
     p.sel_cnt = mem->sel_cnt;
     p.comp_cap = budget->n_sink + budget->n_select;
@@ -645,6 +651,12 @@ sfi_status sfi_schedule_tokens(int32_t steps, const int32_t *tokens, const int32
         if (s)
             last = t;
     }
+    return SFI_OK;
+}
+
+sfi_status sfi_test_inject_stall(int32_t on)
+{
+    g_test_stall.store(on ? 1 : 0);
     return SFI_OK;
 }
 

@@ -567,9 +567,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
                 for (int w = 0; w < 4; ++w)
                     vw[w] = __reduce_or_sync(0xffffffffu, valid[w]);
+                // test hook: CTA 0's first tile expects 16 bytes that never come, so the waits
+                // on it run out (see sfi_test_inject_stall)
                 const uint32_t bytes =
                     __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(rows) * 128u) +
-                    (first ? 2u * G * 128u : 0u);
+                    (first ? 2u * G * 128u : 0u) +
+                    ((p.test_stall && blockIdx.x == 0 && i == 0) ? 16u : 0u);
                 uint64_t *bar = &c.full[s];
                 if (lane == 0) {
                     TileMeta &mt = c.meta[s];

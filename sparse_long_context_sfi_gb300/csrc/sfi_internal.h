@@ -40,6 +40,7 @@ struct AttnParams {
     const void *k_new, *v_new;  // bf16 [units][128]
     void *k_cache, *v_cache;    // the cache the tensor maps view
     int *append_counter;        // CTAs that have read seq_len; zero between launches
+    int test_stall;             // test hook: CTA 0 waits on a barrier that never completes
     // outputs and workspace
     void *out;
     int out_fp32;
