@@ -283,6 +283,37 @@ def test_end_to_end_ragged_paged_full_size_sampled():
     compare_run(wl, 8, units=[0, 8 * 5 + 3, 8 * 17 + 1, 8 * 31 + 7])
 
 
+def test_end_to_end_longcot_full_size_sampled():
+    """The long-CoT workload at full size (32 layers, batch 8, 128K context, 137 GB of KV,
+    window 128, budget 1916, heavy hitters re-seeded at every boundary), issued in segments
+    with the key edits between them exactly as the benchmark does: sampled units over the
+    first decode steps."""
+    torch.cuda.empty_cache()
+    wl = HostWorkload(WORKLOADS["longcot_ctx128k_b8_l32"])
+    cfg = wl.cfg
+    steps = 6
+    st = sdev.make_state(wl)
+    ins = sdev.DeviceInputs(wl, steps, st.k.device)
+    slow = st.schedule(wl.masks[:, :steps])
+    out = torch.zeros((steps, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
+                      dtype=torch.float32, device=st.k.device)
+    sdev.DriftingRun(wl, st, slow, ins.q, ins.k_new, ins.v_new, out, ins.model).issue()
+    torch.cuda.synchronize()
+    assert int(st.err[0]) == 0
+    H, B = cfg.n_kv_heads, cfg.batch
+    units = [0, (17 * B + 3) * H + 5, (31 * B + 7) * H + 7]
+    ref = odecode.run(wl, steps=steps, units=units)
+    got = out.cpu().numpy()
+    G = cfg.group
+    for t in range(steps):
+        for i, u in enumerate(units):
+            layer, b, kvh = unit_coords(cfg, u)
+            ok, err = close(got[t, layer, b, kvh * G:(kvh + 1) * G], ref["out"][t][i])
+            assert ok, f"step {t} unit {u}: max err {err}"
+    del st, ins, out
+    torch.cuda.empty_cache()
+
+
 def test_end_to_end_drifting_heavy_hitters():
     """Long-CoT workload shape (window 128, budget 1916) scaled down, with heavy hitters
     re-seeded at every boundary: the run is issued in segments with the key edits between
