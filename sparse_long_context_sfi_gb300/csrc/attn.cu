@@ -136,6 +136,16 @@ __device__ __forceinline__ void mask_rows(uint32_t (&v)[4], int r0, int r1)
         v[w] |= word_bits(r0, r1, w);
 }
 
+// 2^x with the hardware approximation (PTX ex2.approx.ftz: relative error ~2^-22,
+// subnormal results flushed to zero; 2^-inf = 0). Used for the softmax weights, which are
+// rounded to bf16 for the O MMA anyway.
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // a[i] for a small register array without dynamic indexing (which would move the array to
 // local memory)
 template <int G>
@@ -997,8 +1007,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                        fmaxf(c.red_max[i & 1][2][h], c.red_max[i & 1][3][h]));
                 const float mn = fmaxf(m_run[h], tm);
                 const float mb = (mn == -INFINITY) ? 0.f : mn;
-                alpha[h] = exp2f(m_run[h] - mb);
-                const float pe = valid ? exp2f(z[h] - mb) : 0.f;
+                alpha[h] = ex2_approx(m_run[h] - mb);
+                const float pe = valid ? ex2_approx(z[h] - mb) : 0.f;
                 const __nv_bfloat16 pbf = __float2bfloat16_rn(pe);
                 le[h] = fmaf(le[h], alpha[h], pe);
                 lr[h] = fmaf(lr[h], alpha[h], __bfloat162float(pbf));
