@@ -255,7 +255,7 @@ def cpu_baseline(wl):
 
 
 def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=None,
-            dense_only_runs=0):
+            dense_only_runs=0, pipeline_runs=0):
     """Time whole decode runs of one workload (CUDA-graph replays), the per-kernel durations
     (event-instrumented replays), and optionally the dense-only / fast-only modes and the
     end-to-end run with host buffers."""
@@ -454,6 +454,14 @@ def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=N
         del g_dense
         res["dense_only"] = {"tokens_per_s": world * tokens_per_run * dense_only_runs / (ms_d / 1000.0),
                              "ms_per_run": ms_d / dense_only_runs}
+    if pipeline_runs:
+        # the layer-wise asynchronous pipeline: slow steps layer by layer, the Selector and
+        # compaction of each layer on a side stream beside the next layer's attention
+        g_pipe = capture(run_of(slow, pipeline=True))
+        ms_p = time_graph(g_pipe, pipeline_runs, 1)
+        del g_pipe
+        res["layer_pipeline"] = {"tokens_per_s": world * tokens_per_run * pipeline_runs / (ms_p / 1000.0),
+                                 "ms_per_run": ms_p / pipeline_runs}
     torch.cuda.synchronize()
     res["device_error"] = int(st.err[0])
     res["kv_bytes"] = int(st.k.numel() * 4)
@@ -498,14 +506,18 @@ def main():
         for name in [n for n in args.also.split(",") if n and n != args.workload]:
             w2 = HostWorkload(WORKLOADS[name])
             big = w2.cfg.n_layers * w2.cfg.batch * w2.cfg.ctx > 32 * 10 ** 6
+            multi = w2.cfg.n_layers > 1
             r2 = measure(w2, args, world, dev, stream, 2 if big else max(3, args.steps // 4),
-                         1 if big else 2, extras=False, dense_only_runs=1 if big else 2)
+                         1 if big else 2, extras=False, dense_only_runs=1 if big else 2,
+                         pipeline_runs=(1 if big else 2) if multi else 0)
             others[name] = {"tokens_per_s": r2["value"], "ms_per_run": r2["ms_per_run"],
                             "config": workload_config(w2, r2), "kernels": r2["kernels"],
                             "device_error": r2["device_error"]}
             if "dense_only" in r2:
                 others[name]["dense_only"] = r2["dense_only"]
                 others[name]["sfi_vs_dense_speedup"] = r2["value"] / r2["dense_only"]["tokens_per_s"]
+            if "layer_pipeline" in r2:
+                others[name]["layer_pipeline"] = r2["layer_pipeline"]
             torch.cuda.empty_cache()
 
     peak, peak_kind = measured_peaks()

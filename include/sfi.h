@@ -306,7 +306,23 @@ sfi_status sfi_schedule_tokens(int32_t steps, const int32_t *tokens, const int32
  *   events    optional host array of 2 * n_steps cudaEvent_t (as void*): events[2t] and
  *             events[2t+1] are recorded (external, so they survive graph capture) right
  *             before and after step t's attention kernel (the fused fast step's kernel on
- *             fast steps); NULL = none, and NULL entries are skipped
+ *             fast steps; the whole slow step, joins included, when side_stream is set);
+ *             NULL = none, and NULL entries are skipped
+ *   side_stream layer-wise asynchronous pipeline (technical summary section 3, layer-wise
+ *             overlap): NULL = off. When set, a slow step runs layer by layer: dense
+ *             attention and evidence of layer i on `stream`, then sfi_select and sfi_compact
+ *             of layer i on side_stream, so that they overlap the attention of layer i + 1;
+ *             `stream` waits for side_stream before the step's last operation returns, so
+ *             the next step sees the whole packed memory. A caller-owned stream of the same
+ *             device; ignored when dense_only is set.
+ *   fork_event, join_event  caller-owned cudaEvent_t (as void*, timing may be disabled),
+ *             required with side_stream: fork_event is re-recorded on `stream` after each
+ *             layer's evidence and waited for on side_stream; join_event is recorded on
+ *             side_stream after the last layer and waited for on `stream`. Both work under
+ *             stream capture (the usual fork/join of a captured graph). Missing events with
+ *             side_stream set: SFI_ERR_INVALID_ARG.
+ * Results with side_stream set equal those without up to the rounding of the dense step's
+ * split-KV partition (one launch per layer instead of one for all layers).
  */
 typedef struct sfi_decode_plan {
     int32_t n_steps;
@@ -322,6 +338,9 @@ typedef struct sfi_decode_plan {
     int32_t len_start;
     int32_t dense_only;
     void *const *events;
+    void *side_stream;
+    void *fork_event;
+    void *join_event;
 } sfi_decode_plan;
 
 sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,

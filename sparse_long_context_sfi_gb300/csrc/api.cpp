@@ -178,9 +178,13 @@ uint64_t cache_rows(const sfi_kv_cache *kv)
     return static_cast<uint64_t>(kv->n_layers) * kv->batch * kv->n_kv_heads * kv->capacity;
 }
 
+// ws_kv/unit0: the descriptor whose workspace layout `ws` follows and the first of its units
+// that kv covers (a one-layer view of a larger cache keeps the per-unit regions of the whole
+// cache, so the tickets and counters of every other launch stay where they are).
 sfi_status dense_impl(const sfi_kv_cache *kv, const void *q, void *out, int32_t out_fp32,
                       float *scores_f, const uint8_t *active, void *ws, size_t ws_bytes,
-                      void *stream, cudaEvent_t e0, cudaEvent_t e1)
+                      void *stream, cudaEvent_t e0, cudaEvent_t e1,
+                      const sfi_kv_cache *ws_kv = nullptr, long long unit0 = 0)
 {
     sfi_status st = check_kv(kv);
     if (st != SFI_OK)
@@ -190,7 +194,7 @@ sfi_status dense_impl(const sfi_kv_cache *kv, const void *q, void *out, int32_t 
     const int sms = sm_count();
     if (sms <= 0)
         return SFI_ERR_CUDA;
-    const WsLayout w = ws_layout(kv, sms);
+    const WsLayout w = ws_layout(ws_kv ? ws_kv : kv, sms);
     if (!ws || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u))
         return SFI_ERR_WORKSPACE;
     if (kv->max_len == 0)
@@ -198,14 +202,16 @@ sfi_status dense_impl(const sfi_kv_cache *kv, const void *q, void *out, int32_t 
     char *base = static_cast<char *>(ws);
     AttnParams p;
     fill_common(p, kv, active);
+    const int g = p.group;
     p.out = out;
     p.out_fp32 = out_fp32 ? 1 : 0;
-    p.zbuf = scores_f ? reinterpret_cast<float *>(base + w.zbuf) : nullptr;
+    p.zbuf = scores_f ? reinterpret_cast<float *>(base + w.zbuf) +
+                            unit0 * static_cast<long long>(kv->capacity) * g
+                      : nullptr;
     p.test_stall = g_test_stall.exchange(0);
-    p.stats = reinterpret_cast<float2 *>(base + w.stats);
+    p.stats = reinterpret_cast<float2 *>(base + w.stats) + unit0 * g;
     p.partials = reinterpret_cast<float *>(base + w.part_dense);
-    p.tickets = reinterpret_cast<int *>(base + w.tickets_dense);
-    const int g = p.group;
+    p.tickets = reinterpret_cast<int *>(base + w.tickets_dense) + unit0;
     const long long units = 1LL * kv->n_layers * kv->batch * kv->n_kv_heads;
     CUtensorMap tk, tv, tq;
     const uint32_t box = kv->page_size ? 16u : static_cast<uint32_t>(kTile);
@@ -309,6 +315,27 @@ sfi_status sparse_impl(const sfi_kv_cache *kv, const sfi_sparse_mem *mem,
     if (e1 && record_event(e1, as_stream(stream)) != cudaSuccess)
         return SFI_ERR_CUDA;
     return SFI_OK;
+}
+
+// A cache descriptor and packed memory restricted to layer l (base pointers offset by whole
+// layers; every per-unit array is laid out layer-major).
+void layer_views(const sfi_kv_cache *kv, const sfi_budget *budget, const sfi_sparse_mem *mem,
+                 int l, sfi_kv_cache *kl, sfi_sparse_mem *ml)
+{
+    const size_t units = static_cast<size_t>(kv->batch) * kv->n_kv_heads;
+    const size_t rows = kv->page_size ? static_cast<size_t>(kv->n_pages) * kv->n_kv_heads * 16
+                                      : units * kv->capacity;
+    const size_t comp = static_cast<size_t>(budget->n_sink + budget->n_select);
+    *kl = *kv;
+    kl->n_layers = 1;
+    kl->k = static_cast<char *>(kv->k) + l * rows * kHeadDim * 2;
+    kl->v = static_cast<char *>(kv->v) + l * rows * kHeadDim * 2;
+    *ml = *mem;
+    ml->kc = static_cast<char *>(mem->kc) + l * units * comp * kHeadDim * 2;
+    ml->vc = static_cast<char *>(mem->vc) + l * units * comp * kHeadDim * 2;
+    ml->sel_idx = mem->sel_idx + l * units * budget->n_select;
+    ml->sel_cnt = mem->sel_cnt + l * units;
+    ml->rows = mem->rows + l * units;
 }
 
 }  // namespace
@@ -567,6 +594,47 @@ sfi_status sfi_schedule(int32_t steps, const uint8_t *mask, int32_t t_max, uint8
     return SFI_OK;
 }
 
+// One slow step with the layer-wise asynchronous pipeline (technical summary section 3,
+// layer-wise overlap): attention and evidence of layer l on the main stream, then the
+// Selector and compaction of layer l on the side stream, forked after layer l's evidence so
+// that they run beside the attention of layer l + 1; joined back at the end of the step.
+static sfi_status slow_step_layers(const sfi_kv_cache *k, const sfi_budget *budget,
+                                   const sfi_sparse_mem *mem, const sfi_decode_plan *plan,
+                                   const void *q, void *out, const uint8_t *m_slow, void *ws,
+                                   size_t ws_bytes, void *stream, cudaEvent_t e0, cudaEvent_t e1)
+{
+    cudaStream_t main_s = as_stream(stream), side = as_stream(plan->side_stream);
+    cudaEvent_t fork = static_cast<cudaEvent_t>(plan->fork_event);
+    cudaEvent_t join = static_cast<cudaEvent_t>(plan->join_event);
+    const size_t units = static_cast<size_t>(k->batch) * k->n_kv_heads;
+    const size_t q_layer = static_cast<size_t>(k->batch) * k->n_q_heads * kHeadDim;
+    if (e0 && record_event(e0, main_s) != cudaSuccess)
+        return SFI_ERR_CUDA;
+    for (int l = 0; l < k->n_layers; ++l) {
+        sfi_kv_cache kl;
+        sfi_sparse_mem ml;
+        layer_views(k, budget, mem, l, &kl, &ml);
+        const void *ql = static_cast<const char *>(q) + l * q_layer * 2;
+        void *ol = static_cast<char *>(out) + l * q_layer * (plan->out_fp32 ? 4 : 2);
+        float *fl = plan->scores_f + l * units * k->capacity;
+        sfi_status st = dense_impl(&kl, ql, ol, plan->out_fp32, fl, m_slow, ws, ws_bytes, stream,
+                                   nullptr, nullptr, k, static_cast<long long>(l) * units);
+        if (st != SFI_OK)
+            return st;
+        if (cudaEventRecord(fork, main_s) != cudaSuccess ||
+            cudaStreamWaitEvent(side, fork, 0) != cudaSuccess)
+            return SFI_ERR_CUDA;
+        if ((st = sfi_select(&kl, fl, budget, &ml, m_slow, plan->side_stream)) != SFI_OK ||
+            (st = sfi_compact(&kl, budget, &ml, m_slow, plan->side_stream)) != SFI_OK)
+            return st;
+    }
+    if (cudaEventRecord(join, side) != cudaSuccess || cudaStreamWaitEvent(main_s, join, 0) != cudaSuccess)
+        return SFI_ERR_CUDA;
+    if (e1 && record_event(e1, main_s) != cudaSuccess)
+        return SFI_ERR_CUDA;
+    return SFI_OK;
+}
+
 sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
                           const sfi_sparse_mem *mem, const sfi_decode_plan *plan, void *ws,
                           size_t ws_bytes, void *stream)
@@ -581,6 +649,9 @@ sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
         return SFI_ERR_INVALID_ARG;
     if (plan->len_start + plan->n_steps > kv->capacity)
         return SFI_ERR_CAPACITY;
+    const bool pipe = plan->side_stream != nullptr && !plan->dense_only;
+    if (pipe && (!plan->fork_event || !plan->join_event))
+        return SFI_ERR_INVALID_ARG;
     const int B = kv->batch, g = kv->n_q_heads / kv->n_kv_heads;
     const size_t q_step = static_cast<size_t>(kv->n_layers) * B * kv->n_q_heads * kHeadDim;
     const size_t kv_step = static_cast<size_t>(kv->n_layers) * B * kv->n_kv_heads * kHeadDim;
@@ -617,7 +688,11 @@ sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
                 return st;
             continue;
         }
-        if (n_slow > 0) {
+        if (n_slow > 0 && pipe) {
+            if ((st = slow_step_layers(&k, budget, mem, plan, q, out, m_slow, ws, ws_bytes,
+                                       stream, e0, e1)) != SFI_OK)
+                return st;
+        } else if (n_slow > 0) {
             if ((st = dense_impl(&k, q, out, plan->out_fp32, plan->scores_f, m_slow, ws, ws_bytes,
                                  stream, e0, e1)) != SFI_OK ||
                 (st = sfi_select(&k, plan->scores_f, budget, mem, m_slow, stream)) != SFI_OK ||

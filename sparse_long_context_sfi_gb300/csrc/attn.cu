@@ -17,6 +17,11 @@
 //     N = 16 = query heads padded) and O^T = V^T P^T (M = 128 dims, V read MN-major),
 //     accumulating in TMEM. Warps 2-5 run the online softmax one position per thread
 //     (tcgen05.ld of S^T), write P^T as bf16 and accumulate O^T one dim per thread.
+//   * P carries about 16 significant bits at no extra MMA: head h's weight p goes to operand
+//     row h as bf16(p) and its remainder p - bf16(p) to the otherwise unused row G + h, so
+//     O^T columns h and G + h hold the two parts and their sum is taken at accumulation.
+//     (A bf16-only P errs by up to 2^-9 of a weight, which near-cancelling outputs of two
+//     competing heavy positions turn into absolute errors above 2e-3.)
 //   * Every wait is bounded; a wait that gives up flags SFI_DEVERR_TIMEOUT, drains the
 //     CTA's copies and MMAs, frees TMEM and returns.
 #include <math.h>
@@ -33,6 +38,7 @@ constexpr int kStageBytes = 4 * kChunkBytes;   // K[0:64), K[64:128), V[0:64), V
 constexpr int kOpRows = 16;                    // UMMA N: query heads padded to 16 rows
 constexpr int kOpChunk = kOpRows * 128;        // one 64-element K-chunk of Q^T or P^T
 constexpr int kOpBytes = 2 * kOpChunk;
+static_assert(2 * 8 <= kOpRows, "P^T needs 2 G operand rows (bf16 part and remainder)");
 constexpr uint32_t kTmemCols = 64;             // S^T x2 (cols 0, 16), O^T x2 (cols 32, 48)
 
 constexpr int kQOff = kStages * kStageBytes;
@@ -907,8 +913,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int bb = j & 1, use = j >> 1;
             if (!mbar_wait(&c.o_full[bb], use & 1, &c.abort))
                 return false;
-            float ov[G];
-            tmem_load<G>(t_lane + 32 + bb * 16, ov);
+            float ov2[2 * G], ov[G];
+            tmem_load<2 * G>(t_lane + 32 + bb * 16, ov2);
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+                ov[h] = ov2[h] + ov2[G + h];
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
@@ -1009,14 +1018,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const float mb = (mn == -INFINITY) ? 0.f : mn;
                 alpha[h] = ex2_approx(m_run[h] - mb);
                 const float pe = valid ? ex2_approx(z[h] - mb) : 0.f;
-                const __nv_bfloat16 pbf = __float2bfloat16_rn(pe);
+                const __nv_bfloat16 phi = __float2bfloat16_rn(pe);
+                const __nv_bfloat16 plo = __float2bfloat16_rn(pe - __bfloat162float(phi));
                 le[h] = fmaf(le[h], alpha[h], pe);
-                lr[h] = fmaf(lr[h], alpha[h], __bfloat162float(pbf));
+                lr[h] = fmaf(lr[h], alpha[h], __bfloat162float(phi) + __bfloat162float(plo));
                 m_run[h] = mn;
-                // P^T[h][row], K-major, 128-byte swizzle
-                const int off = (row >> 6) * kOpChunk + h * 128 +
-                                ((((row & 63) >> 3) ^ h) << 4) + (row & 7) * 2;
-                *reinterpret_cast<__nv_bfloat16 *>(pb + off) = pbf;
+                // P^T[h][row] and P^T[G + h][row], K-major, 128-byte swizzle
+                const int base = (row >> 6) * kOpChunk + (row & 7) * 2;
+                const int sw = (row & 63) >> 3;
+                *reinterpret_cast<__nv_bfloat16 *>(pb + base + h * 128 + ((sw ^ h) << 4)) = phi;
+                *reinterpret_cast<__nv_bfloat16 *>(pb + base + (G + h) * 128 +
+                                                   ((sw ^ ((G + h) & 7)) << 4)) = plo;
             }
             if (!valid) {
                 // keep P = 0 rows from meeting stale (possibly non-finite) V data

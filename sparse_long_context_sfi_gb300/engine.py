@@ -116,12 +116,27 @@ class SfiState:
         return mixed and (a_slow, a_fast)
 
     # -- a whole run through the native driver --------------------------------------------------
+    def side_stream(self, priority=0):
+        """The layer-wise pipeline's side stream and its fork and join events (created once;
+        the events are recorded once here so that their driver objects exist before any
+        stream capture)."""
+        if getattr(self, "_side", None) is None:
+            side = torch.cuda.Stream(device=self.device, priority=priority)
+            fork, join = torch.cuda.Event(), torch.cuda.Event()
+            fork.record()
+            join.record()
+            torch.cuda.synchronize(self.device)
+            self._side = (side, fork, join)
+        return self._side
+
     def make_plan(self, slow: np.ndarray, q, k_new, v_new, out, out_fp32=True, out_per_step=True,
-                  dense_only=False, events=None, t0=0, t1=None):
+                  dense_only=False, events=None, t0=0, t1=None, pipeline=False):
         """slow: uint8 [steps][B]; q/k_new/v_new/out: device tensors with a leading step axis.
         events: optional list of 2 * (t1 - t0) torch.cuda.Event(enable_timing=True) or None,
-        recorded before (2 t) and after (2 t + 1) step t's attention kernel (None: not recorded). [t0, t1): the steps this plan covers (a run can
-        be issued as several consecutive plans)."""
+        recorded before (2 t) and after (2 t + 1) step t's attention kernel (None: not
+        recorded). [t0, t1): the steps this plan covers (a run can be issued as several
+        consecutive plans). pipeline: run slow steps layer by layer, with the Selector and
+        compaction of each layer on a side stream beside the next layer's attention."""
         t1 = slow.shape[0] if t1 is None else t1
         q, k_new, v_new = q[t0:t1], k_new[t0:t1], v_new[t0:t1]
         if out_per_step:
@@ -139,6 +154,10 @@ class SfiState:
             out_per_step=1 if out_per_step else 0, scores_f=self.scores.data_ptr(),
             masks=None if masks is None else masks.data_ptr(),
             len_start=int(self.len0.max()) + t0, dense_only=1 if dense_only else 0)
+        if pipeline:
+            side, fork, join = self.side_stream()
+            plan.side_stream, plan.fork_event, plan.join_event = (side.cuda_stream, fork.cuda_event,
+                                                                  join.cuda_event)
         ev_arr = None
         if events is not None:
             assert len(events) == 2 * steps

@@ -85,7 +85,27 @@ def test_decode_plan_layout_matches_header(lib):
     assert C.sizeof(sfi.SfiBudget) == 4 * 4 + 8 + 5 * 4 + 4  # padded to 8
     assert C.sizeof(sfi.SfiSparseMem) == 5 * 8
     assert sfi.SfiDecodePlan.masks.offset == 64 and sfi.SfiDecodePlan.events.offset == 80
-    assert C.sizeof(sfi.SfiDecodePlan) == 88
+    assert sfi.SfiDecodePlan.side_stream.offset == 88 and sfi.SfiDecodePlan.join_event.offset == 104
+    assert C.sizeof(sfi.SfiDecodePlan) == 112
+
+
+def test_layer_pipeline_needs_both_events(lib):
+    """A decode run with a side stream but without its fork and join events is refused
+    before any CUDA call."""
+    dummy = 1 << 20  # never dereferenced: the checks fail first
+    kv = sfi.SfiKvCache(n_layers=2, batch=1, n_q_heads=8, n_kv_heads=2, head_dim=128, capacity=64,
+                        max_len=8, k=dummy, v=dummy, seq_len=dummy, err=dummy)
+    bud = sfi.SfiBudget(n_sink=4, n_window=16, n_select=8, prior_tau=16, lambda_=0.1)
+    mem = sfi.SfiSparseMem(kc=dummy, vc=dummy, sel_idx=dummy, sel_cnt=dummy, rows=dummy)
+    slow = np.ones(4, np.uint8)
+    plan = sfi.SfiDecodePlan(n_steps=4, slow=slow.ctypes.data, q=dummy, k_new=dummy, v_new=dummy,
+                             out=dummy, out_fp32=1, out_per_step=1, scores_f=dummy, len_start=8,
+                             side_stream=dummy, fork_event=dummy)
+    assert lib.sfi_decode_run(C.byref(kv), C.byref(bud), C.byref(mem), C.byref(plan), dummy,
+                              1 << 30, None) == sfi.SFI_ERR_INVALID_ARG
+    plan.fork_event, plan.join_event = None, dummy
+    assert lib.sfi_decode_run(C.byref(kv), C.byref(bud), C.byref(mem), C.byref(plan), dummy,
+                              1 << 30, None) == sfi.SFI_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("t_max", [0, 7, 64])

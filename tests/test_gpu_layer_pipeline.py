@@ -1,0 +1,186 @@
+"""Layer-wise asynchronous pipeline of the decode run (technical summary, section 3: the
+Selector and the cache reorganisation of layer i run asynchronously beside the attention of
+layer i + 1). With a side stream in the plan, each slow step is issued layer by layer: dense
+attention and evidence on the main stream, the Selector and compaction on the side stream.
+
+Parity: one launch per layer rounds the split-KV merge differently from one launch over all
+layers, so a Selector near-tie may flip on either side. The tests therefore compare (a) every
+checked output with the oracle run on the GPU's own selections (|gpu - oracle| <= 2e-3 +
+1e-2 |oracle|), and (b) the GPU's selections with the oracle's own, overlapping >= 99.5 %.
+A graph replay of the pipelined run must equal its eager run bit for bit (the same kernels in
+the same partitions; every merge order is fixed).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import decode as odecode
+from synth import device as sdev
+from synth.configs import WORKLOADS
+from synth.workload import HostWorkload
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 2e-3, 1e-2
+
+
+def close(g, o):
+    g = np.asarray(g, np.float64)
+    o = np.asarray(o, np.float64)
+    bad = np.abs(g - o) > ATOL + RTOL * np.abs(o)
+    return not bad.any(), float(np.abs(g - o).max())
+
+
+def small(name, **kw):
+    return HostWorkload(WORKLOADS[name].scaled(**kw))
+
+
+def unit_coords(cfg, u):
+    return u // (cfg.n_kv_heads * cfg.batch), (u // cfg.n_kv_heads) % cfg.batch, u % cfg.n_kv_heads
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+
+
+def issue(wl, steps, pipeline, graph=False):
+    """Run `steps` decode steps of the workload through the native driver as one run; with
+    graph=True the run is captured once after an eager run and replayed, and both outputs
+    are returned."""
+    cfg = wl.cfg
+    st = sdev.make_state(wl)
+    ins = sdev.DeviceInputs(wl, steps, st.k.device)
+    slow = st.schedule(wl.masks[:, :steps])
+    out = torch.zeros((steps, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
+                      dtype=torch.float32, device=st.k.device)
+    run = sdev.DriftingRun(wl, st, slow, ins.q, ins.k_new, ins.v_new, out, ins.model,
+                           pipeline=pipeline)
+    stream = torch.cuda.Stream()
+    len0 = st.seq_len.clone()
+    with torch.cuda.stream(stream):
+        run.issue(stream)
+    stream.synchronize()
+    assert int(st.err[0]) == 0
+    eager = out.cpu().numpy()
+    if not graph:
+        return st, slow, eager
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+        st.seq_len.copy_(len0)
+        run.issue(stream)
+    out.zero_()
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    assert int(st.err[0]) == 0
+    return st, slow, eager, out.cpu().numpy()
+
+
+def issue_stepwise(wl, steps, units):
+    """The pipelined run issued one step per plan (each slow step still forks and joins its
+    side stream), reading back the GPU's selection for `units` after every slow step."""
+    cfg = wl.cfg
+    st = sdev.make_state(wl)
+    ins = sdev.DeviceInputs(wl, steps, st.k.device)
+    slow = st.schedule(wl.masks[:, :steps])
+    out = torch.zeros((steps, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
+                      dtype=torch.float32, device=st.k.device)
+    run = sdev.DriftingRun(wl, st, slow, ins.q, ins.k_new, ins.v_new, out, ins.model,
+                           pipeline=True)
+    plans = [st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, t0=t, t1=t + 1, pipeline=True)
+             for t in range(steps)]
+    stream = torch.cuda.Stream()
+    s = stream.cuda_stream
+    if 0 in run.edits:
+        sdev.gpu.apply_drift(wl, st.k, run.edits[0], ins.model, s)
+    gpu_sel = {}
+    for t in range(steps):
+        if t > 0 and run.ep[t] != run.ep[t - 1] and int(run.ep[t]) in run.edits:
+            sdev.gpu.apply_drift(wl, st.k, run.edits[int(run.ep[t])], ins.model, s)
+        st.run(plans[t], stream=stream)
+        if slow[t].any():
+            stream.synchronize()
+            idx, cnt = st.sel_idx.cpu().numpy(), st.sel_cnt.cpu().numpy()
+            for u in units:
+                if slow[t][unit_coords(cfg, u)[1]]:
+                    gpu_sel[(t, u)] = idx[u, :cnt[u]].copy()
+    stream.synchronize()
+    assert int(st.err[0]) == 0
+    return st, slow, out.cpu().numpy(), gpu_sel
+
+
+def check_pipelined(wl, steps, units=None, check_steps=None):
+    cfg = wl.cfg
+    all_units = list(range(cfg.n_layers * cfg.batch * cfg.n_kv_heads))
+    units = all_units if units is None else units
+    st, slow, got, gpu_sel = issue_stepwise(wl, steps, units)
+    del st
+    torch.cuda.empty_cache()
+    own = odecode.run(wl, steps=steps, units=units)
+    assert np.array_equal(own["slow"].T, slow)
+    # (b) the selections, each side on its own evidence
+    inter = total = 0
+    for key, g in gpu_sel.items():
+        o = own["sel"][key]
+        assert len(g) == len(o), f"{key}: {len(g)} selected against {len(o)}"
+        assert np.all(np.diff(g) > 0)
+        inter += len(np.intersect1d(g, o))
+        total += len(o)
+    assert total > 0 and inter >= 0.995 * total, f"selection overlap {inter / total:.5f}"
+    # (a) the attention, given the GPU's selections
+    ref = odecode.run(wl, steps=steps, units=units, gpu_selection=gpu_sel)
+    G = cfg.group
+    for t in (range(steps) if check_steps is None else check_steps):
+        for i, u in enumerate(units):
+            layer, b, kvh = unit_coords(cfg, u)
+            ok, err = close(got[t, layer, b, kvh * G:(kvh + 1) * G], ref["out"][t][i])
+            assert ok, f"step {t} unit {u}: max err {err}"
+    return gpu_sel, slow
+
+
+def test_pipelined_four_layers_vs_oracle():
+    """128K-workload shape scaled to 3000 positions and 4 layers: every step, every unit."""
+    wl = small("llama8b_ctx128k_l32", ctx=3000, ctx_lo=3000, n_layers=4, steps=40, mask_param=6)
+    sel, _ = check_pipelined(wl, 40)
+    assert len({t for t, _ in sel}) > 3
+
+
+def test_pipelined_ragged_paged_mixed_steps_vs_oracle():
+    """Paged cache with 3 layers (per-layer page pools), per-sequence schedules (steps that
+    mix slow and fast sequences)."""
+    wl = small("ragged_paged_b32", batch=6, ctx=2400, ctx_lo=600, steps=40, mask_param=6,
+               n_layers=3)
+    _, slow = check_pipelined(wl, 40, check_steps=range(0, 40, 3))
+    assert any(r.any() and not r.all() for r in slow)
+
+
+def test_pipelined_drifting_heavy_hitters_vs_oracle():
+    """Long-CoT shape scaled down (window 128, budget 1916, keys re-seeded at every boundary,
+    key edits between the steps): every step, every unit."""
+    wl = small("longcot_ctx128k_b8_l32", ctx=3000, ctx_lo=3000, batch=2, n_layers=2, steps=40,
+               mask_param=6)
+    check_pipelined(wl, 40)
+
+
+def test_pipelined_graph_replay_equals_eager():
+    """Captured in a CUDA graph (fork and join across the two streams) and replayed: the same
+    outputs bit for bit as the eager pipelined run. Step 0 (a dense step for every sequence)
+    equals the single-stream run's up to the split-KV rounding."""
+    wl = small("llama8b_ctx128k_l32", ctx=2500, ctx_lo=2500, n_layers=3, steps=24, mask_param=5)
+    st, _, eager, replay = issue(wl, 24, pipeline=True, graph=True)
+    assert np.array_equal(eager, replay)
+    del st
+    _, _, single = issue(wl, 24, pipeline=False)
+    ok, err = close(eager[0], single[0])
+    assert ok, f"pipelined vs single-stream dense step max err {err}"
+
+
+def test_pipelined_128k_32_layers_full_size_sampled():
+    """The 128K-context, 32-layer workload at full size (17 GB of KV): sampled units of the
+    first, a middle and the last layer over the first decode steps."""
+    torch.cuda.empty_cache()
+    wl = HostWorkload(WORKLOADS["llama8b_ctx128k_l32"])
+    check_pipelined(wl, 4, units=[0, 8 * 17 + 5, 8 * 31 + 7])

@@ -140,6 +140,49 @@ def test_dense_bf16_output():
     np.testing.assert_allclose(o16, o32, rtol=2 ** -8, atol=1e-6)
 
 
+def test_competing_heavy_positions_with_cancelling_values():
+    """Two heavy positions (softmax weights about 0.59 and 0.29 against 599 flat ones) whose
+    V rows cancel (+3 and -6 in every dimension): o = 0.0245, tolerance 2.25e-3. Rounding the
+    weights to bf16 alone would err by 3.1e-3 here (the weight 0.4931 rounds to 0.4922); the
+    kernels carry each weight as bf16 part + bf16 remainder, leaving about 1e-8. Checked on
+    the dense slow step and on the fast step after it, which selects both positions."""
+    wl = small("gqa4_ctx4k_hh", ctx=600, ctx_lo=600, steps=2)
+    cfg = wl.cfg
+    G, D = cfg.group, cfg.head_dim
+    st = sdev.make_state(wl, on_device=True)
+    ins = sdev.DeviceInputs(wl, 2, st.k.device, on_device=True)
+    a, b = 100, 300
+    st.k.zero_()
+    st.v.zero_()
+    st.k[0, 0, 0, a] = 0.70703125
+    st.k[0, 0, 0, b] = 0.64453125
+    st.v[0, 0, 0, a] = 3.0
+    st.v[0, 0, 0, b] = -6.0
+    ins.q.zero_()
+    ins.q[:, 0, 0, :G] = 1.0
+    ins.k_new.zero_()
+    ins.v_new.zero_()
+    out = torch.zeros((2, cfg.n_layers, cfg.batch, cfg.n_q_heads, D), dtype=torch.float32,
+                      device=st.k.device)
+    for t in range(2):
+        st.step(ins.q[t], ins.k_new[t], ins.v_new[t], np.full(cfg.batch, t == 0), out[t])
+    torch.cuda.synchronize()
+    assert int(st.err[0]) == 0
+    sel = st.sel_idx[0, :int(st.sel_cnt[0])].cpu().numpy()
+    assert a in sel and b in sel
+    bits = lambda x: x.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    L0 = int(wl.len0[0])
+    k, v = bits(st.k[0, 0, 0, :L0 + 2]), bits(st.v[0, 0, 0, :L0 + 2])
+    q = bits(ins.q[0, 0, 0, :G])
+    got = out.cpu().numpy()
+    for t, rows in ((0, np.arange(L0 + 1)),
+                    (1, oracle.sparse_rows(L0 + 1, L0 + 2, cfg.n_sink, cfg.n_window, sel))):
+        o, _ = oracle.attend(q, k, v, rows)
+        assert abs(o[0, 0]) > 0.01
+        ok, err = close(got[t, 0, 0, :G], o)
+        assert ok and err < 2e-4, f"step {t}: max err {err}"
+
+
 # ------------------------------------------------------------------------------ fast step
 
 @pytest.mark.parametrize("fused", [True, False], ids=["fused_append", "append_then_sparse"])
