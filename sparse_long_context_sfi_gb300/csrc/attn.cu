@@ -77,7 +77,7 @@ struct Ctrl {
     uint64_t app_ready;         // clustered, fused append: the new row is in the cache
     TileMeta meta[kStages];
     float red_max[2][4][8];
-    float red_sum[4][16];
+    float red_sum[4][8];
     uint32_t tmem_base;
     int abort;
     int last_flag;
@@ -756,7 +756,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int gw = warp - 2;              // index within the softmax group
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         uint32_t gphase = 0;
-        float m_run[G], le[G], lr[G], acc[G];
+        float m_run[G], le[G], acc[G];
         // the tile waiting for its O^T accumulation
         float a_alpha[G], a_m[G], a_le[G], a_lr[G];
         // clustered: this CTA's (max, sum) of its slice, with acc[] its unnormalised output
@@ -766,7 +766,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             m_run[h] = -INFINITY;
-            le[h] = lr[h] = acc[h] = 0.f;
+            le[h] = acc[h] = 0.f;
             fin_m[h] = -INFINITY;
             fin_lr[h] = 0.f;
         }
@@ -966,7 +966,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
                     m_run[h] = -INFINITY;
-                    le[h] = lr[h] = 0.f;
+                    le[h] = 0.f;
                 }
             }
             float sv[G];
@@ -1020,8 +1020,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const float pe = valid ? ex2_approx(z[h] - mb) : 0.f;
                 const __nv_bfloat16 phi = __float2bfloat16_rn(pe);
                 const __nv_bfloat16 plo = __float2bfloat16_rn(pe - __bfloat162float(phi));
+                // phi + plo equals pe to about 2^-17, so the fp32 sum also normalises the O^T
+                // the MMAs accumulate from the two parts
                 le[h] = fmaf(le[h], alpha[h], pe);
-                lr[h] = fmaf(lr[h], alpha[h], __bfloat162float(phi) + __bfloat162float(plo));
                 m_run[h] = mn;
                 // P^T[h][row] and P^T[G + h][row], K-major, 128-byte swizzle
                 const int base = (row >> 6) * kOpChunk + (row & 7) * 2;
@@ -1051,11 +1052,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (flags & kFlagLast) {
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    const float s1 = warp_sum(le[h]), s2 = warp_sum(lr[h]);
-                    if (lane == 0) {
+                    const float s1 = warp_sum(le[h]);
+                    if (lane == 0)
                         c.red_sum[gw][h] = s1;
-                        c.red_sum[gw][8 + h] = s2;
-                    }
                 }
                 if (!group_sync(c, gphase, lane)) {
                     ok = false;
@@ -1065,8 +1064,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int h = 0; h < G; ++h) {
                     fm[h] = m_run[h];
                     fle[h] = c.red_sum[0][h] + c.red_sum[1][h] + c.red_sum[2][h] + c.red_sum[3][h];
-                    flr[h] = c.red_sum[0][8 + h] + c.red_sum[1][8 + h] + c.red_sum[2][8 + h] +
-                             c.red_sum[3][8 + h];
+                    flr[h] = fle[h];
                 }
             }
             if (i > 0 && !correct(i - 1)) {
