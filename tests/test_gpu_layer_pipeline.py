@@ -79,9 +79,10 @@ def issue(wl, steps, pipeline, graph=False):
     return st, slow, eager, out.cpu().numpy()
 
 
-def issue_stepwise(wl, steps, units):
-    """The pipelined run issued one step per plan (each slow step still forks and joins its
-    side stream), reading back the GPU's selection for `units` after every slow step."""
+def issue_stepwise(wl, steps, units, pipeline=True):
+    """The run issued one step per plan (with the pipeline, each slow step still forks and
+    joins its side stream), reading back the GPU's selection for `units` after every slow
+    step."""
     cfg = wl.cfg
     st = sdev.make_state(wl)
     ins = sdev.DeviceInputs(wl, steps, st.k.device)
@@ -89,9 +90,9 @@ def issue_stepwise(wl, steps, units):
     out = torch.zeros((steps, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
                       dtype=torch.float32, device=st.k.device)
     run = sdev.DriftingRun(wl, st, slow, ins.q, ins.k_new, ins.v_new, out, ins.model,
-                           pipeline=True)
-    plans = [st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, t0=t, t1=t + 1, pipeline=True)
-             for t in range(steps)]
+                           pipeline=pipeline)
+    plans = [st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, t0=t, t1=t + 1,
+                          pipeline=pipeline) for t in range(steps)]
     stream = torch.cuda.Stream()
     s = stream.cuda_stream
     if 0 in run.edits:
@@ -112,11 +113,11 @@ def issue_stepwise(wl, steps, units):
     return st, slow, out.cpu().numpy(), gpu_sel
 
 
-def check_pipelined(wl, steps, units=None, check_steps=None):
+def check_run(wl, steps, units=None, check_steps=None, pipeline=True):
     cfg = wl.cfg
     all_units = list(range(cfg.n_layers * cfg.batch * cfg.n_kv_heads))
     units = all_units if units is None else units
-    st, slow, got, gpu_sel = issue_stepwise(wl, steps, units)
+    st, slow, got, gpu_sel = issue_stepwise(wl, steps, units, pipeline)
     del st
     torch.cuda.empty_cache()
     own = odecode.run(wl, steps=steps, units=units)
@@ -144,16 +145,17 @@ def check_pipelined(wl, steps, units=None, check_steps=None):
 def test_pipelined_four_layers_vs_oracle():
     """128K-workload shape scaled to 3000 positions and 4 layers: every step, every unit."""
     wl = small("llama8b_ctx128k_l32", ctx=3000, ctx_lo=3000, n_layers=4, steps=40, mask_param=6)
-    sel, _ = check_pipelined(wl, 40)
+    sel, _ = check_run(wl, 40)
     assert len({t for t, _ in sel}) > 3
 
 
-def test_pipelined_ragged_paged_mixed_steps_vs_oracle():
-    """Paged cache with 3 layers (per-layer page pools), per-sequence schedules (steps that
-    mix slow and fast sequences)."""
+@pytest.mark.parametrize("pipeline", [True, False], ids=["pipelined", "single_stream"])
+def test_ragged_paged_multi_layer_mixed_steps_vs_oracle(pipeline):
+    """Paged cache with 3 layers (per-layer page pools sharing one page table), per-sequence
+    schedules (steps that mix slow and fast sequences); pipelined and on one stream."""
     wl = small("ragged_paged_b32", batch=6, ctx=2400, ctx_lo=600, steps=40, mask_param=6,
                n_layers=3)
-    _, slow = check_pipelined(wl, 40, check_steps=range(0, 40, 3))
+    _, slow = check_run(wl, 40, check_steps=range(0, 40, 3), pipeline=pipeline)
     assert any(r.any() and not r.all() for r in slow)
 
 
@@ -162,7 +164,7 @@ def test_pipelined_drifting_heavy_hitters_vs_oracle():
     key edits between the steps): every step, every unit."""
     wl = small("longcot_ctx128k_b8_l32", ctx=3000, ctx_lo=3000, batch=2, n_layers=2, steps=40,
                mask_param=6)
-    check_pipelined(wl, 40)
+    check_run(wl, 40)
 
 
 def test_pipelined_graph_replay_equals_eager():
@@ -183,4 +185,4 @@ def test_pipelined_128k_32_layers_full_size_sampled():
     first, a middle and the last layer over the first decode steps."""
     torch.cuda.empty_cache()
     wl = HostWorkload(WORKLOADS["llama8b_ctx128k_l32"])
-    check_pipelined(wl, 4, units=[0, 8 * 17 + 5, 8 * 31 + 7])
+    check_run(wl, 4, units=[0, 8 * 17 + 5, 8 * 31 + 7])
