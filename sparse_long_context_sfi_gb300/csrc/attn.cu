@@ -725,10 +725,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     idle = 0;
                     continue;
                 }
-                // nothing ready: yield the issue slot briefly; give up after kWaitTimeoutNs
-                // without progress, or as soon as another role has given up
-                if (idle > 8u)
-                    __nanosleep(20);
+                // nothing ready: poll again (the softmax warps leave most issue slots free);
+                // give up after kWaitTimeoutNs without progress, or as soon as another role
+                // has given up
                 if ((++idle & 63u) == 0u) {
                     if (c.abort) {
                         ok = false;
