@@ -610,29 +610,35 @@ static sfi_status slow_step_layers(const sfi_kv_cache *k, const sfi_budget *budg
     const size_t q_layer = static_cast<size_t>(k->batch) * k->n_q_heads * kHeadDim;
     if (e0 && record_event(e0, main_s) != cudaSuccess)
         return SFI_ERR_CUDA;
-    for (int l = 0; l < k->n_layers; ++l) {
+    sfi_status st = SFI_OK;
+    bool forked = false;
+    for (int l = 0; l < k->n_layers && st == SFI_OK; ++l) {
         sfi_kv_cache kl;
         sfi_sparse_mem ml;
         layer_views(k, budget, mem, l, &kl, &ml);
         const void *ql = static_cast<const char *>(q) + l * q_layer * 2;
         void *ol = static_cast<char *>(out) + l * q_layer * (plan->out_fp32 ? 4 : 2);
         float *fl = plan->scores_f + l * units * k->capacity;
-        sfi_status st = dense_impl(&kl, ql, ol, plan->out_fp32, fl, m_slow, ws, ws_bytes, stream,
-                                   nullptr, nullptr, k, static_cast<long long>(l) * units);
+        st = dense_impl(&kl, ql, ol, plan->out_fp32, fl, m_slow, ws, ws_bytes, stream, nullptr,
+                        nullptr, k, static_cast<long long>(l) * units);
         if (st != SFI_OK)
-            return st;
+            break;
         if (cudaEventRecord(fork, main_s) != cudaSuccess ||
-            cudaStreamWaitEvent(side, fork, 0) != cudaSuccess)
-            return SFI_ERR_CUDA;
-        if ((st = sfi_select(&kl, fl, budget, &ml, m_slow, plan->side_stream)) != SFI_OK ||
-            (st = sfi_compact(&kl, budget, &ml, m_slow, plan->side_stream)) != SFI_OK)
-            return st;
+            cudaStreamWaitEvent(side, fork, 0) != cudaSuccess) {
+            st = SFI_ERR_CUDA;
+            break;
+        }
+        forked = true;
+        if ((st = sfi_select(&kl, fl, budget, &ml, m_slow, plan->side_stream)) == SFI_OK)
+            st = sfi_compact(&kl, budget, &ml, m_slow, plan->side_stream);
     }
-    if (cudaEventRecord(join, side) != cudaSuccess || cudaStreamWaitEvent(main_s, join, 0) != cudaSuccess)
-        return SFI_ERR_CUDA;
-    if (e1 && record_event(e1, main_s) != cudaSuccess)
-        return SFI_ERR_CUDA;
-    return SFI_OK;
+    // joined on every path once forked, so a stream capture around the call stays joinable
+    if (forked && (cudaEventRecord(join, side) != cudaSuccess ||
+                   cudaStreamWaitEvent(main_s, join, 0) != cudaSuccess) && st == SFI_OK)
+        st = SFI_ERR_CUDA;
+    if (st == SFI_OK && e1 && record_event(e1, main_s) != cudaSuccess)
+        st = SFI_ERR_CUDA;
+    return st;
 }
 
 sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
