@@ -14,6 +14,8 @@ constexpr int kMaxBatch = 256;
 constexpr int kAttnThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2-5 softmax/epilogue
 constexpr int kSelectThreads = 1024;
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // bounded pipeline waits: 1 s
+// split-KV partial: G x 128 unnormalised outputs, then per head the max, the weight sum and
+// the normaliser
 constexpr int kPartialFloats(int G) { return G * kHeadDim + 3 * G; }
 
 // Everything the attention kernels read besides the tensor maps.
