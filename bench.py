@@ -29,6 +29,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "SFI decode-attn tokens/s (slow/fast mix) at 32K/128K; % of HBM roofline"
+DATA = "synthetic (seeded counter-based generator, Zipf(1.1) key-norm boost)"
+NOMINAL_HBM_GBS = 7900.0     # GB300 HBM3e, nominal
 BYTES_PER_ROW = 512          # one K row + one V row of 128 bf16
 LOGIT_BYTES = 16             # the slow step's fp32 logits (4 heads) written per position
 
@@ -43,7 +45,8 @@ def parse():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the dense-only/fast-only modes, the CPU baseline and the other "
                          "workloads")
-    ap.add_argument("--also", default="llama8b_ctx128k_l32,ragged_paged_b32,longcot_ctx128k_b8_l32",
+    ap.add_argument("--also", default="llama8b_ctx128k_l32,ragged_paged_b32,longcot_ctx128k_b8_l32,"
+                                      "llama8b_ctx32k_b4_tok",
                     help="comma-separated workloads measured after the headline one")
     return ap.parse_args()
 
@@ -193,43 +196,59 @@ def bytes_model(wl, slow, sel_rows):
 
 # ------------------------------------------------------------------------- reference arm
 
+def oracle_cycle(wl):
+    """A bounded sample of the workload for the CPU oracle: one SFI cycle of every unit -- a
+    slow decode step, then the fast steps that reuse its selection, as many as the run's own
+    schedule has per slow step on average (15 on the 32K batch-4 workload: 16 slow of 256).
+    Returns (prepared rows, forced step types [B][steps], steps)."""
+    from oracle import decode as odecode
+    cfg = wl.cfg
+    frac = float(odecode.schedule(wl).mean())
+    steps = 1 + max(0, int(round(1.0 / frac)) - 1)
+    forced = np.zeros((cfg.batch, steps), np.uint8)
+    forced[:, 0] = 1
+    return odecode.prepare(wl, steps), forced, steps
+
+
+def time_oracle_cycles(wl, n_min: int, seconds_min: float = 0.0):
+    """Run the oracle cycle at least n_min times and until seconds_min have passed; returns
+    the per-cycle seconds and the tokens of one cycle."""
+    from oracle import decode as odecode
+    prepared, forced, steps = oracle_cycle(wl)
+    secs = []
+    while len(secs) < n_min or sum(secs) < seconds_min:
+        r = odecode.run(wl, steps=steps, prepared=prepared, slow=forced)
+        secs.append(float(r["seconds"].sum()))
+    return secs, wl.cfg.batch * steps, steps
+
+
 def run_reference(args, world, rank):
-    """The CPU oracle, as it stands, on the host cores: each step is a bounded sample of the
-    workload (the first decode steps of every unit), extrapolated to the whole run's mix."""
+    """The CPU oracle, as it stands, on the host cores. One step = one timed SFI cycle of
+    every unit (oracle_cycle): value = tokens of the timed cycles / their seconds."""
     if rank != 0:
         return
-    import oracle
     from oracle import decode as odecode
     from synth.configs import WORKLOADS
     from synth.workload import HostWorkload
     wl = HostWorkload(WORKLOADS[args.workload])
     cfg = wl.cfg
-    n_sample = 12
-    prepared = odecode.prepare(wl, n_sample)
-    slow_full = np.stack([oracle.schedule(wl.masks[b], cfg.t_max) for b in range(cfg.batch)], 1)
-    n_slow_full = int(slow_full.any(axis=1).sum())
-    vals = []
-    for i in range(args.warmup + args.steps):
-        r = odecode.run(wl, steps=n_sample, prepared=prepared)
-        sl = r["slow"].any(axis=0)
-        t_slow = r["seconds"][sl].mean()
-        t_fast = r["seconds"][~sl].mean()
-        full = n_slow_full * t_slow + (cfg.steps - n_slow_full) * t_fast
-        if i >= args.warmup:
-            vals.append(cfg.batch * cfg.steps / full)
-    v = float(np.mean(vals))
+    time_oracle_cycles(wl, args.warmup)
+    secs, tokens, steps = time_oracle_cycles(wl, args.steps)
+    v = tokens * len(secs) / sum(secs)
     cores = os.cpu_count()
-    sample = (f"first {n_sample} decode steps of all {wl.n_units} units per step "
-              f"({int(slow_full[:n_sample].any(axis=1).sum())} slow), per-step costs extrapolated "
-              f"to the run's {n_slow_full} slow + {cfg.steps - n_slow_full} fast steps")
+    sample = (f"per step: decode steps 0..{steps - 1} of all {wl.n_units} units, step 0 slow and "
+              f"{steps - 1} fast (the run's slow:fast mix), {tokens} tokens; "
+              f"{len(secs)} timed steps took {sum(secs):.2f} s")
+    slow_full = odecode.schedule(wl)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1000.0 * cfg.batch * cfg.steps / v, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg.name},
+        "ms_per_step": 1000.0 * sum(secs) / len(secs), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
+        "config": dict(workload_config(wl, int(slow_full.any(axis=0).sum())),
+                       parallelism="replicas" if world > 1 else "single"),
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "seconds": sum(secs)},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
@@ -237,25 +256,17 @@ def run_reference(args, world, rank):
 # ------------------------------------------------------------------------------- our arm
 
 def cpu_baseline(wl):
-    import oracle
-    from oracle import decode as odecode
-    cfg = wl.cfg
-    n_sample = 12
-    prepared = odecode.prepare(wl, n_sample)
-    r = odecode.run(wl, steps=n_sample, prepared=prepared)
-    slow_full = np.stack([oracle.schedule(wl.masks[b], cfg.t_max) for b in range(cfg.batch)], 1)
-    n_slow = int(slow_full.any(axis=1).sum())
-    sl = r["slow"].any(axis=0)
-    full = n_slow * r["seconds"][sl].mean() + (cfg.steps - n_slow) * r["seconds"][~sl].mean()
-    return {"value": cfg.batch * cfg.steps / full, "unit": "tokens/s", "cores": os.cpu_count(),
+    """The oracle on the host cores over about 10 s of SFI cycles (see oracle_cycle)."""
+    secs, tokens, steps = time_oracle_cycles(wl, 2, seconds_min=10.0)
+    return {"value": tokens * len(secs) / sum(secs), "unit": "tokens/s", "cores": os.cpu_count(),
             "kind": "oracle",
-            "sample": f"first {n_sample} decode steps of all {wl.n_units} units "
-                      f"({int(sl.sum())} slow), per-step costs extrapolated to the full mix",
-            "seconds": float(r["seconds"].sum())}
+            "sample": f"{len(secs)} SFI cycles of all {wl.n_units} units (decode steps "
+                      f"0..{steps - 1}: step 0 slow, the rest fast), {tokens} tokens each",
+            "seconds": float(sum(secs))}
 
 
 def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=None,
-            dense_only_runs=0, pipeline_runs=0):
+            dense_only_runs=0, pipeline_runs=0, cold_fast=False):
     """Time whole decode runs of one workload (CUDA-graph replays), the per-kernel durations
     (event-instrumented replays), and optionally the dense-only / fast-only modes and the
     end-to-end run with host buffers."""
@@ -264,7 +275,7 @@ def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=N
     cfg = wl.cfg
     st = sdev.make_state(wl, device=dev)
     ins = sdev.DeviceInputs(wl, cfg.steps, dev)
-    slow = st.schedule(wl.masks)                       # [steps][B]
+    slow = sdev.schedule(wl, st)                       # [steps][B]
     out = torch.empty((cfg.steps, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
                       dtype=torch.bfloat16, device=dev)
     len0 = st.seq_len.clone()
@@ -462,23 +473,126 @@ def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=N
         del g_pipe
         res["layer_pipeline"] = {"tokens_per_s": world * tokens_per_run * pipeline_runs / (ms_p / 1000.0),
                                  "ms_per_run": ms_p / pipeline_runs}
+    if cold_fast:
+        res["fast_cold"] = fast_step_cold(wl, st, ins, stream, dev, world)
     torch.cuda.synchronize()
     res["device_error"] = int(st.err[0])
-    res["kv_bytes"] = int(st.k.numel() * 4)
     del g_mix
     return res
 
 
-def workload_config(wl, res):
+def fast_step_cold(wl, st, ins, stream, dev, world, per_replica=8, k=10, w=3):
+    """The fused fast step with a cold L2. Its working set (packed rows + window) fits in L2
+    for small workloads, so consecutive fast steps of one run hit in L2 (the in-run, warm
+    figure). Here R copies of the decode state (cache and packed memory, as the timed runs
+    left them) take the launches in turn, R chosen so that their per-launch working sets
+    together exceed 2x L2: every launch then reads its rows from HBM, as the fast step of
+    one layer among many would. Lengths restart 8 positions past the prefill."""
+    import math
+
+    import torch
+    from sparse_long_context_sfi_gb300 import sfi_fast_decode_step
+    from sparse_long_context_sfi_gb300.engine import SfiState
     cfg = wl.cfg
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    len_start = wl.len0.astype(np.int64) + 8
+    rows = st.rows.view(cfg.n_layers, cfg.batch, cfg.n_kv_heads).double().cpu().numpy()
+    per_unit_q = cfg.group * 256 + cfg.group * 128 * 2
+
+    def launch_bytes(L):                     # L: lengths before the launch's append
+        Ln = L + 1
+        win = Ln - np.maximum(np.minimum(cfg.n_sink, Ln), Ln - cfg.n_window)
+        return float(((rows + win[None, :, None]) * BYTES_PER_ROW).sum() +
+                     rows.size * (per_unit_q + 2 * BYTES_PER_ROW))
+
+    per_launch = launch_bytes(len_start)
+    R = max(4, math.ceil(2 * l2 / per_launch) + 1)
+    reps = [st]
+    for _ in range(R - 1):
+        r = SfiState(cfg, wl.len0, device=dev, page_table=wl.table, n_pages=wl.n_pages)
+        for name in ("k", "v", "kc", "vc", "sel_idx", "sel_cnt", "rows"):
+            getattr(r, name).copy_(getattr(st, name))
+        reps.append(r)
+    start = torch.from_numpy(len_start.astype(np.int32)).to(dev)
+    for r in reps:
+        r.seq_len.copy_(start)
+        r.kv.max_len = r.capacity - 1        # host bound on every length these launches see
+    out = torch.empty((cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
+                      dtype=torch.bfloat16, device=dev)
+    n = R * per_replica
+
+    def issue():
+        for i in range(n):
+            r = reps[i % R]
+            t = i % ins.q.shape[0]
+            sfi_fast_decode_step(r.kv, r.mem, r.budget, ins.k_new[t], ins.v_new[t], ins.q[t], out,
+                                 False, r.ws, r.ws_bytes, stream=stream)
+
+    with torch.cuda.stream(stream):
+        issue()                               # eager: builds the maps, checks the arguments
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+        issue()
+    with torch.cuda.stream(stream):
+        for _ in range(w):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(k):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+    ms = allreduce_max(e0.elapsed_time(e1), world)
+    err = max(int(r.err[0]) for r in reps)
+    # lengths grew by one per launch on each replica; bytes of the middle launch stand in
+    mid = launch_bytes(len_start + per_replica * (1 + w + k // 2))
+    avg = ms * 1e-3 / (k * n)
+    peak, _ = measured_peaks()
+    del g, reps
+    torch.cuda.empty_cache()
+    return {"avg_us": avg * 1e6, "bytes_per_launch": mid, "achieved_gbs": mid / avg / 1e9,
+            "frac_of_peak": mid / avg / 1e9 / peak, "replicas": R,
+            "working_set_bytes_all_replicas": per_launch * R, "l2_bytes": l2,
+            "launches_timed": k * n, "device_error": err}
+
+
+def kv_bytes(wl) -> int:
+    """Bytes of the resident K+V cache of a workload's decode state."""
+    cfg = wl.cfg
+    if cfg.page_size:
+        rows = cfg.n_layers * wl.n_pages * cfg.n_kv_heads * cfg.page_size
+    else:
+        rows = cfg.n_layers * cfg.batch * cfg.n_kv_heads * (int(wl.len0.max()) + cfg.steps)
+    return rows * BYTES_PER_ROW
+
+
+def data_of(cfg) -> str:
+    model = ("Zipf(1.1) key-norm boost" if cfg.key_model == "zipf" else
+             "planted heavy hitters" + (", drifting at boundaries" if cfg.drift else ""))
+    trig = ("trigger tokens in seeded per-sequence token streams" if cfg.trigger == "tokens"
+            else "seeded boundary masks")
+    return f"synthetic (seeded counter-based generator; {model}; slow steps from {trig})"
+
+
+def workload_config(wl, slow_steps: int):
+    cfg = wl.cfg
+    fast_ws = (cfg.n_layers * cfg.batch * cfg.n_kv_heads *
+               (cfg.n_sink + cfg.n_select + cfg.n_window) * BYTES_PER_ROW)
     return {"workload": cfg.name, "layers": cfg.n_layers, "batch": cfg.batch,
             "q_heads": cfg.n_q_heads, "kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim,
             "context": int(wl.len0.max()) if cfg.ctx_lo == cfg.ctx else f"{cfg.ctx_lo}-{cfg.ctx}",
             "paged": bool(cfg.page_size), "decode_steps_per_step": cfg.steps,
-            "slow_steps_per_step": res["slow_steps"],
+            "slow_steps_per_step": slow_steps,
+            "trigger": "tokens" if cfg.trigger == "tokens" else "boundary mask",
             "budget": f"{cfg.n_sink} sinks + {cfg.n_window} window + {cfg.n_select} selected",
-            "l2": f"inputs larger than L2: every slow step streams the {res['kv_bytes'] / 1e6:.0f} MB "
-                  "KV cache; no flush"}
+            "l2": (f"no flush: the {kv_bytes(wl) / 1e6:.0f} MB KV cache is larger than L2 and every "
+                   f"slow step streams it from HBM; the fast steps' working set (packed rows + "
+                   f"window, up to {fast_ws / 1e6:.1f} MB per launch) is re-read by consecutive "
+                   f"fast steps, and stays L2-resident between them when it fits (the in-run, "
+                   f"warm figure); roofline.cold times the fast step over replica states whose "
+                   f"working sets together exceed 2x L2")}
 
 
 def main():
@@ -499,7 +613,7 @@ def main():
     stream = torch.cuda.Stream(device=dev)
     wl = HostWorkload(WORKLOADS[args.workload])
     res = measure(wl, args, world, dev, stream, args.steps, args.warmup, extras=not args.no_extras,
-                  clock_index=local)
+                  clock_index=local, cold_fast=not args.no_extras)
     torch.cuda.empty_cache()
     others = {}
     if not args.no_extras and args.also:
@@ -509,26 +623,46 @@ def main():
             multi = w2.cfg.n_layers > 1
             r2 = measure(w2, args, world, dev, stream, 2 if big else max(3, args.steps // 4),
                          1 if big else 2, extras=False, dense_only_runs=1 if big else 2,
-                         pipeline_runs=(1 if big else 2) if multi else 0)
+                         pipeline_runs=(1 if big else 2) if multi else 0, cold_fast=not big)
             others[name] = {"tokens_per_s": r2["value"], "ms_per_run": r2["ms_per_run"],
-                            "config": workload_config(w2, r2), "kernels": r2["kernels"],
+                            "config": workload_config(w2, r2["slow_steps"]),
+                            "kernels": r2["kernels"],
                             "device_error": r2["device_error"]}
             if "dense_only" in r2:
                 others[name]["dense_only"] = r2["dense_only"]
                 others[name]["sfi_vs_dense_speedup"] = r2["value"] / r2["dense_only"]["tokens_per_s"]
             if "layer_pipeline" in r2:
                 others[name]["layer_pipeline"] = r2["layer_pipeline"]
+            if "fast_cold" in r2:
+                others[name]["fast_step_cold"] = r2["fast_cold"]
             torch.cuda.empty_cache()
 
     peak, peak_kind = measured_peaks()
     ks = res["kernels"]
     dom_name, dom = max(ks.items(), key=lambda x: -1 if x[1] is None else x[1]["total_us_per_run"])
     traffic = traffic_record(dom_name)
-    roofline = {"bound": "hbm", "achieved": dom["achieved_gbs"], "peak": peak, "unit": "GB/s",
-                "frac": dom["achieved_gbs"] / peak, "kernel": dom_name,
-                "peak_kind": f"{peak_kind} (hbm_gbs, STREAM-style copy)",
-                "bytes_per_launch": dom["bytes_per_launch"], "avg_launch_us": dom["avg_us"],
-                "traffic": None if traffic is None else traffic["dram_bytes_per_launch"]}
+    warm = {"achieved": dom["achieved_gbs"], "frac": dom["achieved_gbs"] / peak,
+            "avg_launch_us": dom["avg_us"], "bytes_per_launch": dom["bytes_per_launch"],
+            "how": "in the timed runs (CUDA events around every slow step's dense kernel and "
+                   "every stretch of consecutive fast steps)"}
+    cold = None
+    if dom_name == "sfi_sparse_decode_attn" and res.get("fast_cold"):
+        fc = res["fast_cold"]
+        cold = {"achieved": fc["achieved_gbs"], "frac": fc["frac_of_peak"],
+                "avg_launch_us": fc["avg_us"], "bytes_per_launch": fc["bytes_per_launch"],
+                "how": f"fast steps over {fc['replicas']} replica states taken in turn "
+                       f"({fc['working_set_bytes_all_replicas'] / 1e6:.0f} MB of working sets, "
+                       f"L2 {fc['l2_bytes'] / 1e6:.0f} MB)"}
+    head = cold or warm
+    roofline = {"bound": "hbm", "achieved": head["achieved"], "peak": peak, "unit": "GB/s",
+                "frac": head["achieved"] / peak, "kernel": dom_name,
+                "peak_kind": f"{peak_kind} (hbm_gbs, STREAM-style copy); frac is judged on it",
+                "frac_of_nominal": head["achieved"] / NOMINAL_HBM_GBS,
+                "nominal_gbs": NOMINAL_HBM_GBS,
+                "bytes_per_launch": head["bytes_per_launch"], "avg_launch_us": head["avg_launch_us"],
+                "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
+                "cold": cold, "warm": warm,
+                "headline": "cold" if cold else "in-run"}
     cpu = None
     if rank == 0 and world == 1 and not args.no_extras:
         cpu = cpu_baseline(wl)
@@ -537,8 +671,8 @@ def main():
             "metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_run"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded counter-based generator, Zipf(1.1) key-norm boost)",
-            "config": dict(workload_config(wl, res),
+            "data": data_of(wl.cfg),
+            "config": dict(workload_config(wl, res["slow_steps"]),
                            parallelism="replicas" if world > 1 else "single"),
             "roofline": roofline,
             "kernels": ks,

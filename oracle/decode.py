@@ -23,6 +23,27 @@ def epochs(mask: np.ndarray) -> np.ndarray:
     return e
 
 
+def schedule(wl, steps: int | None = None) -> np.ndarray:
+    """Slow flags [B][steps] by the oracle's trigger policy: on the workload's boundary masks,
+    or, for a token-triggered workload, on its generated token streams (trigger tokens
+    '.', '?', '!', newline; gist.science summary, section 2C)."""
+    cfg = wl.cfg
+    n = cfg.steps if steps is None else steps
+    if cfg.trigger == "tokens":
+        from synth.gen import TRIGGER_TOKENS
+        trig = np.asarray(TRIGGER_TOKENS, np.int32)
+        return np.stack([oracle.schedule_tokens(wl.tokens[b][:n], trig, cfg.t_max)
+                         for b in range(cfg.batch)])
+    return np.stack([oracle.schedule(wl.masks[b][:n], cfg.t_max) for b in range(cfg.batch)])
+
+
+def _sub(kc, vc, idx):
+    """The caches of the units in idx (no copy when that is every unit)."""
+    if len(idx) == kc.shape[0]:
+        return kc, vc
+    return kc[idx], vc[idx]
+
+
 def prepare(wl, steps: int, units=None):
     """Generate (untimed) the K/V rows every simulated unit will read: prefill + appended."""
     cfg = wl.cfg
@@ -44,8 +65,11 @@ def prepare(wl, steps: int, units=None):
 
 
 def run(wl, steps: int | None = None, units=None, threads: int = 0, want_f: bool = False,
-        gpu_selection=None, prepared=None):
+        gpu_selection=None, prepared=None, slow=None):
     """Simulate `steps` decode steps for the given units (default: all).
+
+    slow (optional): uint8 [B][steps] step types to use instead of the trigger policy's
+    (a benchmark sample of one slow step and the fast steps that follow it).
 
     gpu_selection (optional): {(t, u): ascending positions} to use instead of the oracle's
     own selection at slow steps (isolates the attention from selection near-ties).
@@ -60,13 +84,14 @@ def run(wl, steps: int | None = None, units=None, threads: int = 0, want_f: bool
     G, D = cfg.group, cfg.head_dim
     S, W, K = cfg.n_sink, cfg.n_window, cfg.n_select
     nU = len(units)
-    slow = np.stack([oracle.schedule(wl.masks[b][:steps], cfg.t_max) for b in range(cfg.batch)])
+    slow = schedule(wl, steps) if slow is None else np.asarray(slow, np.uint8)[:, :steps]
     ep = np.stack([epochs(wl.masks[b][:steps]) for b in range(cfg.batch)])
     L_slow = np.zeros(nU, np.int64)
     sel = [np.zeros(0, np.int32) for _ in range(nU)]
     res = {"slow": slow, "out": {}, "sel": {}, "f": {}, "seconds": np.zeros(steps)}
+    qcache = {}
     for t in range(steps):
-        t0 = time.perf_counter()
+        # input generation and the drifting-key edits are harness work: not timed
         if cfg.drift and t > 0:
             for i, (layer, b, kvh) in enumerate(coords):
                 if ep[b, t] != ep[b, t - 1]:
@@ -74,13 +99,16 @@ def run(wl, steps: int | None = None, units=None, threads: int = 0, want_f: bool
                     new = wl.hh_positions(layer, b, kvh, int(ep[b, t]))
                     ch = np.union1d(old, new)
                     kc[i, ch] = wl.rows("k", layer, b, kvh, ch, epoch=int(ep[b, t]))
-        q = np.stack([wl.query(t, layer, b)[kvh * G:(kvh + 1) * G] for (layer, b, kvh) in coords])
+        for (layer, b) in {(layer, b) for (layer, b, _) in coords}:
+            qcache[(layer, b)] = wl.query(t, layer, b)
+        q = np.stack([qcache[(layer, b)][kvh * G:(kvh + 1) * G] for (layer, b, kvh) in coords])
         L = np.array([int(wl.len0[b]) + t + 1 for (_, b, _) in coords], np.int64)
         is_slow = np.array([slow[b, t] for (_, b, _) in coords], bool)
+        t0 = time.perf_counter()
         out = np.zeros((nU, G, D))
         if is_slow.any():
             idx = np.flatnonzero(is_slow)
-            o, f = oracle.attend_batch(q[idx], kc[idx], vc[idx], L[idx], want_f=True,
+            o, f = oracle.attend_batch(q[idx], *_sub(kc, vc, idx), L[idx], want_f=True,
                                        threads=threads)
             out[idx] = o
             for j, i in enumerate(idx):
@@ -100,7 +128,7 @@ def run(wl, steps: int | None = None, units=None, threads: int = 0, want_f: bool
             rr = np.zeros((len(idx), rmax), np.int32)
             for j, r in enumerate(rows):
                 rr[j, :len(r)] = r
-            o, _ = oracle.attend_batch(q[idx], kc[idx], vc[idx],
+            o, _ = oracle.attend_batch(q[idx], *_sub(kc, vc, idx),
                                        np.array([len(r) for r in rows]), rows=rr,
                                        threads=threads)
             out[idx] = o

@@ -759,17 +759,4 @@ sfi_status sfi_clear_error(const sfi_kv_cache *kv, void *stream)
     return launch_status(cudaMemsetAsync(kv->err, 0, sizeof(uint32_t), as_stream(stream)));
 }
 
-#ifdef SFI_TRACE
-// Tuning builds only: copy the per-CTA timeline of the last attention launch.
-int sfi_trace_read(unsigned long long *host, int n_ctas)
-{
-    return static_cast<int>(sfi::trace_read(host, n_ctas));
-}
-
-int sfi_trace_read_select(unsigned long long *host, int n_ctas)
-{
-    return static_cast<int>(sfi::trace_read_select(host, n_ctas));
-}
-#endif
-
 }  // extern "C"

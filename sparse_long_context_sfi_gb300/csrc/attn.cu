@@ -48,17 +48,6 @@ constexpr int kCtrlOff = kPOff + 2 * kOpBytes;
 constexpr int kFlagFirst = 1;   // first tile of a segment (a unit's tiles inside one CTA)
 constexpr int kFlagLast = 2;    // last tile of a segment
 
-// Optional per-CTA timeline for tuning (compile with -DSFI_TRACE): globaltimer stamps at
-// fixed checkpoints, read back through sfi_trace_read. Off in normal builds.
-#ifdef SFI_TRACE
-__device__ unsigned long long g_sfi_trace[1024][32];
-#define SFI_STAMP(slot) (g_sfi_trace[blockIdx.x & 1023][(slot)] = global_timer_ns())
-#define SFI_TRACE_SET(slot, v) (g_sfi_trace[blockIdx.x & 1023][(slot)] = (v))
-#else
-#define SFI_STAMP(slot) ((void)0)
-#define SFI_TRACE_SET(slot, v) ((void)0)
-#endif
-
 struct TileMeta {
     int unit;
     int tile;
@@ -191,8 +180,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     // ---- set-up touching no global memory: overlaps the previous kernel's tail ----------
     pdl_trigger();
-    if (threadIdx.x == 0)
-        SFI_STAMP(0);
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&c.full[s], 1);
@@ -246,8 +233,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     // ---- tile space: per-sequence tile counts and this CTA's range --------------------
     pdl_wait();
-    if (threadIdx.x == 0)
-        SFI_STAMP(1);
     long long g0 = 0, g1 = 0;
     int n_tiles = 0;
     if (!clustered) {
@@ -344,10 +329,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             fail(c, p.err);
         }
     }
-    if (tid == 0) {
-        SFI_STAMP(2);
-        SFI_TRACE_SET(12, n_tiles);
-    }
     const uint32_t tmem = c.tmem_base;
 
     if (warp == 0) {
@@ -356,8 +337,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // 64-column half of K or V for one page / block of rows), and lane 0 publishes the
         // tile with a single arrive.expect_tx of the warp's summed bytes.
         if (n_tiles > 0) {
-            if (lane == 0)
-                SFI_STAMP(22);
             const uint64_t pol = policy_evict_first();
             // decode the first tile of the range
             long long g = g0;
@@ -436,8 +415,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const int s = i % kStages;
                 if (lane == 0)
                     ok = mbar_wait(&c.empty[s], ((i / kStages) & 1) ^ 1, &c.abort);
-                if (lane == 0 && i == 0)
-                    SFI_STAMP(23);
                 const int u = (layer * B + b) * Hkv + kvh;
                 const bool first = (i == 0) || (t == 0);
                 const bool last = (i == n_tiles - 1) || (t == ntiles_of(b) - 1);
@@ -465,8 +442,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         appended = false;
                     }
                 }
-                if (lane == 0 && i == 0)
-                    SFI_STAMP(29);
                 if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
                     if (lane == 0)
                         fail(c, p.err);
@@ -576,8 +551,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                     appended = true;
                 }
-                if (lane == 0 && i == 0)
-                    SFI_STAMP(30);
                 // ---- publish the tile, then issue ---------------------------------------
                 uint32_t vw[4];
 #pragma unroll
@@ -599,8 +572,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     for (int w = 0; w < 4; ++w)
                         mt.valid[w] = vw[w];
                     mbar_arrive_expect_tx(bar, bytes);  // releases the metadata
-                    if (i == 0)
-                        SFI_STAMP(31);
                 }
                 __syncwarp();
                 if (first && lane < 2) {
@@ -619,8 +590,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     append_row(u, layer, b, kvh, L - 1);
                     appended = true;
                 }
-                if (lane == 0 && i == 0)
-                    SFI_STAMP(3);
                 ++issued;
                 if (paged_dense && i + 1 < n_tiles) {
                     int nb = b, nt2 = t + 1;
@@ -677,8 +646,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const int s = ns % kStages, bb = ns & 1, use = ns >> 1;
                     if (mbar_test_wait(&c.full[s], (ns / kStages) & 1) &&
                         mbar_test_wait(&c.s_free[bb], (use & 1) ^ 1)) {
-                        if (ns == 0)
-                            SFI_STAMP(4);
                         const int flags = c.meta[s].flags;
                         if (flags & kFlagFirst)
                             ++seg;
@@ -692,8 +659,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             umma_bf16(tmem + bb * 16, a, bd, idesc_s, kk > 0 ? 1u : 0u);
                         }
                         umma_commit(&c.s_full[bb]);
-                        if (ns == 0)
-                            SFI_STAMP(11);
                         if (flags & kFlagLast)
                             umma_commit(&c.q_free[seg & 1]);
                         ++ns;
@@ -715,8 +680,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         }
                         umma_commit(&c.o_full[bb]);
                         umma_commit(&c.empty[s]);
-                        if (np == 0)
-                            SFI_STAMP(15);
                         ++np;
                         prog = true;
                     }
@@ -757,9 +720,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         uint32_t gphase = 0;
         float m_run[G], le[G], acc[G];
         // the tile waiting for its O^T accumulation
-        float a_alpha[G], a_m[G], a_le[G], a_lr[G];
+        float a_alpha[G], a_m[G], a_le[G];
         // clustered: this CTA's (max, sum) of its slice, with acc[] its unnormalised output
-        float fin_m[G], fin_lr[G];
+        float fin_m[G], fin_le[G];
         int a_flags = 0, a_unit = 0;
         bool ok = true;
 #pragma unroll
@@ -767,7 +730,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             m_run[h] = -INFINITY;
             le[h] = acc[h] = 0.f;
             fin_m[h] = -INFINITY;
-            fin_lr[h] = 0.f;
+            fin_le[h] = 0.f;
         }
 
         if (clustered && fused && warp == 2 && c.cl_app_tile >= 0) {
@@ -799,8 +762,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 mbar_arrive(&c.app_ready);
         }
 
-        auto finalize = [&](int u, const float (&fm)[G], const float (&fle)[G],
-                            const float (&flr)[G]) -> bool {
+        auto finalize = [&](int u, const float (&fm)[G], const float (&fle)[G]) -> bool {
             const int kvh = u % Hkv, b = (u / Hkv) % B, layer = u / (Hkv * B);
             const long long su = layer * c.TL + c.pre[b] + static_cast<long long>(kvh) * c.nt[b];
             const long long eu = su + c.nt[b];
@@ -812,7 +774,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (cf == cl) {
 #pragma unroll
                 for (int h = 0; h < G; ++h)
-                    o[h] = flr[h] > 0.f ? acc[h] / flr[h] : 0.f;
+                    o[h] = fle[h] > 0.f ? acc[h] / fle[h] : 0.f;
                 store_out<G>(p, u, row, o);
                 if (DENSE && row < G)
                     p.stats[u * G + row] = make_float2(pick<G>(fm, row), pick<G>(fle, row));
@@ -826,15 +788,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (row < G) {
                 part[G * kHeadDim + row] = pick<G>(fm, row);
                 part[G * kHeadDim + G + row] = pick<G>(fle, row);
-                part[G * kHeadDim + 2 * G + row] = pick<G>(flr, row);
             }
             // Every thread's partial writes happen before thread 0's release fence (group
             // barrier), which publishes them before the ticket; the last contributor's
             // acquire fence and the second barrier make all partials visible to its threads.
             if (!group_sync(c, gphase, lane))
                 return false;
-            if (row == 0)
-                SFI_STAMP(24);
             if (row == 0) {
                 fence_acq_rel_gpu();
                 const int tk = atomicAdd(&p.tickets[u], 1);
@@ -844,28 +803,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     fence_acq_rel_gpu();
                 }
                 c.last_flag = is_last;
-                SFI_STAMP(25);
             }
             if (!group_sync(c, gphase, lane))
                 return false;
             if (!c.last_flag)
                 return true;
-            if (row == 0)
-                SFI_STAMP(26);
             // One-pass online merge starting from this CTA's own partial (in registers);
             // the other contributors are read four at a time so their loads overlap.
-            float M[G], Le[G], Lr[G];
+            float M[G], Le[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) {
                 M[h] = fm[h];
                 Le[h] = fle[h];
-                Lr[h] = flr[h];
                 o[h] = acc[h];
             }
             // u may be the last segment of cf's range (slot 1)
             const bool cf_tail = static_cast<long long>(cf) * T / P < su;
             for (int c0 = cf; c0 <= cl; c0 += 4) {
-                float mc[4][G], lc[4][G], rc[4][G], ac[4][G];
+                float mc[4][G], lc[4][G], ac[4][G];
                 bool use[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -879,7 +834,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     for (int h = 0; h < G; ++h) {
                         mc[k][h] = use[k] ? __ldcg(pc + G * kHeadDim + h) : -INFINITY;
                         lc[k][h] = use[k] ? __ldcg(pc + G * kHeadDim + G + h) : 0.f;
-                        rc[k][h] = use[k] ? __ldcg(pc + G * kHeadDim + 2 * G + h) : 0.f;
                         ac[k][h] = use[k] ? __ldcg(pc + h * kHeadDim + row) : 0.f;
                     }
                 }
@@ -891,17 +845,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const float a = (M[h] == -INFINITY) ? 0.f : exp2f(M[h] - mn);
                         const float w = (mc[k][h] == -INFINITY) ? 0.f : exp2f(mc[k][h] - mn);
                         Le[h] = Le[h] * a + w * lc[k][h];
-                        Lr[h] = Lr[h] * a + w * rc[k][h];
                         o[h] = o[h] * a + w * ac[k][h];
                         M[h] = mn;
                     }
                 }
             }
-            if (row == 0)
-                SFI_STAMP(27);
 #pragma unroll
             for (int h = 0; h < G; ++h)
-                o[h] = Lr[h] > 0.f ? o[h] / Lr[h] : 0.f;
+                o[h] = Le[h] > 0.f ? o[h] / Le[h] : 0.f;
             store_out<G>(p, u, row, o);
             if (DENSE && row < G)
                 p.stats[u * G + row] = make_float2(pick<G>(M, row), pick<G>(Le, row));
@@ -925,20 +876,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int h = 0; h < G; ++h)
                 acc[h] = (a_flags & kFlagFirst) ? ov[h] : fmaf(acc[h], a_alpha[h], ov[h]);
             if (a_flags & kFlagLast) {
-                if (row == 0)
-                    SFI_STAMP(6);
                 if (clustered) {  // merged across the cluster after the loop
 #pragma unroll
                     for (int h = 0; h < G; ++h) {
                         fin_m[h] = a_m[h];
-                        fin_lr[h] = a_lr[h];
+                        fin_le[h] = a_le[h];
                     }
                     return true;
                 }
-                if (!finalize(a_unit, a_m, a_le, a_lr))
+                if (!finalize(a_unit, a_m, a_le))
                     return false;
-                if (row == 0)
-                    SFI_STAMP(7);
 #pragma unroll
                 for (int h = 0; h < G; ++h)
                     acc[h] = 0.f;
@@ -953,10 +900,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 ok = false;
                 break;
             }
-            if (i == 0 && row == 0)
-                SFI_STAMP(5);
-            if (i == 1 && row == 0)
-                SFI_STAMP(16);
             const int u = c.meta[s].unit;
             const int tile = c.meta[s].tile;
             const int flags = c.meta[s].flags;
@@ -974,10 +917,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&c.s_free[bb]);
-            if (i == 0 && row == 0)
-                SFI_STAMP(13);
-            if (i == 1 && row == 0)
-                SFI_STAMP(17);
             float z[G];
 #pragma unroll
             for (int h = 0; h < G; ++h)
@@ -1003,10 +942,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 ok = false;
                 break;
             }
-            if (i == 0 && row == 0)
-                SFI_STAMP(14);
-            if (i == 1 && row == 0)
-                SFI_STAMP(18);
             float alpha[G];
             uint8_t *pb = smem + kPOff + bb * kOpBytes;
 #pragma unroll
@@ -1039,15 +974,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     reinterpret_cast<uint4 *>(vrow + kChunkBytes)[k] = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            if (i == 1 && row == 0)
-                SFI_STAMP(19);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&c.p_full[bb]);
-            if (i == 1 && row == 0)
-                SFI_STAMP(20);
-            float fm[G], fle[G], flr[G];
+            float fm[G], fle[G];
             if (flags & kFlagLast) {
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
@@ -1063,15 +994,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int h = 0; h < G; ++h) {
                     fm[h] = m_run[h];
                     fle[h] = c.red_sum[0][h] + c.red_sum[1][h] + c.red_sum[2][h] + c.red_sum[3][h];
-                    flr[h] = fle[h];
                 }
             }
             if (i > 0 && !correct(i - 1)) {
                 ok = false;
                 break;
             }
-            if (i == 1 && row == 0)
-                SFI_STAMP(21);
             // this tile now waits for its accumulation
 #pragma unroll
             for (int h = 0; h < G; ++h) {
@@ -1079,19 +1007,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (flags & kFlagLast) {
                     a_m[h] = fm[h];
                     a_le[h] = fle[h];
-                    a_lr[h] = flr[h];
                 }
             }
             a_flags = flags;
             a_unit = u;
             (void)tile;
         }
-        if (row == 0)
-            SFI_STAMP(8);
         if (ok && n_tiles > 0 && !correct(n_tiles - 1))
             ok = false;
-        if (row == 0)
-            SFI_STAMP(9);
         if (clustered && c.cl_live) {
             // ---- merge the cluster's partials through distributed shared memory ----------
             // CTA r owns dims [r 128/C, (r+1) 128/C). Every CTA pushes, with remote stores,
@@ -1120,35 +1043,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const uint32_t b2 = map_to_rank(recv, static_cast<uint32_t>(ow));
                     const int o2 = acc_floats + (rank * G + h) * 2;
                     st_cluster_f32(b2 + 4u * o2, pick<G>(fin_m, h));
-                    st_cluster_f32(b2 + 4u * (o2 + 1), pick<G>(fin_lr, h));
+                    st_cluster_f32(b2 + 4u * (o2 + 1), pick<G>(fin_le, h));
                 }
             }
-            if (row == 0)
-                SFI_STAMP(26);
             bool good = group_sync(c, gphase, lane) && ok;  // every thread's pushes are issued
             if (row < C)  // lanes 0..C-1 of one warp, one owner each, in parallel
                 mbar_arrive_cluster(map_to_rank(&c.cl_ready, static_cast<uint32_t>(row)));
-            if (row == 0)
-                SFI_STAMP(28);
             // A peer arrives within its own bounded waits even when it fails; this limit is
             // well above those, so no CTA leaves while a live peer may still push to it.
             good = mbar_wait_cluster(&c.cl_ready, 0, 8 * kWaitTimeoutNs) && good;
-            if (row == 0)
-                SFI_STAMP(24);
             if (good) {
                 for (int o = row; o < nd * G; o += 4 * 32) {
                     const int h = o / nd, j = o - h * nd;
                     float M = -INFINITY;
                     for (int q = 0; q < C; ++q)
                         M = fmaxf(M, recv[acc_floats + (q * G + h) * 2]);
-                    float Lr = 0.f, O = 0.f;
+                    float Lsum = 0.f, O = 0.f;
                     for (int q = 0; q < C; ++q) {
                         const float mq = recv[acc_floats + (q * G + h) * 2];
                         const float w = (mq == -INFINITY) ? 0.f : exp2f(mq - M);
-                        Lr = fmaf(w, recv[acc_floats + (q * G + h) * 2 + 1], Lr);
+                        Lsum = fmaf(w, recv[acc_floats + (q * G + h) * 2 + 1], Lsum);
                         O = fmaf(w, recv[(q * G + h) * nd + j], O);
                     }
-                    const float v = Lr > 0.f ? O / Lr : 0.f;
+                    const float v = Lsum > 0.f ? O / Lsum : 0.f;
                     const size_t idx = (static_cast<size_t>(u) * G + h) * kHeadDim + rank * nd + j;
                     if (p.out_fp32)
                         static_cast<float *>(p.out)[idx] = v;
@@ -1156,8 +1073,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         static_cast<__nv_bfloat16 *>(p.out)[idx] = __float2bfloat16_rn(v);
                 }
             }
-            if (row == 0)
-                SFI_STAMP(25);
             if (!good)
                 ok = false;
         }
@@ -1170,8 +1085,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
-        if (lane == 0)
-            SFI_STAMP(10);
     }
 }
 
@@ -1409,12 +1322,5 @@ cudaError_t launch_sparse_static(int group, const CUtensorMap &tm_k, const CUten
         return e;
     return launch_attention(false, group, tm_k, tm_v, tm_q, tm_kc, tm_vc, p, grid, stream);
 }
-
-#ifdef SFI_TRACE
-cudaError_t trace_read(unsigned long long *host, int n)
-{
-    return cudaMemcpyFromSymbol(host, g_sfi_trace, sizeof(unsigned long long) * 32 * (n < 1024 ? n : 1024));
-}
-#endif
 
 }  // namespace sfi

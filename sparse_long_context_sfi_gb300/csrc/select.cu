@@ -27,16 +27,6 @@ constexpr int kWarps = NT / 32;
 constexpr int kListCap = 8192;    // keys gathered for the refining passes
 constexpr int kBatch = 8;         // candidates per thread per streaming step
 
-// Optional per-CTA timeline for tuning (compile with -DSFI_TRACE), read back through
-// sfi_trace_read_select. Off in normal builds.
-#ifdef SFI_TRACE
-__device__ unsigned long long g_sel_trace[1024][16];
-#define SEL_STAMP(slot) \
-    do { if (threadIdx.x == 0) g_sel_trace[blockIdx.x & 1023][(slot)] = global_timer_ns(); } while (0)
-#else
-#define SEL_STAMP(slot) ((void)0)
-#endif
-
 __device__ __forceinline__ uint32_t order_key(float x)
 {
     if (x != x)
@@ -166,10 +156,8 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
     __shared__ float sh_c[3];
 
     pdl_trigger();
-    SEL_STAMP(0);
     const int tid = threadIdx.x, lane = tid & 31;
     pdl_wait();
-    SEL_STAMP(8);
     const int u = blockIdx.x;
     const int b = (u / p.n_kv_heads) % p.batch;
     if (p.active && !p.active[b])
@@ -234,7 +222,6 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
     if (tid == 0)
         sh_count = 0;
     __syncthreads();
-    SEL_STAMP(1);
     fz.c1 = sh_c[0];
     fz.c2 = sh_c[1];
     fz.inv_tau = sh_c[2];
@@ -312,10 +299,8 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
     }
     __syncthreads();
     keys_ready = staged;
-    SEL_STAMP(2);
     int krem = K;
     find_digit(4096, krem);
-    SEL_STAMP(3);
     const uint32_t d0 = sh_digit;
     uint32_t prefix = d0 << 20, pmask = 0xFFF00000u;
     krem -= sh_above;
@@ -340,7 +325,6 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
         }
         __syncthreads();
     }
-    SEL_STAMP(4);
     // passes 1 and 2: 10-bit digits, over the gathered list (or every candidate)
 #pragma unroll 1
     for (int pass = 1; pass < 3; ++pass) {
@@ -371,12 +355,10 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
         pmask |= 1023u << shift;
         krem -= sh_above;
         __syncthreads();
-        SEL_STAMP(4 + pass);
     }
     const uint32_t thr = prefix;  // exact key of the K-th largest score
     const int need_eq = krem;     // how many keys equal to thr are taken (lowest first)
 
-    SEL_STAMP(9);
     // ---- ordered compaction ------------------------------------------------------------
     // A chosen candidate's slot = (keys > thr before it) + min(keys == thr before it,
     // need_eq). Warp w takes one contiguous range of candidates, 32 per step (lane =
@@ -396,10 +378,8 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
             n_gt += __popc(__ballot_sync(0xffffffffu, in && k > thr));
             n_eq += __popc(__ballot_sync(0xffffffffu, in && k == thr));
         }
-        SEL_STAMP(10);
         int2 tot;
         const int2 before = warp_totals_exclusive_scan(n_gt, n_eq, scratch, &tot);
-        SEL_STAMP(11);
         int gt_before = before.x, eq_before = before.y;
         for (int i0 = w0; i0 < w1; i0 += 32) {
             const int i = i0 + lane;
@@ -419,12 +399,7 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
     }
     if (tid == 0) {
         p.sel_cnt[u] = K;
-        SEL_STAMP(7);
     }
-#ifdef SFI_TRACE
-    if (tid == 0)
-        g_sel_trace[blockIdx.x & 1023][12] = static_cast<unsigned long long>(n_lst);
-#endif
 }
 
 // ---------------------------------------------------------------------------------------
@@ -455,9 +430,7 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
     __shared__ float sh_c[3];
 
     pdl_trigger();
-    SEL_STAMP(0);
     pdl_wait();
-    SEL_STAMP(8);
     const int C = p.cluster;
     const int rank = static_cast<int>(blockIdx.x) % C;
     const int u = static_cast<int>(blockIdx.x) / C;
@@ -518,7 +491,6 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
     for (int i = tid; i < 4096; i += NT)
         hbuf0[i] = 0u;
     __syncthreads();
-    SEL_STAMP(1);
     fz.c1 = sh_c[0];
     fz.c2 = sh_c[1];
     fz.inv_tau = sh_c[2];
@@ -559,9 +531,7 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
         __syncthreads();
     };
     int krem = K;
-    SEL_STAMP(2);
     merged_digit(hbuf0, 4096, krem);
-    SEL_STAMP(3);
     uint32_t prefix = sh_digit << 20, pmask = 0xFFF00000u;
     krem -= sh_above;
     // passes 1 and 2: 10-bit digits over this CTA's keys that share the prefix
@@ -582,7 +552,6 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
         pmask |= 1023u << shift;
         krem -= sh_above;
         __syncthreads();
-        SEL_STAMP(4 + pass);
     }
     const uint32_t thr = prefix;  // exact key of the K-th largest score
     const int need_eq = krem;     // how many keys equal to thr are taken (lowest first)
@@ -605,9 +574,7 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
         sh_counts[0] = tot.x;
         sh_counts[1] = tot.y;
     }
-    SEL_STAMP(10);
     cluster_sync_all();  // every CTA's counts are in place
-    SEL_STAMP(11);
     int gt_before = before.x, eq_before = before.y;
     for (int r = 0; r < rank; ++r) {
         gt_before += static_cast<int>(ld_cluster_u32(map_to_rank(&sh_counts[0], static_cast<uint32_t>(r))));
@@ -630,9 +597,7 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
     }
     if (tid == 0 && rank == 0)
         p.sel_cnt[u] = K;
-    SEL_STAMP(9);
     cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
-    SEL_STAMP(7);
 }
 
 template <typename Kern>
@@ -689,13 +654,6 @@ int select_cluster_size(int max_cluster)
 }
 
 int select_cluster_key_cap() { return kClusterKeyCap; }
-
-#ifdef SFI_TRACE
-cudaError_t trace_read_select(unsigned long long *host, int n)
-{
-    return cudaMemcpyFromSymbol(host, g_sel_trace, sizeof(unsigned long long) * 16 * (n < 1024 ? n : 1024));
-}
-#endif
 
 cudaError_t launch_select(const SelectParams &p, cudaStream_t stream)
 {

@@ -14,9 +14,9 @@ constexpr int kMaxBatch = 256;
 constexpr int kAttnThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2-5 softmax/epilogue
 constexpr int kSelectThreads = 1024;
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // bounded pipeline waits: 1 s
-// split-KV partial: G x 128 unnormalised outputs, then per head the max, the weight sum and
-// the normaliser
-constexpr int kPartialFloats(int G) { return G * kHeadDim + 3 * G; }
+// split-KV partial: G x 128 unnormalised outputs, then per head the running max and the
+// weight sum (base-2 logits)
+constexpr int kPartialFloats(int G) { return G * kHeadDim + 2 * G; }
 
 // Everything the attention kernels read besides the tensor maps.
 struct AttnParams {
@@ -123,11 +123,6 @@ cudaError_t launch_compact(const void *k, const void *v, void *kc, void *vc,
                            int n_select, uint32_t *err, cudaStream_t stream);
 
 size_t attention_smem_bytes();
-#ifdef SFI_TRACE
-cudaError_t trace_read(unsigned long long *host, int n);
-cudaError_t trace_read_select(unsigned long long *host, int n);
-#endif
-
 // Fast-step attention with its split-KV scratch in a library-owned device array instead of
 // a caller workspace (see sfi_sparse_decode_attn_static). p.partials and p.tickets are
 // filled in here. Limits: at most kStaticMaxUnits units; the grid is capped at

@@ -13,8 +13,8 @@ import numpy as np
 import torch
 
 from . import (SfiBudget, SfiDecodePlan, SfiKvCache, SfiSparseMem, sfi_append_kv, sfi_compact,
-               sfi_decode_run, sfi_dense_decode_attn, sfi_schedule, sfi_select,
-               sfi_fast_decode_step, sfi_sparse_decode_attn, sfi_workspace_bytes,
+               sfi_decode_run, sfi_dense_decode_attn, sfi_schedule, sfi_schedule_tokens,
+               sfi_select, sfi_fast_decode_step, sfi_sparse_decode_attn, sfi_workspace_bytes,
                sfi_workspace_init)
 
 
@@ -75,6 +75,12 @@ class SfiState:
     def schedule(self, masks: np.ndarray) -> np.ndarray:
         """Slow flags [steps][B] from per-sequence boundary masks [B][steps]."""
         return np.stack([sfi_schedule(masks[b], self.cfg.t_max) for b in range(self.cfg.batch)], 1)
+
+    def schedule_tokens(self, tokens: np.ndarray, trigger_ids) -> np.ndarray:
+        """Slow flags [steps][B] from per-sequence generated token ids [B][steps]: a slow step
+        follows a trigger token (or T_max steps without one)."""
+        return np.stack([sfi_schedule_tokens(tokens[b], trigger_ids, self.cfg.t_max)
+                         for b in range(self.cfg.batch)], 1)
 
     # -- one decode step through the individual calls -----------------------------------------
     def step(self, q, k_new, v_new, slow_b: np.ndarray, out, out_fp32=True, stream=None,

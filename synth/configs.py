@@ -30,6 +30,8 @@ class Workload:
     per_seq_mask: bool = False
     page_size: int = 0       # 0 = contiguous cache, 16 = paged
     drift: bool = False      # heavy hitters re-seeded at each boundary
+    trigger: str = "mask"    # 'mask': seeded boundary mask; 'tokens': trigger tokens in a
+                             # seeded token stream (mean span mask_param) decide the slow steps
     lam: float = 0.1         # fusion weight of the prior
     t_max: int = 64          # forced refresh after this many steps without a slow step
     seed: int = 0
@@ -75,6 +77,13 @@ WORKLOADS = {
         head_dim=128, ctx=131072, ctx_lo=131072, steps=512, n_sink=4, n_window=128,
         n_select=1916, key_model="hh", mask_kind="geometric", mask_param=24, drift=True,
         seed=0x5F1000 + 5),
+    # the 32K batch-4 shape with the trigger rule itself: every sequence generates its own
+    # token stream, and a slow step follows a trigger token ('.', '?', '!', newline)
+    "llama8b_ctx32k_b4_tok": Workload(
+        name="llama8b_ctx32k_b4_tok", n_layers=1, batch=4, n_q_heads=32, n_kv_heads=8,
+        head_dim=128, ctx=32768, ctx_lo=32768, steps=256, n_sink=4, n_window=64, n_select=1980,
+        key_model="zipf", mask_kind="geometric", mask_param=18, per_seq_mask=True,
+        trigger="tokens", seed=0x5F1000 + 6),
 }
 
 ORDER = ["gqa4_ctx4k_hh", "llama8b_ctx32k_b4", "llama8b_ctx128k_l32", "ragged_paged_b32",

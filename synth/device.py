@@ -6,7 +6,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import gpu
+from . import gen, gpu
 from .workload import HostWorkload
 
 
@@ -54,6 +54,16 @@ def fill_state_cache(wl: HostWorkload, state, on_device: bool = True, model=None
             state.k.copy_(_bf16(wl.cache_contiguous("k", state.capacity), dev))
             state.v.copy_(_bf16(wl.cache_contiguous("v", state.capacity), dev))
     return model
+
+
+def schedule(wl: HostWorkload, state, steps: int | None = None) -> np.ndarray:
+    """Slow flags [steps][B] of the workload's first `steps` decode steps, from the native
+    trigger policy: on the boundary masks, or on the generated token streams for a
+    token-triggered workload."""
+    n = wl.cfg.steps if steps is None else steps
+    if wl.cfg.trigger == "tokens":
+        return state.schedule_tokens(wl.tokens[:, :n], gen.TRIGGER_TOKENS)
+    return state.schedule(wl.masks[:, :n])
 
 
 def boundary_epochs(wl: HostWorkload, steps: int) -> np.ndarray:

@@ -19,7 +19,14 @@ class HostWorkload:
             self.len0 = np.full(B, cfg.ctx, dtype=np.int64)
         else:
             self.len0 = gen.ragged_lengths(self.key, B, cfg.ctx_lo, cfg.ctx)
-        if cfg.per_seq_mask:
+        self.tokens = None
+        if cfg.trigger == "tokens":
+            # generated token ids [B][steps]; masks[b][t] = 1 where token t is a trigger
+            ts = [gen.token_stream(self.key, cfg.steps, mean_span=cfg.mask_param,
+                                   b=b if cfg.per_seq_mask else 0) for b in range(B)]
+            self.tokens = np.stack(ts).astype(np.int32)
+            self.masks = np.isin(self.tokens, gen.TRIGGER_TOKENS).astype(np.uint8)
+        elif cfg.per_seq_mask:
             self.masks = np.stack([gen.boundary_mask(self.key, cfg.steps, cfg.mask_kind,
                                                      cfg.mask_param, b) for b in range(B)])
         else:
