@@ -53,7 +53,7 @@ def issue(wl, steps, pipeline, graph=False):
     cfg = wl.cfg
     st = sdev.make_state(wl)
     ins = sdev.DeviceInputs(wl, steps, st.k.device)
-    slow = st.schedule(wl.masks[:, :steps])
+    slow = sdev.schedule(wl, st, steps)
     out = torch.zeros((steps, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
                       dtype=torch.float32, device=st.k.device)
     run = sdev.DriftingRun(wl, st, slow, ins.q, ins.k_new, ins.v_new, out, ins.model,
@@ -86,7 +86,7 @@ def issue_stepwise(wl, steps, units, pipeline=True):
     cfg = wl.cfg
     st = sdev.make_state(wl)
     ins = sdev.DeviceInputs(wl, steps, st.k.device)
-    slow = st.schedule(wl.masks[:, :steps])
+    slow = sdev.schedule(wl, st, steps)
     out = torch.zeros((steps, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
                       dtype=torch.float32, device=st.k.device)
     run = sdev.DriftingRun(wl, st, slow, ins.q, ins.k_new, ins.v_new, out, ins.model,

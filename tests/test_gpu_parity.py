@@ -22,10 +22,13 @@ pytestmark = pytest.mark.gpu
 ATOL, RTOL = 2e-3, 1e-2
 
 
-def close(g, o):
+def close(g, o, bf16_out=False):
+    """|g - o| <= 2e-3 + 1e-2 |o|; a bf16 output also carries its own rounding, at most half
+    a bf16 ulp (2^-8 |o|), on top."""
     g = np.asarray(g, np.float64)
     o = np.asarray(o, np.float64)
-    bad = np.abs(g - o) > ATOL + RTOL * np.abs(o)
+    rtol = RTOL + (2.0 ** -8 if bf16_out else 0.0)
+    bad = np.abs(g - o) > ATOL + rtol * np.abs(o)
     return not bad.any(), float(np.abs(g - o).max())
 
 
@@ -185,48 +188,66 @@ def test_competing_heavy_positions_with_cancelling_values():
 
 # ------------------------------------------------------------------------------ fast step
 
-@pytest.mark.parametrize("fused", [True, False], ids=["fused_append", "append_then_sparse"])
-@pytest.mark.parametrize("case", [
+SPARSE_CASES = [
     dict(name="gqa4_ctx4k_hh"),
     dict(name="llama8b_ctx32k_b4", ctx=5000, batch=2),               # clusters of 8 CTAs
     dict(name="llama8b_ctx32k_b4", ctx=150, batch=2),                # n_C < K: all selected
     dict(name="llama8b_ctx32k_b4", ctx=40, batch=1),                 # window clipped at sinks
     dict(name="llama8b_ctx32k_b4", ctx=1300, batch=3, n_layers=5),   # 120 units: tile ranges
     dict(name="ragged_paged_b32", batch=4, ctx=2500, ctx_lo=700),    # paged window
-])
-def test_sparse_step_vs_oracle(case, fused):
+]
+
+
+def check_sparse_steps(case, fused, out_fp32=True, n=20, check_every=3):
     """Slow step at t=0, then fast steps: each fast output equals attention over sinks +
     the (GPU-selected) memory + the sliding window."""
     case = dict(case)
-    wl = small(case.pop("name"), steps=20, **case)
+    wl = small(case.pop("name"), steps=n, **case)
     cfg = wl.cfg
     st = sdev.make_state(wl, on_device=True)
-    n = 20
     ins = sdev.DeviceInputs(wl, n, st.k.device)
     outs = torch.zeros((n, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
-                       dtype=torch.float32, device=st.k.device)
+                       dtype=torch.float32 if out_fp32 else torch.bfloat16, device=st.k.device)
     sel = None
     for t in range(n):
         slow = np.full(cfg.batch, t == 0)
-        st.step(ins.q[t], ins.k_new[t], ins.v_new[t], slow, outs[t], fused=fused)
+        st.step(ins.q[t], ins.k_new[t], ins.v_new[t], slow, outs[t], out_fp32, fused=fused)
         if t == 0:
             torch.cuda.synchronize()
             sel = [st.sel_idx[u, :int(st.sel_cnt[u])].cpu().numpy() for u in range(st.n_units)]
     torch.cuda.synchronize()
     assert int(st.err[0]) == 0
-    outs = outs.cpu().numpy()
+    outs = outs.float().cpu().numpy()
     G, S, W = cfg.group, cfg.n_sink, cfg.n_window
     for u in range(st.n_units):
         layer, b, kvh = unit_coords(cfg, u)
         Ls = int(wl.len0[b]) + 1
         k = wl.rows("k", layer, b, kvh, np.arange(Ls + n))
         v = wl.rows("v", layer, b, kvh, np.arange(Ls + n))
-        for t in range(1, n, 3):
+        for t in range(1, n, check_every):
             rows = oracle.sparse_rows(Ls, Ls + t, S, W, sel[u])
             q = wl.query(t, layer, b)[kvh * G:(kvh + 1) * G]
             o, _ = oracle.attend(q, k, v, rows)
-            ok, err = close(outs[t, layer, b, kvh * G:(kvh + 1) * G], o)
+            ok, err = close(outs[t, layer, b, kvh * G:(kvh + 1) * G], o, bf16_out=not out_fp32)
             assert ok, f"unit {u} step {t}: sparse max err {err}"
+
+
+@pytest.mark.parametrize("fused", [True, False], ids=["fused_append", "append_then_sparse"])
+@pytest.mark.parametrize("case", SPARSE_CASES)
+def test_sparse_step_vs_oracle(case, fused):
+    check_sparse_steps(case, fused)
+
+
+@pytest.mark.parametrize("case", [
+    dict(name="llama8b_ctx32k_b4", ctx=5000, batch=2),               # clustered: merge store
+    dict(name="llama8b_ctx32k_b4", ctx=1300, batch=3, n_layers=5),   # tile ranges: store_out
+    dict(name="llama8b_ctx32k_b4", ctx=900, batch=2, n_q_heads=64),  # group 8, tile ranges
+    dict(name="ragged_paged_b32", batch=4, ctx=2500, ctx_lo=700),    # paged window
+])
+def test_sparse_step_bf16_output_vs_oracle(case):
+    """The output format the benchmark times: bf16 outputs of the fused fast step, from the
+    cluster merge and from the split-unit / whole-unit stores, against the oracle."""
+    check_sparse_steps(case, True, out_fp32=False, n=10, check_every=1)
 
 
 @pytest.mark.parametrize("case", [
@@ -269,7 +290,7 @@ def decode_on_gpu(wl, steps, on_device=True):
     cfg = wl.cfg
     st = sdev.make_state(wl, on_device=on_device)
     ins = sdev.DeviceInputs(wl, steps, st.k.device, on_device=on_device)
-    slow = st.schedule(wl.masks[:, :steps])
+    slow = sdev.schedule(wl, st, steps)
     out = torch.zeros((steps, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
                       dtype=torch.float32, device=st.k.device)
     plan = st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out)
@@ -307,37 +328,45 @@ def test_end_to_end_ragged_paged_per_sequence_schedule():
 
 def test_end_to_end_32k_batch4_sampled():
     """The 32K-context, batch-4 workload at full size through the native driver: sampled
-    units over the first steps (a slow step and the fast steps that reuse its memory)."""
+    units over the first 20 decode steps -- slow steps 0, 3 and 15 (two selection refreshes)
+    and the fast steps after each, whose window slides past the packed memory."""
     wl = HostWorkload(WORKLOADS["llama8b_ctx32k_b4"])
-    compare_run(wl, 6, units=[0, 7, 13, 31])
+    st, ref = compare_run(wl, 20, units=[0, 7, 13, 31])
+    assert np.flatnonzero(ref["slow"][0]).tolist()[:3] == [0, 3, 15]
 
 
 def test_end_to_end_128k_32_layers_sampled():
     """The 128K-context, 32-layer workload at full size (17 GB of KV): sampled units over
-    the first decode steps."""
+    the first 31 decode steps -- slow steps 0, 26 and 29; the fast steps before step 26 run
+    with a window 25 positions past the packed memory."""
     wl = HostWorkload(WORKLOADS["llama8b_ctx128k_l32"])
-    compare_run(wl, 4, units=[0, 8 * 17 + 5, 8 * 31 + 7])
+    st, ref = compare_run(wl, 31, units=[0, 8 * 17 + 5, 8 * 31 + 7],
+                          check_steps=list(range(0, 6)) + list(range(20, 31)))
+    assert np.flatnonzero(ref["slow"][0]).tolist()[:3] == [0, 26, 29]
 
 
 def test_end_to_end_ragged_paged_full_size_sampled():
     """The ragged batch-32 paged workload at full size: sampled units (different sequence
-    lengths and per-sequence schedules) over the first decode steps."""
+    lengths and per-sequence schedules) over the first 24 decode steps (sequence 0 refreshes
+    its selection at steps 3, 9 and 21)."""
     wl = HostWorkload(WORKLOADS["ragged_paged_b32"])
-    compare_run(wl, 8, units=[0, 8 * 5 + 3, 8 * 17 + 1, 8 * 31 + 7])
+    compare_run(wl, 24, units=[0, 8 * 5 + 3, 8 * 17 + 1, 8 * 31 + 7])
 
 
 def test_end_to_end_longcot_full_size_sampled():
     """The long-CoT workload at full size (32 layers, batch 8, 128K context, 137 GB of KV,
     window 128, budget 1916, heavy hitters re-seeded at every boundary), issued in segments
     with the key edits between them exactly as the benchmark does: sampled units over the
-    first decode steps."""
+    first 12 decode steps, across the first heavy-hitter drift and the selection refresh it
+    triggers."""
     torch.cuda.empty_cache()
     wl = HostWorkload(WORKLOADS["longcot_ctx128k_b8_l32"])
     cfg = wl.cfg
-    steps = 6
+    steps = 12                   # slow steps 0 and 7; the heavy hitters drift at step 7
+    assert sdev.boundary_epochs(wl, steps).tolist() == [0] * 7 + [1] * 5
     st = sdev.make_state(wl)
     ins = sdev.DeviceInputs(wl, steps, st.k.device)
-    slow = st.schedule(wl.masks[:, :steps])
+    slow = sdev.schedule(wl, st, steps)
     out = torch.zeros((steps, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
                       dtype=torch.float32, device=st.k.device)
     sdev.DriftingRun(wl, st, slow, ins.q, ins.k_new, ins.v_new, out, ins.model).issue()
@@ -367,7 +396,7 @@ def test_end_to_end_drifting_heavy_hitters():
     assert wl.n_epochs() > 3
     st = sdev.make_state(wl)
     ins = sdev.DeviceInputs(wl, cfg.steps, st.k.device)
-    slow = st.schedule(wl.masks)
+    slow = sdev.schedule(wl, st)
     out = torch.zeros((cfg.steps, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
                       dtype=torch.float32, device=st.k.device)
     sdev.DriftingRun(wl, st, slow, ins.q, ins.k_new, ins.v_new, out, ins.model).issue()
@@ -381,6 +410,34 @@ def test_end_to_end_drifting_heavy_hitters():
             layer, b, kvh = unit_coords(cfg, u)
             ok, err = close(got[t, layer, b, kvh * G:(kvh + 1) * G], ref["out"][t][u])
             assert ok, f"step {t} unit {u}: max err {err}"
+
+
+def test_end_to_end_token_triggered_schedule():
+    """Trigger policy on generated tokens (gist.science technical summary, section 2C): every
+    sequence has its own seeded token stream, and a slow step follows a trigger token ('.',
+    '?', '!', newline) or T_max steps without one. The GPU run is scheduled by the native
+    sfi_schedule_tokens and issued by sfi_decode_run (mixed slow/fast steps); the oracle
+    replays the same run with its own token rule. Scaled-down 32K batch-4 workload, every
+    unit and step."""
+    wl = small("llama8b_ctx32k_b4_tok", ctx=2600, steps=60, mask_param=6)
+    assert wl.tokens is not None
+    st, slow, out = decode_on_gpu(wl, 60)
+    ref = odecode.run(wl, steps=60)
+    assert np.array_equal(ref["slow"].T, slow)
+    assert (slow.any(axis=1) & ~slow.all(axis=1)).sum() >= 5      # mixed steps
+    G = wl.cfg.group
+    for t in range(60):
+        for u in range(st.n_units):
+            layer, b, kvh = unit_coords(wl.cfg, u)
+            ok, err = close(out[t, layer, b, kvh * G:(kvh + 1) * G], ref["out"][t][u])
+            assert ok, f"step {t} unit {u}: max err {err}"
+
+
+def test_end_to_end_token_triggered_full_size_sampled():
+    """The token-triggered 32K batch-4 workload at full size: sampled units of all four
+    sequences over the first 20 decode steps (their own token-driven schedules)."""
+    wl = HostWorkload(WORKLOADS["llama8b_ctx32k_b4_tok"])
+    compare_run(wl, 20, units=[0, 8 + 3, 16 + 5, 24 + 7])
 
 
 # ------------------------------------------------------------------------------ error paths
