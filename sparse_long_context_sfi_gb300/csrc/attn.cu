@@ -61,17 +61,17 @@ struct Ctrl {
     uint64_t s_full[2], s_free[2], p_full[2], o_full[2], o_free[2], q_free[2];
     uint64_t gsync;             // softmax-group barrier (one arrive per warp)
     uint64_t drain;             // MMA drain on exit
-    uint64_t unit_meta;         // clustered: this CTA's unit and tile slice are known
+    uint64_t unit_meta;         // clustered: the unit's length and activity are known
     uint64_t cl_ready;          // clustered: every CTA of the cluster has its partial in place
-    uint64_t app_ready;         // clustered, fused append: the new row is in the cache
+    uint64_t q_full;            // clustered: the query has landed
+    uint64_t meta_full[kStages];  // clustered: the stage's TileMeta (row mask) is written
     TileMeta meta[kStages];
     float red_max[2][4][8];
     float red_sum[4][8];
     uint32_t tmem_base;
     int abort;
     int last_flag;
-    int cl_tiles, cl_t0, cl_live, cl_rows, cl_sel;  // clustered: slice of the unit's tiles
-    int cl_app_tile;            // clustered, fused append: tile holding the new row, or -1
+    int cl_live;                // clustered: the unit is active and its length valid
     int P;
     long long T, TL, g0, g1;
     int nt[kMaxBatch];
@@ -81,12 +81,15 @@ struct Ctrl {
 
 constexpr int kSmemBytes = kCtrlOff + static_cast<int>(sizeof(Ctrl)) + 1024;
 
+// Warp-wide max of non-NaN floats in one redux: the float bits as a signed integer, with the
+// magnitude bits of negatives flipped, order like the floats (-inf lowest, -0 below +0).
 __device__ __forceinline__ float warp_max(float x)
 {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-    return x;
+    int k = __float_as_int(x);
+    k ^= (k >> 31) & 0x7fffffff;
+    int m = __reduce_max_sync(0xffffffffu, k);
+    m ^= (m >> 31) & 0x7fffffff;
+    return __int_as_float(m);
 }
 
 __device__ __forceinline__ float warp_sum(float x)
@@ -196,7 +199,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_init(&c.gsync, 4);
         mbar_init(&c.drain, 1);
         mbar_init(&c.unit_meta, 1);
-        mbar_init(&c.app_ready, 1);
+        mbar_init(&c.q_full, 1);
+        for (int s = 0; s < kStages; ++s)
+            mbar_init(&c.meta_full[s], 1);
         mbar_init(&c.cl_ready, static_cast<uint32_t>(p.cluster > 1 ? p.cluster : 1));
         mbar_fence_init();
         tma_prefetch_map(&tm_k);
@@ -208,7 +213,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         c.abort = 0;
         c.cl_live = 0;
-        c.cl_app_tile = -1;
     }
     if (warp == 1) {
         tmem_alloc(&c.tmem_base, kTmemCols);
@@ -226,9 +230,134 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     constexpr bool clustered = !DENSE && CL;
     const bool fused = !DENSE && p.k_new != nullptr;
     if (clustered) {
+        // arrive now, wait only before the first access to a peer's shared memory (the merge)
         tc_fence_before();
-        cluster_sync_all();
+        cluster_arrive_release();
+        __syncthreads();
         tc_fence_after();
+    }
+
+    // Clustered fast step: this CTA's unit and its static slice [cl_t0, cl_t0 + cl_n) of the
+    // unit's tiles (the MMA and softmax roles iterate over the whole slice; a unit found
+    // inactive only gets empty tiles and no output). Producer state: the unit's packed row
+    // count cl_rows and packed sinks cl_ns, and cl_i, the next tile of the slice to publish.
+    int cl_u = 0, cl_t0 = 0, cl_n = 0, cl_rows = 0, cl_ns = 0, cl_i = 0, cl_pre = 0;
+    if (clustered) {
+        cl_u = static_cast<int>(blockIdx.x) / p.cluster;
+        const int rank = static_cast<int>(blockIdx.x) % p.cluster;
+        cl_t0 = rank * p.tiles_per_unit / p.cluster;
+        cl_n = (rank + 1) * p.tiles_per_unit / p.cluster - cl_t0;
+    }
+    // Tile t of the slice in ring stage i % kStages (producer warp, clustered): its row mask
+    // is written and published on meta_full (what the softmax waits for), and with `issue`
+    // its boxes are requested on full (what the MMA waits for): the packed rows below
+    // cl_rows in 64-row boxes, and with `win` the window boxes of a sequence of length L
+    // whose window starts at ws (wpg: the page of this lane's window box, paged cache).
+    auto cl_tile = [&](int i, int t, bool win, int L, int ws, int wpg, bool issue) {
+        const int s = i % kStages;
+        const int h2 = lane >> 4, j16 = lane & 15, op = lane & 3;
+        const int R = t * kTile + 64 * h2;
+        const CUtensorMap *map = nullptr;
+        int y = 0, row0 = 0, rows = 0, kv = 0, half = 0;
+        uint32_t valid[4] = {0u, 0u, 0u, 0u};
+        if (R < 64 * p.n_cbox) {
+            const int k = R >> 6;
+            const int vr = max(0, min(64, cl_rows - 64 * k));
+            if (vr > 0 && j16 < 4) {
+                kv = j16 >> 1;
+                half = j16 & 1;
+                map = kv ? &tm_vc : &tm_kc;
+                y = cl_u * p.comp_cap + 64 * k;
+                row0 = 64 * h2;
+                rows = 64;
+                if (j16 == 0)
+                    mask_rows(valid, row0, row0 + vr);
+            }
+        } else if (win) {
+            const int q = j16 >> 2;
+            const int j = (R + 16 * q - 64 * p.n_cbox) >> 4;
+            const int rr0 = 64 * h2 + 16 * q;
+            if (j < p.n_wbox && p.page_size == 0) {
+                const int p0 = ws + 16 * j;
+                const int vr = max(0, min(16, L - p0));
+                if (vr > 0) {
+                    kv = op >> 1;
+                    half = op & 1;
+                    map = kv ? &tm_v : &tm_k;
+                    y = cl_u * p.capacity + p0;
+                    row0 = rr0;
+                    rows = 16;
+                    if (op == 0)
+                        mask_rows(valid, rr0, rr0 + vr);
+                }
+            } else if (j < p.n_wbox) {
+                const int lp = (ws >> 4) + j;
+                const int r0 = max(ws - lp * 16, 0), r1 = min(L - lp * 16, 16);
+                if (r1 > r0) {
+                    const int b = (cl_u / Hkv) % B, layer = cl_u / (Hkv * B), kvh = cl_u % Hkv;
+                    const int page = p.n_wbox <= 32 ? wpg : __ldg(p.page_table + b * p.max_pages + lp);
+                    if (page < 0 || page >= p.n_pages) {
+                        if (op == 0)
+                            raise_error(p.err, 0x1u);  // SFI_DEVERR_PAGE_RANGE
+                    } else {
+                        kv = op >> 1;
+                        half = op & 1;
+                        map = kv ? &tm_v : &tm_k;
+                        y = ((layer * p.n_pages + page) * Hkv + kvh) * 16;
+                        row0 = rr0;
+                        rows = 16;
+                        if (op == 0)
+                            mask_rows(valid, rr0 + r0, rr0 + r1);
+                    }
+                }
+            }
+        }
+        uint32_t vw[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+            vw[w] = __reduce_or_sync(0xffffffffu, valid[w]);
+        // test hook: CTA 0's first tile expects 16 bytes that never come (sfi_test_inject_stall)
+        const uint32_t bytes = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(rows) * 128u) +
+                               ((p.test_stall && blockIdx.x == 0 && i == 0) ? 16u : 0u);
+        if (lane == 0) {
+            TileMeta &mt = c.meta[s];
+            mt.unit = cl_u;
+            mt.tile = t;
+            mt.flags = (i == 0 ? kFlagFirst : 0) | (i == cl_n - 1 ? kFlagLast : 0);
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+                mt.valid[w] = vw[w];
+            mbar_arrive(&c.meta_full[s]);  // releases the metadata
+            if (issue)
+                mbar_arrive_expect_tx(&c.full[s], bytes);
+        }
+        __syncwarp();
+        if (issue && rows > 0)
+            tma_load_2d(smem + s * kStageBytes + kv * 2 * kChunkBytes + half * kChunkBytes + row0 * 128,
+                        map, &c.full[s], 64 * half, y);
+    };
+    // The packed memory is complete before this launch starts (sfi_compact and sfi_select let
+    // their dependents start only after their writes), so the slice's first tiles of packed
+    // rows are requested before the wait on the preceding grid: every box of them, since the
+    // unit's packed row count is known only after the wait (rows past it are masked then).
+    // Their arrival on full lets the score MMAs start as soon as the query lands.
+    if (clustered && warp == 0) {
+        const int packed_tiles = 64 * p.n_cbox / kTile;   // tiles of packed rows only
+        cl_pre = max(0, min(min(kStages, cl_n), packed_tiles - cl_t0));
+        const int h2 = lane >> 4, j16 = lane & 15;
+        for (int i = 0; i < cl_pre; ++i) {
+            if (lane == 0)
+                mbar_arrive_expect_tx(&c.full[i], 4u * 2u * 64u * 128u +
+                                                      ((p.test_stall && blockIdx.x == 0 && i == 0) ? 16u : 0u));
+            __syncwarp();
+            if (j16 < 4) {
+                const int k = ((cl_t0 + i) * kTile + 64 * h2) >> 6;
+                const int kv = j16 >> 1, half = j16 & 1;
+                tma_load_2d(smem + i * kStageBytes + kv * 2 * kChunkBytes + half * kChunkBytes +
+                                64 * h2 * 128,
+                            kv ? &tm_vc : &tm_kc, &c.full[i], 64 * half, cl_u * p.comp_cap + 64 * k);
+            }
+        }
     }
 
     // ---- tile space: per-sequence tile counts and this CTA's range --------------------
@@ -271,94 +400,170 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         g1 = c.g1;
         n_tiles = static_cast<int>(blockIdx.x) < c.P ? static_cast<int>(g1 - g0) : 0;
     } else {
-        // The producer warp reads the unit's length, flag, packed rows and selection count
-        // in one round and publishes them; the other roles wait for that.
-        if (warp == 0) {
-            const int u = static_cast<int>(blockIdx.x) / p.cluster;
-            const int rank = static_cast<int>(blockIdx.x) % p.cluster;
-            const int b = (u / Hkv) % B;
-            int v = 0;
-            if (lane == 0)
-                v = p.seq_len[b];
-            else if (lane == 1)
-                v = p.active ? p.active[b] : 1;
-            else if (lane == 2)
-                v = p.comp_rows[u];
-            else if (lane == 3)
-                v = p.sel_cnt[u];
-            const int L0 = __shfl_sync(0xffffffffu, v, 0);
-            const int act = __shfl_sync(0xffffffffu, v, 1);
-            const int rows = __shfl_sync(0xffffffffu, v, 2);
-            const int sel = __shfl_sync(0xffffffffu, v, 3);
-            const int L = fused ? L0 + 1 : L0;
-            bool live = act != 0;
-            if (live && (L0 < 0 || L0 > p.max_len || L > p.capacity)) {
-                if (lane == 0)
-                    raise_error(p.err, 0x8u);  // SFI_DEVERR_LENGTH
-                live = false;
-            }
-            live = live && L > 0;
-            if (lane == 0) {
-                const int nt = p.tiles_per_unit, C = p.cluster;
-                const int t0 = rank * nt / C, t1 = (rank + 1) * nt / C;
-                c.cl_t0 = t0;
-                c.cl_tiles = live ? t1 - t0 : 0;
-                c.cl_live = live ? 1 : 0;
-                c.cl_rows = rows;
-                c.cl_sel = sel;
-                c.len[0] = L;
-                // the tile of the unit's window that holds the new row (position L - 1)
-                int app = -1;
-                if (fused && live) {
-                    const int rows_c = max(0, min(rows, p.comp_cap));
-                    const int n_s = max(0, rows_c - max(0, sel));
-                    const int ws = max(n_s, L - p.n_window);
-                    const int jn = p.page_size == 0 ? ((L - 1 - ws) >> 4) : (((L - 1) >> 4) - (ws >> 4));
-                    const int t_new = (64 * p.n_cbox + 16 * jn) / kTile;
-                    app = (t_new >= t0 && t_new < t1) ? t_new : -1;
-                }
-                c.cl_app_tile = app;
-                mbar_arrive(&c.unit_meta);
-            }
-        }
-        if (mbar_wait(&c.unit_meta, 0, &c.abort)) {
-            n_tiles = c.cl_tiles;
-            g0 = c.cl_t0;
-            g1 = g0 + n_tiles;
-        } else {
-            fail(c, p.err);
-        }
+        n_tiles = cl_n;
+        g0 = cl_t0;
+        g1 = g0 + n_tiles;
     }
     const uint32_t tmem = c.tmem_base;
 
-    if (warp == 0) {
+    if (warp == 0 && clustered) {
+        // ========================= TMA producer, clustered fast step =======================
+        // After the wait: the query first (its own barrier: it may come from the preceding
+        // kernel), then the unit's length, activity and packed counts in one round, then the
+        // row masks of the tiles requested before the wait and the rest of the slice; the
+        // window tile gets the new row written into the cache (fused append) before its boxes
+        // are issued.
+        const int layer = cl_u / (Hkv * B), b = (cl_u / Hkv) % B, kvh = cl_u % Hkv;
+        if (lane == 0)
+            mbar_arrive_expect_tx(&c.q_full, 2u * G * 128u);
+        __syncwarp();
+        if (lane < 2)
+            tma_load_2d(smem + kQOff + lane * kOpChunk, &tm_q, &c.q_full, 64 * lane, cl_u * G);
+        int v = 0;
+        if (lane == 0)
+            v = p.seq_len[b];
+        else if (lane == 1)
+            v = p.active ? p.active[b] : 1;
+        else if (lane == 2)
+            v = __ldg(p.comp_rows + cl_u);
+        else if (lane == 3)
+            v = __ldg(p.sel_cnt + cl_u);
+        const int L0 = __shfl_sync(0xffffffffu, v, 0);
+        const int act = __shfl_sync(0xffffffffu, v, 1);
+        const int v2 = __shfl_sync(0xffffffffu, v, 2), v3 = __shfl_sync(0xffffffffu, v, 3);
+        cl_rows = max(0, min(v2, p.comp_cap));
+        cl_ns = max(0, cl_rows - max(0, v3));
+        const int L = fused ? L0 + 1 : L0;  // with the fused append: the new row included
+        bool live = act != 0;
+        if (live && (L0 < 0 || L0 > p.max_len || L > p.capacity)) {
+            if (lane == 0)
+                raise_error(p.err, 0x8u);  // SFI_DEVERR_LENGTH
+            live = false;
+        }
+        live = live && L > 0;
+        const int ws = max(cl_ns, L - p.n_window);
+        // paged: the page of every window box, one per lane (up to 32 boxes)
+        const bool wpf = p.page_size != 0 && p.n_wbox <= 32;
+        int wpage = 0;
+        if (live && wpf) {
+            const int lp = (ws >> 4) + lane;
+            wpage = (lane < p.n_wbox && lp * 16 < L) ? __ldg(p.page_table + b * p.max_pages + lp) : 0;
+        }
+        // The tile of this slice that holds the new row (position L - 1), if any: the window
+        // tile that reads it; a row outside the window (only in an inconsistent sparse state)
+        // is still written once, by the unit's first tile.
+        int app = -1, jn = 0;
+        if (fused && live) {
+            jn = p.page_size == 0 ? ((L - 1 - ws) >> 4) : (((L - 1) >> 4) - (ws >> 4));
+            const int t_new = L - 1 >= ws ? (64 * p.n_cbox + 16 * jn) / kTile : 0;
+            app = (t_new >= cl_t0 && t_new < cl_t0 + cl_n) ? t_new : -1;
+        }
+        if (lane == 0) {
+            c.cl_live = live ? 1 : 0;
+            mbar_arrive(&c.unit_meta);
+        }
+        // Fused append: the new K and V rows go to position L - 1, 16 bytes per lane (lanes
+        // 0-15 K, 16-31 V); each lane fences its write against the async proxy and the warp
+        // synchronises before the box covering the row is issued.
+        auto append_new_row = [&]() {
+            const int pos = L - 1;
+            long long row = static_cast<long long>(cl_u) * p.capacity + pos;
+            bool good = true;
+            if (p.page_size != 0) {
+                int page = __shfl_sync(0xffffffffu, wpage, max(0, min(jn, 31)));
+                if (!wpf || jn < 0 || jn >= p.n_wbox)
+                    page = __ldg(p.page_table + b * p.max_pages + (pos >> 4));
+                good = page >= 0 && page < p.n_pages;
+                if (!good && lane == 0)
+                    raise_error(p.err, 0x1u);  // SFI_DEVERR_PAGE_RANGE
+                row = ((static_cast<long long>(layer) * p.n_pages + page) * Hkv + kvh) * 16 + (pos & 15);
+            }
+            if (good) {
+                const int kvsel = lane >> 4, chunk = lane & 15;
+                const uint4 x = static_cast<const uint4 *>(kvsel ? p.v_new : p.k_new)
+                    [static_cast<size_t>(cl_u) * 16 + chunk];
+                static_cast<uint4 *>(kvsel ? p.v_cache : p.k_cache)[row * 16 + chunk] = x;
+                fence_proxy_async_global();
+            }
+            __syncwarp();
+        };
+        // masks of the tiles requested before the wait (packed rows only)
+        for (; cl_i < cl_pre; ++cl_i)
+            cl_tile(cl_i, cl_t0 + cl_i, false, 0, 0, 0, false);
+        if (app >= 0 && app < cl_t0 + cl_i)   // its tile was requested before the wait
+            append_new_row();
+        bool ok = true;
+        for (; cl_i < cl_n; ++cl_i) {
+            const int st = cl_i % kStages, t = cl_t0 + cl_i;
+            if (lane == 0)
+                ok = mbar_wait(&c.empty[st], ((cl_i / kStages) & 1) ^ 1, &c.abort);
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+                if (lane == 0)
+                    fail(c, p.err);
+                break;
+            }
+            const bool has_win = live && (t + 1) * kTile > 64 * p.n_cbox;
+            int wpg = 0;
+            if (has_win && wpf) {
+                const int jl = (t * kTile + 64 * (lane >> 4) + 16 * ((lane & 15) >> 2) -
+                                64 * p.n_cbox) >> 4;
+                wpg = __shfl_sync(0xffffffffu, wpage, jl & 31);
+            }
+            if (t == app)
+                append_new_row();
+            cl_tile(cl_i, t, has_win, L, ws, wpg, true);
+        }
+        // Never leave a copy in flight into shared memory we are about to give up.
+        if (lane == 0) {
+            for (int j = max(0, cl_i - kStages); j < cl_i; ++j)
+                mbar_wait(&c.full[j % kStages], (j / kStages) & 1, nullptr);
+            mbar_wait(&c.q_full, 0, nullptr);
+        }
+        // Fused append: the last CTA of the grid to get here advances the lengths.
+        if (fused) {
+            int is_last = 0;
+            if (lane == 0)
+                is_last = atomic_add_acq_rel_gpu(p.append_counter, 1) == static_cast<int>(gridDim.x) - 1;
+            if (__shfl_sync(0xffffffffu, is_last, 0)) {
+                int32_t *len = const_cast<int32_t *>(p.seq_len);
+                for (int bb = lane; bb < B; bb += 32) {
+                    const int Lb = len[bb];
+                    const int ab = p.active ? p.active[bb] : 1;
+                    if (ab && Lb >= 0 && Lb <= p.max_len && Lb + 1 <= p.capacity)
+                        len[bb] = Lb + 1;
+                }
+                if (lane == 0)
+                    *p.append_counter = 0;
+            }
+        }
+    } else if (warp == 0) {
         // =============================== TMA producer ===================================
         // The whole warp runs the loop; each lane issues at most one TMA box per tile (a
         // 64-column half of K or V for one page / block of rows), and lane 0 publishes the
         // tile with a single arrive.expect_tx of the warp's summed bytes.
+        int issued = 0;
         if (n_tiles > 0) {
             const uint64_t pol = policy_evict_first();
             // decode the first tile of the range
             long long g = g0;
-            int layer, b, kvh, t;
-            if (clustered) {  // a slice of one unit's tiles
-                const int u0 = static_cast<int>(blockIdx.x) / p.cluster;
-                layer = u0 / (Hkv * B);
-                b = (u0 / Hkv) % B;
-                kvh = u0 % Hkv;
-                t = static_cast<int>(g0);
-            } else {
-                layer = static_cast<int>(g / c.TL);
+            int layer = static_cast<int>(g / c.TL), b = 0, kvh, t;
+            {
                 const int r = static_cast<int>(g - static_cast<long long>(layer) * c.TL);
-                b = 0;
                 while (b + 1 < B && (c.nt[b] == 0 || c.pre[b] + Hkv * c.nt[b] <= r))
                     ++b;
                 kvh = (r - c.pre[b]) / c.nt[b];
                 t = (r - c.pre[b]) - kvh * c.nt[b];
             }
-            auto ntiles_of = [&](int bb) { return clustered ? p.tiles_per_unit : c.nt[bb]; };
-            int seg = -1, issued = 0;
+            auto ntiles_of = [&](int bb) { return c.nt[bb]; };
+            int seg = -1;
             int seg_len = 0, seg_rows_c = 0, seg_ws = 0;
+            // Sparse step: per-segment values loaded ahead of use, so the producer does not
+            // wait on global memory at the tile that needs them. Lanes 0 and 1 hold the packed
+            // row count and selection count of the current (cur_meta) and the next (nxt_meta)
+            // segment, the next loaded when the current one starts; lane j < n_wbox holds the
+            // page of window box j of the current segment (paged cache, up to 32 boxes).
+            int cur_meta = 0, nxt_meta = 0, wpage = 0, app_page = 0;
+            const bool wpage_pf = !DENSE && p.page_size != 0 && p.n_wbox <= 32;
             const int my_q = lane >> 2, my_op = lane & 3;  // page / block and (K|V, half)
             // paged dense tiles: this lane's page id, loaded one tile ahead
             const bool paged_dense = DENSE && p.page_size != 0;
@@ -381,7 +586,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (p.page_size == 0) {
                     row = static_cast<long long>(uu) * p.capacity + pos;
                 } else {
-                    const int page = __ldg(p.page_table + bb * p.max_pages + (pos >> 4));
+                    const int page = wpage_pf ? app_page
+                                              : __ldg(p.page_table + bb * p.max_pages + (pos >> 4));
                     good = page >= 0 && page < p.n_pages;
                     if (!good && lane == 0)
                         raise_error(p.err, 0x1u);  // SFI_DEVERR_PAGE_RANGE
@@ -422,23 +628,56 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     ++seg;
                     if (lane == 0 && ok && seg >= 2)
                         ok = mbar_wait(&c.q_free[seg & 1], ((seg >> 1) - 1) & 1, &c.abort);
-                    seg_len = clustered ? c.len[0] : c.len[b];
+                    seg_len = c.len[b];
                     if (!DENSE) {
-                        const int rows_c = max(0, min(clustered ? c.cl_rows : __ldg(p.comp_rows + u),
-                                                      p.comp_cap));
-                        const int n_s = max(0, rows_c - max(0, clustered ? c.cl_sel : __ldg(p.sel_cnt + u)));
+                        int rows_c, sel;
+                        {
+                            cur_meta = seg == 0 ? (lane == 0 ? __ldg(p.comp_rows + u)
+                                                   : lane == 1 ? __ldg(p.sel_cnt + u) : 0)
+                                                : nxt_meta;
+                            // the next segment of the range, if any: its counts, loaded now
+                            if (i + (ntiles_of(b) - t) < n_tiles) {
+                                int nl = layer, nb = b, nk = kvh;
+                                if (++nk == Hkv) {
+                                    nk = 0;
+                                    do {
+                                        if (++nb == B) {
+                                            nb = 0;
+                                            ++nl;
+                                        }
+                                    } while (ntiles_of(nb) == 0);
+                                }
+                                const int un = (nl * B + nb) * Hkv + nk;
+                                nxt_meta = lane == 0 ? __ldg(p.comp_rows + un)
+                                                     : lane == 1 ? __ldg(p.sel_cnt + un) : 0;
+                            }
+                            rows_c = __shfl_sync(0xffffffffu, cur_meta, 0);
+                            sel = __shfl_sync(0xffffffffu, cur_meta, 1);
+                        }
+                        rows_c = max(0, min(rows_c, p.comp_cap));
+                        const int n_s = max(0, rows_c - max(0, sel));
                         seg_rows_c = rows_c;
                         seg_ws = max(n_s, seg_len - p.n_window);
+                        if (wpage_pf) {
+                            const int lp = (seg_ws >> 4) + lane;
+                            wpage = (lane < p.n_wbox && lp * 16 < seg_len)
+                                        ? __ldg(p.page_table + b * p.max_pages + lp) : 0;
+                        }
                     }
                     if (fused) {
                         const int Ln = seg_len - 1;  // position of the new row
                         const int jn = p.page_size == 0 ? ((Ln - seg_ws) >> 4)
                                                         : ((Ln >> 4) - (seg_ws >> 4));
+                        if (wpage_pf) {
+                            app_page = __shfl_sync(0xffffffffu, wpage, max(0, min(jn, 31)));
+                            // the new row outside the window (a sequence no longer than its
+                            // sinks): look its page up directly
+                            if ((jn < 0 || jn >= min(p.n_wbox, 32)) && Ln >= 0)
+                                app_page = __ldg(p.page_table + b * p.max_pages + (Ln >> 4));
+                        }
                         const int t_new = (64 * p.n_cbox + 16 * jn) / kTile;
                         const int t_end = min(ntiles_of(b) - 1, t + (n_tiles - 1 - i));
                         app_tile = (seg_len >= 1 && t_new >= t && t_new <= t_end) ? t_new : -1;
-                        if (clustered)
-                            app_tile = c.cl_app_tile;
                         appended = false;
                     }
                 }
@@ -448,6 +687,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     break;
                 }
                 const int L = seg_len;
+                // page of this lane's window box, from the segment's prefetch (all lanes take
+                // part in the shuffle; lanes without a window box ignore the value)
+                int wpg = 0;
+                if (wpage_pf && (t + 1) * kTile > 64 * p.n_cbox) {   // a tile with window boxes
+                    const int jl = (t * kTile + 64 * (lane >> 4) + 16 * ((lane & 15) >> 2) -
+                                    64 * p.n_cbox) >> 4;
+                    wpg = __shfl_sync(0xffffffffu, wpage, jl & 31);
+                }
                 // ---- this lane's box ----------------------------------------------------
                 const CUtensorMap *map = nullptr;
                 int y = 0, row0 = 0, rows = 0, kv = 0, half = 0;
@@ -518,7 +765,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             const int r0 = max(seg_ws - lp * 16, 0);
                             const int r1 = min(L - lp * 16, 16);
                             if (r1 > r0) {
-                                const int page = __ldg(p.page_table + b * p.max_pages + lp);
+                                const int page = wpage_pf ? wpg
+                                                          : __ldg(p.page_table + b * p.max_pages + lp);
                                 if (page < 0 || page >= p.n_pages) {
                                     if (my_op == 0)
                                         raise_error(p.err, 0x1u);
@@ -537,18 +785,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                 }
                 if (fused && app_tile == t && !appended) {  // this tile holds the new row
-                    if (clustered) {  // written by softmax warp 2 at the start: wait for it
-                        bool w = true;
-                        if (lane == 0)
-                            w = mbar_wait(&c.app_ready, 0, &c.abort);
-                        if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) {
-                            if (lane == 0)
-                                fail(c, p.err);
-                            break;
-                        }
-                    } else {
-                        append_row(u, layer, b, kvh, L - 1);
-                    }
+                    append_row(u, layer, b, kvh, L - 1);
                     appended = true;
                 }
                 // ---- publish the tile, then issue ---------------------------------------
@@ -586,7 +823,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     else
                         tma_load_2d(dst, map, bar, 64 * half, y);
                 }
-                if (fused && !clustered && app_tile >= 0 && !appended) {  // a later tile holds it
+                if (fused && app_tile >= 0 && !appended) {  // a later tile holds it
                     append_row(u, layer, b, kvh, L - 1);
                     appended = true;
                 }
@@ -605,11 +842,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     load_page(nb, nt2);
                 }
             }
-            // Never leave a copy in flight into shared memory we are about to give up.
-            if (lane == 0)
-                for (int j = max(0, issued - kStages); j < issued; ++j)
-                    mbar_wait(&c.full[j % kStages], (j / kStages) & 1, nullptr);
         }
+        // Never leave a copy in flight into shared memory we are about to give up.
+        if (lane == 0)
+            for (int j = max(0, issued - kStages); j < issued; ++j)
+                mbar_wait(&c.full[j % kStages], (j / kStages) & 1, nullptr);
         // Fused append: this CTA has read seq_len (set-up); the last CTA of the grid to get
         // here advances the length of every sequence whose new row was appended.
         if (fused) {
@@ -644,9 +881,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 bool prog = false;
                 if (ns < n_tiles) {
                     const int s = ns % kStages, bb = ns & 1, use = ns >> 1;
+                    // (clustered: the query has its own barrier, awaited before the first S)
                     if (mbar_test_wait(&c.full[s], (ns / kStages) & 1) &&
-                        mbar_test_wait(&c.s_free[bb], (use & 1) ^ 1)) {
-                        const int flags = c.meta[s].flags;
+                        mbar_test_wait(&c.s_free[bb], (use & 1) ^ 1) &&
+                        (!clustered || ns > 0 || mbar_test_wait(&c.q_full, 0))) {
+                        // clustered: the row masks may still be in flight; the flags are static
+                        const int flags = clustered ? ((ns == 0 ? kFlagFirst : 0) |
+                                                       (ns == n_tiles - 1 ? kFlagLast : 0))
+                                                    : c.meta[s].flags;
                         if (flags & kFlagFirst)
                             ++seg;
                         tc_fence_after();
@@ -733,35 +975,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             fin_le[h] = 0.f;
         }
 
-        if (clustered && fused && warp == 2 && c.cl_app_tile >= 0) {
-            // Clustered fused append, off the producer's path: the unit's new K and V rows go
-            // to cache position L - 1 (16 bytes per lane: lanes 0-15 K, 16-31 V); each lane
-            // fences its write against the async proxy before the warp signals app_ready, on
-            // which the producer waits before loading the box that covers the row.
-            const int u = static_cast<int>(blockIdx.x) / p.cluster;
-            const int b = (u / Hkv) % B, layer = u / (Hkv * B), kvh = u % Hkv;
-            const int pos = c.len[0] - 1;
-            long long r = static_cast<long long>(u) * p.capacity + pos;
-            bool good = true;
-            if (p.page_size != 0) {
-                const int page = __ldg(p.page_table + b * p.max_pages + (pos >> 4));
-                good = page >= 0 && page < p.n_pages;
-                if (!good && lane == 0)
-                    raise_error(p.err, 0x1u);  // SFI_DEVERR_PAGE_RANGE
-                r = ((static_cast<long long>(layer) * p.n_pages + page) * Hkv + kvh) * 16 + (pos & 15);
-            }
-            if (good) {
-                const int kvsel = lane >> 4, chunk = lane & 15;
-                const uint4 x = static_cast<const uint4 *>(kvsel ? p.v_new : p.k_new)
-                    [static_cast<size_t>(u) * 16 + chunk];
-                static_cast<uint4 *>(kvsel ? p.v_cache : p.k_cache)[r * 16 + chunk] = x;
-                fence_proxy_async_global();
-            }
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&c.app_ready);
-        }
-
         auto finalize = [&](int u, const float (&fm)[G], const float (&fle)[G]) -> bool {
             const int kvh = u % Hkv, b = (u / Hkv) % B, layer = u / (Hkv * B);
             const long long su = layer * c.TL + c.pre[b] + static_cast<long long>(kvh) * c.nt[b];
@@ -809,7 +1022,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (!c.last_flag)
                 return true;
             // One-pass online merge starting from this CTA's own partial (in registers);
-            // the other contributors are read four at a time so their loads overlap.
+            // the other contributors are read in batches (8 for groups up to 4, else 4) so
+            // that their loads overlap: a unit split over ~20 CTAs then takes 3 rounds of
+            // L2 latency instead of 5.
+            constexpr int kMB = G <= 4 ? 8 : 4;
             float M[G], Le[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) {
@@ -819,11 +1035,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             // u may be the last segment of cf's range (slot 1)
             const bool cf_tail = static_cast<long long>(cf) * T / P < su;
-            for (int c0 = cf; c0 <= cl; c0 += 4) {
-                float mc[4][G], lc[4][G], ac[4][G];
-                bool use[4];
+            for (int c0 = cf; c0 <= cl; c0 += kMB) {
+                float mc[kMB][G], lc[kMB][G], ac[kMB][G];
+                bool use[kMB];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < kMB; ++k) {
                     const int cc = c0 + k;
                     use[k] = cc <= cl && cc != static_cast<int>(blockIdx.x);
                     const int sl = (cc == cf && cf_tail) ? 1 : 0;
@@ -838,7 +1054,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                 }
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < kMB; ++k) {
 #pragma unroll
                     for (int h = 0; h < G; ++h) {
                         const float mn = fmaxf(M[h], mc[k][h]);
@@ -895,8 +1111,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
         for (int i = 0; i < n_tiles && ok; ++i) {
             const int s = i % kStages, bb = i & 1, use = i >> 1;
+            // the tile's scores, then its row mask (clustered: published on its own barrier,
+            // possibly after the data)
             if (!mbar_wait(&c.s_full[bb], use & 1, &c.abort) ||
-                !mbar_wait(&c.full[s], (i / kStages) & 1, &c.abort)) {
+                !mbar_wait(clustered ? &c.meta_full[s] : &c.full[s], (i / kStages) & 1, &c.abort)) {
                 ok = false;
                 break;
             }
@@ -1015,7 +1233,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         if (ok && n_tiles > 0 && !correct(n_tiles - 1))
             ok = false;
-        if (clustered && c.cl_live) {
+        // clustered: the unit's liveness is published by the producer with unit_meta (it
+        // arrives there before its first wait, so this completes unless it never started)
+        bool meta_ok = true;
+        if (clustered && !(meta_ok = mbar_wait(&c.unit_meta, 0, &c.abort)))
+            ok = false;
+        if (clustered && meta_ok && c.cl_live) {
             // ---- merge the cluster's partials through distributed shared memory ----------
             // CTA r owns dims [r 128/C, (r+1) 128/C). Every CTA pushes, with remote stores,
             // its (max, sum) and its unnormalised outputs of each owner's dims into that
@@ -1025,6 +1248,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // own shared memory; after that no peer touches it, so it may exit. Every CTA of
             // a live cluster pushes and arrives even after a failed wait, so no peer waits for
             // it; outputs are written only when everything succeeded.
+            cluster_wait_acquire();            // the peers' barriers are initialised
             const int C = p.cluster;           // 2, 4 or 8 (group <= 4: see the host)
             const int nd = kHeadDim / C;       // dims per owner
             const int rank = static_cast<int>(blockIdx.x) % C;

@@ -68,6 +68,14 @@ __global__ void __launch_bounds__(256) append_kernel(
         seq_len[b] = pos + 1;
 }
 
+// Rows of one unit per compact block: 16 half-warps x kCompactRows consecutive rows each.
+constexpr int kCompactRows = 8;
+constexpr int kCompactBlockRows = 16 * kCompactRows;
+
+// Each half-warp copies kCompactRows consecutive packed rows (2 KB of K and 2 KB of V,
+// contiguous in the packed buffer). The positions, then (paged) their pages, then all 16
+// row loads are issued before anything waits on them, so a block spends three memory round
+// trips instead of one chain of dependent loads per row.
 __global__ void __launch_bounds__(256) compact_kernel(
     const uint4 *__restrict__ k, const uint4 *__restrict__ v, uint4 *__restrict__ kc,
     uint4 *__restrict__ vc, const int32_t *__restrict__ sel_idx, const int32_t *__restrict__ sel_cnt,
@@ -80,7 +88,8 @@ __global__ void __launch_bounds__(256) compact_kernel(
     const int kvh = u % n_kv_heads;
     const int b = (u / n_kv_heads) % batch;
     const int layer = u / (n_kv_heads * batch);
-    pdl_trigger();
+    // Dependents start only once the packed rows are written (pdl_trigger_after_writes): the
+    // fast step loads them before its own wait.
     pdl_wait();
     if (active && !active[b])
         return;
@@ -92,27 +101,53 @@ __global__ void __launch_bounds__(256) compact_kernel(
     if (blockIdx.y == 0 && threadIdx.x == 0)
         rows_out[u] = rows;
     const int sub = threadIdx.x >> 4, ch = threadIdx.x & 15;
-    for (int r = blockIdx.y * 16 + sub; r < rows; r += gridDim.y * 16) {
-        const int pos = r < n_s ? r : __ldg(sel_idx + static_cast<size_t>(u) * n_select + (r - n_s));
-        if (pos < 0 || pos >= L)
-            continue;
-        size_t src_row;
-        if (page_size == 0) {
-            src_row = static_cast<size_t>(u) * capacity + pos;
-        } else {
-            const int page = __ldg(page_table + b * max_pages + pos / page_size);
-            if (page < 0 || page >= n_pages) {
-                if (ch == 0)
-                    raise_error(err, 0x1u);
-                continue;
-            }
-            src_row = (static_cast<size_t>(layer * n_pages + page) * n_kv_heads + kvh) * page_size +
-                      pos % page_size;
+    const int r0 = blockIdx.y * kCompactBlockRows + sub * kCompactRows;
+    auto copy_rows = [&](int rb) {
+        int pos[kCompactRows];
+#pragma unroll
+        for (int j = 0; j < kCompactRows; ++j) {
+            const int r = rb + j;
+            pos[j] = r >= rows ? -1
+                     : r < n_s ? r
+                               : __ldg(sel_idx + static_cast<size_t>(u) * n_select + (r - n_s));
         }
-        const size_t dst_row = static_cast<size_t>(u) * comp_cap + r;
-        kc[dst_row * 16 + ch] = __ldg(k + src_row * 16 + ch);
-        vc[dst_row * 16 + ch] = __ldg(v + src_row * 16 + ch);
-    }
+        long long src[kCompactRows];
+#pragma unroll
+        for (int j = 0; j < kCompactRows; ++j) {
+            const bool in = pos[j] >= 0 && pos[j] < L;
+            if (page_size == 0) {
+                src[j] = in ? static_cast<long long>(u) * capacity + pos[j] : -1;
+            } else {
+                const int page = in ? __ldg(page_table + b * max_pages + pos[j] / page_size) : -1;
+                const bool good = page >= 0 && page < n_pages;
+                if (in && !good && ch == 0)
+                    raise_error(err, 0x1u);  // SFI_DEVERR_PAGE_RANGE: row skipped
+                src[j] = (in && good) ? (static_cast<long long>(layer * n_pages + page) * n_kv_heads + kvh) *
+                                                page_size + pos[j] % page_size
+                                      : -1;
+            }
+        }
+        uint4 kx[kCompactRows], vx[kCompactRows];
+#pragma unroll
+        for (int j = 0; j < kCompactRows; ++j) {
+            if (src[j] >= 0) {
+                kx[j] = __ldg(k + src[j] * 16 + ch);
+                vx[j] = __ldg(v + src[j] * 16 + ch);
+            }
+        }
+        const size_t dst0 = static_cast<size_t>(u) * comp_cap + rb;
+#pragma unroll
+        for (int j = 0; j < kCompactRows; ++j) {
+            if (src[j] >= 0) {
+                kc[(dst0 + j) * 16 + ch] = kx[j];
+                vc[(dst0 + j) * 16 + ch] = vx[j];
+            }
+        }
+    };
+    if (r0 < rows)
+        copy_rows(r0);
+    __syncthreads();
+    pdl_trigger_after_writes();
 }
 
 }  // namespace
@@ -138,7 +173,7 @@ cudaError_t launch_compact(const void *k, const void *v, void *kc, void *vc, con
 {
     const int units = n_layers * batch * n_kv_heads;
     const int comp_cap = n_sink + n_select;
-    dim3 grid(units, (comp_cap + 127) / 128);
+    dim3 grid(units, (comp_cap + kCompactBlockRows - 1) / kCompactBlockRows);
     const cudaError_t e = launch_pdl(
         compact_kernel, grid, dim3(256), 0, stream, static_cast<const uint4 *>(k),
         static_cast<const uint4 *>(v), static_cast<uint4 *>(kc), static_cast<uint4 *>(vc), sel_idx,

@@ -155,7 +155,8 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
     __shared__ int sh_count;
     __shared__ float sh_c[3];
 
-    pdl_trigger();
+    // Dependents start only once the selection is written (pdl_trigger_after_writes): the
+    // fast step reads the packed memory that follows from it before its own wait.
     const int tid = threadIdx.x, lane = tid & 31;
     pdl_wait();
     const int u = blockIdx.x;
@@ -172,6 +173,8 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
             out[i] = S + i;
         if (tid == 0)
             p.sel_cnt[u] = nC;
+        __syncthreads();
+        pdl_trigger_after_writes();
         return;
     }
     const float *fg = p.f + static_cast<size_t>(u) * p.capacity + S;
@@ -400,6 +403,8 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
     if (tid == 0) {
         p.sel_cnt[u] = K;
     }
+    __syncthreads();
+    pdl_trigger_after_writes();
 }
 
 // ---------------------------------------------------------------------------------------
@@ -429,7 +434,7 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
     __shared__ int sh_counts[2];  // this CTA's (greater, equal) keys for the ordered output
     __shared__ float sh_c[3];
 
-    pdl_trigger();
+    // dependents start only once the selection is written (see select_kernel)
     pdl_wait();
     const int C = p.cluster;
     const int rank = static_cast<int>(blockIdx.x) % C;
@@ -451,6 +456,8 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
             out[i] = S + i;
         if (tid == 0 && rank == 0)
             p.sel_cnt[u] = nC;
+        __syncthreads();
+        pdl_trigger_after_writes();
         return;
     }
     Fuse fz;
@@ -597,6 +604,8 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
     }
     if (tid == 0 && rank == 0)
         p.sel_cnt[u] = K;
+    __syncthreads();
+    pdl_trigger_after_writes();
     cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
 }
 

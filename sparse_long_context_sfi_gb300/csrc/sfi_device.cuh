@@ -111,10 +111,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 
 // ----------------------------------------------------- programmatic dependent launch
 
+// Publish global writes at GPU scope, then let the next kernel be scheduled. For kernels
+// whose output a later kernel may read before its own pdl_wait (the packing's sparse memory
+// and the Selector's counts): every thread of the CTA calls it after a CTA barrier that
+// follows all of the CTA's writes (the fence is cumulative over what the barrier ordered).
+// A CTA that exits without writing counts as triggered.
+__device__ __forceinline__ void pdl_trigger_after_writes();
+
 // Let the next kernel in the stream be scheduled now (its CTAs run their prologue and then
 // block in pdl_wait until this grid has completed).
 __device__ __forceinline__ void pdl_trigger()
 {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_trigger_after_writes()
+{
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
@@ -353,6 +366,19 @@ __device__ __forceinline__ void cluster_sync_all()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The two halves of cluster_sync_all, for a CTA that has cluster-wide work to publish early
+// and needs its peers' only much later: every thread arrives once (release), and the threads
+// that then touch peers' shared memory wait (acquire).
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // The shared::cluster address of the same shared-memory location in CTA `rank`.
