@@ -466,19 +466,72 @@ def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=N
         res["dense_only"] = {"tokens_per_s": world * tokens_per_run * dense_only_runs / (ms_d / 1000.0),
                              "ms_per_run": ms_d / dense_only_runs}
     if pipeline_runs:
-        # the layer-wise asynchronous pipeline: slow steps layer by layer, the Selector and
-        # compaction of each layer on a side stream beside the next layer's attention
-        g_pipe = capture(run_of(slow, pipeline=True))
-        ms_p = time_graph(g_pipe, pipeline_runs, 1)
-        del g_pipe
-        res["layer_pipeline"] = {"tokens_per_s": world * tokens_per_run * pipeline_runs / (ms_p / 1000.0),
-                                 "ms_per_run": ms_p / pipeline_runs}
+        # the layer-wise asynchronous pipeline: slow steps group of layers by group, the
+        # Selector and compaction of each group on a side stream beside the next group's
+        # attention; measured for several group sizes (layers per dense launch)
+        res["layer_pipeline"] = {}
+        for grp in (1, 4, 8):
+            if grp > cfg.n_layers:
+                continue
+            g_pipe = capture(run_of(slow, pipeline=True, pipeline_group=grp))
+            ms_p = time_graph(g_pipe, pipeline_runs, 1)
+            del g_pipe
+            res["layer_pipeline"][f"group_{grp}"] = {
+                "tokens_per_s": world * tokens_per_run * pipeline_runs / (ms_p / 1000.0),
+                "ms_per_run": ms_p / pipeline_runs, "layers_per_dense_launch": grp}
     if cold_fast:
         res["fast_cold"] = fast_step_cold(wl, st, ins, stream, dev, world)
+    if extras:
+        res["dense_isolated"] = dense_isolated(wl, st, ins, stream, world)
     torch.cuda.synchronize()
     res["device_error"] = int(st.err[0])
     del g_mix
     return res
+
+
+def dense_isolated(wl, st, ins, stream, world, n=4, k=5, w=2):
+    """The dense kernel alone (no evidence), n launches back to back per graph replay on the
+    state the timed runs left (every sequence at its final length). In the run each dense
+    launch is bracketed by event nodes, which cost it its programmatic-launch overlap; this
+    is the kernel's own rate. The cache is far larger than L2, so every launch reads HBM."""
+    import torch
+    from sparse_long_context_sfi_gb300 import sfi_dense_decode_attn
+    cfg = wl.cfg
+    out = torch.empty((cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
+                      dtype=torch.bfloat16, device=st.k.device)
+    st.kv.max_len = st.capacity
+
+    def issue():
+        for _ in range(n):
+            sfi_dense_decode_attn(st.kv, ins.q[0], out, False, None, st.ws, st.ws_bytes,
+                                  stream=stream)
+    with torch.cuda.stream(stream):
+        issue()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+        issue()
+    with torch.cuda.stream(stream):
+        for _ in range(w):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(k):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+    ms = allreduce_max(e0.elapsed_time(e1), world)
+    L = st.seq_len.double().cpu().numpy()
+    per_unit_q = cfg.group * 256 + cfg.group * 128 * 2
+    byt = float(L.sum() * cfg.n_layers * cfg.n_kv_heads * BYTES_PER_ROW +
+                cfg.n_layers * cfg.batch * cfg.n_kv_heads * per_unit_q)
+    avg = ms * 1e-3 / (k * n)
+    peak, _ = measured_peaks()
+    del g
+    return {"avg_us": avg * 1e6, "bytes_per_launch": byt, "achieved_gbs": byt / avg / 1e9,
+            "frac_of_peak": byt / avg / 1e9 / peak,
+            "how": f"{n} dense launches (no evidence) back to back per graph replay, {k} replays"}
 
 
 def fast_step_cold(wl, st, ins, stream, dev, world, per_replica=8, k=10, w=3):
@@ -676,6 +729,7 @@ def main():
                            parallelism="replicas" if world > 1 else "single"),
             "roofline": roofline,
             "kernels": ks,
+            "dense_isolated": res.get("dense_isolated"),
             "cpu_baseline": cpu,
             "e2e": res.get("e2e"),
             "gpu_launches": res["launches_per_run"] * args.steps,

@@ -218,6 +218,15 @@ sfi_status sfi_compact(const sfi_kv_cache *kv, const sfi_budget *budget,
                        const sfi_sparse_mem *mem, const uint8_t *active, void *stream);
 
 /*
+ * Inputs a fast step reads early. The fast-step calls (sfi_sparse_decode_attn,
+ * sfi_fast_decode_step, sfi_sparse_decode_attn_static) start loading the packed memory (kc,
+ * vc, rows, sel_cnt) and read `active` before they wait for the kernel issued before them on
+ * the stream to finish (programmatic dependent launch). These must therefore be complete
+ * when the call is issued. A kernel that writes them must not let its dependents start
+ * before its writes: without programmatic dependent launch that is always so, and the
+ * library's own sfi_select and sfi_compact let their dependents start only after their
+ * writes. The query, the lengths and the new rows are read only after that wait.
+ *
  * Fast step (blog, "How SFI Works": attention restricted to the support of the last slow
  * step; summary 2A "Fast Steps"): attention of each query head over the packed rows
  * kc/vc[0 .. mem->rows) of its unit plus the recent window [max(n_s, L - n_window), L) read
@@ -309,20 +318,22 @@ sfi_status sfi_schedule_tokens(int32_t steps, const int32_t *tokens, const int32
  *             fast steps; the whole slow step, joins included, when side_stream is set);
  *             NULL = none, and NULL entries are skipped
  *   side_stream layer-wise asynchronous pipeline (technical summary section 3, layer-wise
- *             overlap): NULL = off. When set, a slow step runs layer by layer: dense
- *             attention and evidence of layer i on `stream`, then sfi_select and sfi_compact
- *             of layer i on side_stream, so that they overlap the attention of layer i + 1;
+ *             overlap): NULL = off. When set, a slow step runs group of layers by group: dense
+ *             attention and evidence of group i on `stream`, then sfi_select and sfi_compact
+ *             of group i on side_stream, so that they overlap the attention of group i + 1;
  *             `stream` waits for side_stream before the step's last operation returns, so
  *             the next step sees the whole packed memory. A caller-owned stream of the same
  *             device; ignored when dense_only is set.
  *   fork_event, join_event  caller-owned cudaEvent_t (as void*, timing may be disabled),
  *             required with side_stream: fork_event is re-recorded on `stream` after each
- *             layer's evidence and waited for on side_stream; join_event is recorded on
- *             side_stream after the last layer and waited for on `stream`. Both work under
+ *             group's evidence and waited for on side_stream; join_event is recorded on
+ *             side_stream after the last group and waited for on `stream`. Both work under
  *             stream capture (the usual fork/join of a captured graph). Missing events with
  *             side_stream set: SFI_ERR_INVALID_ARG.
+ *   pipeline_group layers per dense launch with side_stream set (the Selector and packing of
+ *             one group overlap the attention of the next): 0 = about a quarter of the layers
  * Results with side_stream set equal those without up to the rounding of the dense step's
- * split-KV partition (one launch per layer instead of one for all layers).
+ * split-KV partition (one launch per group of layers instead of one for all layers).
  */
 typedef struct sfi_decode_plan {
     int32_t n_steps;
@@ -341,6 +352,7 @@ typedef struct sfi_decode_plan {
     void *side_stream;
     void *fork_event;
     void *join_event;
+    int32_t pipeline_group;
 } sfi_decode_plan;
 
 sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,

@@ -317,17 +317,17 @@ sfi_status sparse_impl(const sfi_kv_cache *kv, const sfi_sparse_mem *mem,
     return SFI_OK;
 }
 
-// A cache descriptor and packed memory restricted to layer l (base pointers offset by whole
-// layers; every per-unit array is laid out layer-major).
+// A cache descriptor and packed memory restricted to layers [l, l + nl) (base pointers
+// offset by whole layers; every per-unit array is laid out layer-major).
 void layer_views(const sfi_kv_cache *kv, const sfi_budget *budget, const sfi_sparse_mem *mem,
-                 int l, sfi_kv_cache *kl, sfi_sparse_mem *ml)
+                 int l, int nl, sfi_kv_cache *kl, sfi_sparse_mem *ml)
 {
     const size_t units = static_cast<size_t>(kv->batch) * kv->n_kv_heads;
     const size_t rows = kv->page_size ? static_cast<size_t>(kv->n_pages) * kv->n_kv_heads * 16
                                       : units * kv->capacity;
     const size_t comp = static_cast<size_t>(budget->n_sink + budget->n_select);
     *kl = *kv;
-    kl->n_layers = 1;
+    kl->n_layers = nl;
     kl->k = static_cast<char *>(kv->k) + l * rows * kHeadDim * 2;
     kl->v = static_cast<char *>(kv->v) + l * rows * kHeadDim * 2;
     *ml = *mem;
@@ -595,9 +595,10 @@ sfi_status sfi_schedule(int32_t steps, const uint8_t *mask, int32_t t_max, uint8
 }
 
 // One slow step with the layer-wise asynchronous pipeline (technical summary section 3,
-// layer-wise overlap): attention and evidence of layer l on the main stream, then the
-// Selector and compaction of layer l on the side stream, forked after layer l's evidence so
-// that they run beside the attention of layer l + 1; joined back at the end of the step.
+// layer-wise overlap): attention and evidence of a group of layers on the main stream, then
+// the Selector and compaction of that group on the side stream, forked after the group's
+// evidence so that they run beside the attention of the next group; joined back at the end
+// of the step. Groups of several layers keep each dense launch long enough to fill the GPU.
 static sfi_status slow_step_layers(const sfi_kv_cache *k, const sfi_budget *budget,
                                    const sfi_sparse_mem *mem, const sfi_decode_plan *plan,
                                    const void *q, void *out, const uint8_t *m_slow, void *ws,
@@ -608,14 +609,18 @@ static sfi_status slow_step_layers(const sfi_kv_cache *k, const sfi_budget *budg
     cudaEvent_t join = static_cast<cudaEvent_t>(plan->join_event);
     const size_t units = static_cast<size_t>(k->batch) * k->n_kv_heads;
     const size_t q_layer = static_cast<size_t>(k->batch) * k->n_q_heads * kHeadDim;
+    // layers per group: the plan's, or about a quarter of the layers
+    int group = plan->pipeline_group > 0 ? plan->pipeline_group : (k->n_layers + 3) / 4;
+    group = group < 1 ? 1 : (group > k->n_layers ? k->n_layers : group);
     if (e0 && record_event(e0, main_s) != cudaSuccess)
         return SFI_ERR_CUDA;
     sfi_status st = SFI_OK;
     bool forked = false;
-    for (int l = 0; l < k->n_layers && st == SFI_OK; ++l) {
+    for (int l = 0; l < k->n_layers && st == SFI_OK; l += group) {
+        const int nl = l + group <= k->n_layers ? group : k->n_layers - l;
         sfi_kv_cache kl;
         sfi_sparse_mem ml;
-        layer_views(k, budget, mem, l, &kl, &ml);
+        layer_views(k, budget, mem, l, nl, &kl, &ml);
         const void *ql = static_cast<const char *>(q) + l * q_layer * 2;
         void *ol = static_cast<char *>(out) + l * q_layer * (plan->out_fp32 ? 4 : 2);
         float *fl = plan->scores_f + l * units * k->capacity;

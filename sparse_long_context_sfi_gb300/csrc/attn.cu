@@ -32,6 +32,23 @@
 
 namespace sfi {
 namespace {
+// Remote shared-memory stores whose completion is counted in bytes on the receiving CTA's
+// mbarrier (st.async ... mbarrier::complete_tx): no separate arrive or release fence.
+__device__ __forceinline__ void st_async_f32x4(uint32_t addr, float a, float b, float c, float d, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+                 :: "r"(addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void st_async_f32x2(uint32_t addr, float a, float b, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+                 :: "r"(addr), "f"(a), "f"(b), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float a, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];"
+                 :: "r"(addr), "f"(a), "r"(bar) : "memory");
+}
 
 constexpr int kChunkBytes = kTile * 128;       // 128 rows x 128 B: one 64-dim half of a tile
 constexpr int kStageBytes = 4 * kChunkBytes;   // K[0:64), K[64:128), V[0:64), V[64:128)
@@ -45,6 +62,7 @@ constexpr int kQOff = kStages * kStageBytes;
 constexpr int kPOff = kQOff + 2 * kOpBytes;
 constexpr int kCtrlOff = kPOff + 2 * kOpBytes;
 
+constexpr int kMetaRing = 8;    // slots of the tile-metadata ring (see Ctrl)
 constexpr int kFlagFirst = 1;   // first tile of a segment (a unit's tiles inside one CTA)
 constexpr int kFlagLast = 2;    // last tile of a segment
 
@@ -57,15 +75,22 @@ struct TileMeta {
 };
 
 struct Ctrl {
-    uint64_t full[kStages], empty[kStages];
+    // Ring barriers per stage, separate for the K and the V half: K is free again once the
+    // score MMA has read it, V only after the P.V MMA, so the next tile's K can land early.
+    uint64_t fullK[kStages], fullV[kStages], emptyK[kStages], emptyV[kStages];
     uint64_t s_full[2], s_free[2], p_full[2], o_full[2], o_free[2], q_free[2];
     uint64_t gsync;             // softmax-group barrier (one arrive per warp)
     uint64_t drain;             // MMA drain on exit
     uint64_t unit_meta;         // clustered: the unit's length and activity are known
     uint64_t cl_ready;          // clustered: every CTA of the cluster has its partial in place
     uint64_t q_full;            // clustered: the query has landed
-    uint64_t meta_full[kStages];  // clustered: the stage's TileMeta (row mask) is written
-    TileMeta meta[kStages];
+    // Tile metadata (unit, flags, row mask) in a ring of its own, one barrier per slot: the
+    // producer publishes tile j only after the score MMA of tile j - 3, which the MMA issued
+    // after the softmax had read tile j - 5's metadata, so at most tiles j - 4 .. j - 1 are
+    // unread: kMetaRing >= 5 slots never collide, and a slot's barrier is never two phases
+    // ahead of the softmax waiting on it.
+    uint64_t meta_full[kMetaRing];
+    TileMeta meta[kMetaRing];
     float red_max[2][4][8];
     float red_sum[4][8];
     uint32_t tmem_base;
@@ -183,34 +208,89 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     // ---- set-up touching no global memory: overlaps the previous kernel's tail ----------
     pdl_trigger();
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&c.full[s], 1);
-            mbar_init(&c.empty[s], 1);
+    // the tensor maps' descriptors, fetched while the barriers are set up
+    if (warp == 1 && lane < (DENSE ? 3 : 5))
+        tma_prefetch_map(lane == 0 ? &tm_k : lane == 1 ? &tm_v : lane == 2 ? &tm_q
+                                    : lane == 3 ? &tm_kc : &tm_vc);
+    // CL: the clustered fast step, compiled as its own instance (launched only with
+    // p.cluster > 1), so neither instance carries the other's code paths
+    constexpr bool clustered = !DENSE && CL;
+    const bool fused = !DENSE && p.k_new != nullptr;
+    // Clustered fast step: this CTA's unit and its static slice [cl_t0, cl_t0 + cl_n) of the
+    // unit's tiles (the MMA and softmax roles iterate over the whole slice; a unit found
+    // inactive only gets empty tiles and no output). Producer state: the unit's packed row
+    // count cl_rows and packed sinks cl_ns, and cl_i, the next tile of the slice to publish.
+    int cl_u = 0, cl_t0 = 0, cl_n = 0, cl_rows = 0, cl_ns = 0, cl_i = 0, cl_pre = 0;
+    if (clustered) {
+        cl_u = static_cast<int>(blockIdx.x) / p.cluster;
+        const int rank = static_cast<int>(blockIdx.x) % p.cluster;
+        cl_t0 = rank * p.tiles_per_unit / p.cluster;
+        cl_n = (rank + 1) * p.tiles_per_unit / p.cluster - cl_t0;
+    }
+    if (warp == 0) {
+        // the barriers of the set-up, spread over the warp's lanes (its fence then publishes
+        // them all): index -> (barrier, expected arrivals)
+        constexpr int kRing = 4 * kStages, kNBars = kRing + kMetaRing + 12 + 5;
+        for (int idx = lane; idx < kNBars; idx += 32) {
+            uint64_t *bar = nullptr;
+            uint32_t cnt = 1;
+            if (idx < kRing) {
+                const int r = idx / kStages, st = idx % kStages;
+                bar = r == 0 ? &c.fullK[st] : r == 1 ? &c.fullV[st] : r == 2 ? &c.emptyK[st] : &c.emptyV[st];
+            } else if (idx < kRing + kMetaRing) {
+                bar = &c.meta_full[idx - kRing];
+            } else if (idx < kRing + kMetaRing + 12) {
+                const int j = idx - kRing - kMetaRing, bb = j & 1;
+                switch (j >> 1) {
+                case 0: bar = &c.s_full[bb]; break;
+                case 1: bar = &c.s_free[bb]; cnt = 4; break;
+                case 2: bar = &c.p_full[bb]; cnt = 4; break;
+                case 3: bar = &c.o_full[bb]; break;
+                case 4: bar = &c.o_free[bb]; cnt = 4; break;
+                default: bar = &c.q_free[bb]; break;
+                }
+            } else {
+                switch (idx - kRing - kMetaRing - 12) {
+                case 0: bar = &c.gsync; cnt = 4; break;
+                case 1: bar = &c.drain; break;
+                case 2: bar = &c.unit_meta; break;
+                case 3: bar = &c.q_full; break;
+                default: bar = &c.cl_ready; cnt = 1; break;
+                }
+            }
+            mbar_init(bar, cnt);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&c.s_full[b], 1);
-            mbar_init(&c.s_free[b], 4);
-            mbar_init(&c.p_full[b], 4);
-            mbar_init(&c.o_full[b], 1);
-            mbar_init(&c.o_free[b], 4);
-            mbar_init(&c.q_free[b], 1);
-        }
-        mbar_init(&c.gsync, 4);
-        mbar_init(&c.drain, 1);
-        mbar_init(&c.unit_meta, 1);
-        mbar_init(&c.q_full, 1);
-        for (int s = 0; s < kStages; ++s)
-            mbar_init(&c.meta_full[s], 1);
-        mbar_init(&c.cl_ready, static_cast<uint32_t>(p.cluster > 1 ? p.cluster : 1));
         mbar_fence_init();
-        tma_prefetch_map(&tm_k);
-        tma_prefetch_map(&tm_v);
-        tma_prefetch_map(&tm_q);
-        if (!DENSE) {
-            tma_prefetch_map(&tm_kc);
-            tma_prefetch_map(&tm_vc);
+        __syncwarp();
+        // The packed memory is complete before this launch starts (sfi_compact and
+        // sfi_select let their dependents start only after their writes), so the slice's
+        // first tiles of packed rows are requested here, before the rest of the set-up and
+        // the wait on the preceding grid: every box of them, since the unit's packed row
+        // count is known only after the wait (rows past it are masked then). Their arrival on
+        // full lets the score MMAs start as soon as the query lands.
+        if constexpr (clustered) {
+            const int packed_tiles = 64 * p.n_cbox / kTile;   // tiles of packed rows only
+            cl_pre = max(0, min(min(kStages, cl_n), packed_tiles - cl_t0));
+            const int h2 = lane >> 4, j16 = lane & 15;
+            for (int i = 0; i < cl_pre; ++i) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&c.fullK[i], 2u * 2u * 64u * 128u +
+                                                           ((p.test_stall && blockIdx.x == 0 && i == 0) ? 16u : 0u));
+                    mbar_arrive_expect_tx(&c.fullV[i], 2u * 2u * 64u * 128u);
+                }
+                __syncwarp();
+                if (j16 < 4) {
+                    const int k = ((cl_t0 + i) * kTile + 64 * h2) >> 6;
+                    const int kv = j16 >> 1, half = j16 & 1;
+                    tma_load_2d(smem + i * kStageBytes + kv * 2 * kChunkBytes + half * kChunkBytes +
+                                    64 * h2 * 128,
+                                kv ? &tm_vc : &tm_kc, kv ? &c.fullV[i] : &c.fullK[i], 64 * half,
+                                cl_u * p.comp_cap + 64 * k);
+                }
+            }
         }
+    }
+    if (tid == 0) {
         c.abort = 0;
         c.cl_live = 0;
     }
@@ -225,10 +305,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // Clustered fast step: one unit per cluster, its tiles split evenly over the cluster's
     // CTAs, which merge their partials through distributed shared memory. The cluster
     // barrier publishes the mbarrier initialisation and the TMEM base cluster-wide.
-    // CL: the clustered fast step, compiled as its own instance (launched only with
-    // p.cluster > 1), so neither instance carries the other's code paths
-    constexpr bool clustered = !DENSE && CL;
-    const bool fused = !DENSE && p.k_new != nullptr;
     if (clustered) {
         // arrive now, wait only before the first access to a peer's shared memory (the merge)
         tc_fence_before();
@@ -237,23 +313,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_after();
     }
 
-    // Clustered fast step: this CTA's unit and its static slice [cl_t0, cl_t0 + cl_n) of the
-    // unit's tiles (the MMA and softmax roles iterate over the whole slice; a unit found
-    // inactive only gets empty tiles and no output). Producer state: the unit's packed row
-    // count cl_rows and packed sinks cl_ns, and cl_i, the next tile of the slice to publish.
-    int cl_u = 0, cl_t0 = 0, cl_n = 0, cl_rows = 0, cl_ns = 0, cl_i = 0, cl_pre = 0;
-    if (clustered) {
-        cl_u = static_cast<int>(blockIdx.x) / p.cluster;
-        const int rank = static_cast<int>(blockIdx.x) % p.cluster;
-        cl_t0 = rank * p.tiles_per_unit / p.cluster;
-        cl_n = (rank + 1) * p.tiles_per_unit / p.cluster - cl_t0;
-    }
     // Tile t of the slice in ring stage i % kStages (producer warp, clustered): its row mask
     // is written and published on meta_full (what the softmax waits for), and with `issue`
     // its boxes are requested on full (what the MMA waits for): the packed rows below
     // cl_rows in 64-row boxes, and with `win` the window boxes of a sequence of length L
     // whose window starts at ws (wpg: the page of this lane's window box, paged cache).
-    auto cl_tile = [&](int i, int t, bool win, int L, int ws, int wpg, bool issue) {
+    auto cl_tile = [&](int i, int t, bool win, int L, int ws, int wpg, bool issue) -> bool {
         const int s = i % kStages;
         const int h2 = lane >> 4, j16 = lane & 15, op = lane & 3;
         const int R = t * kTile + 64 * h2;
@@ -317,80 +382,76 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int w = 0; w < 4; ++w)
             vw[w] = __reduce_or_sync(0xffffffffu, valid[w]);
         // test hook: CTA 0's first tile expects 16 bytes that never come (sfi_test_inject_stall)
-        const uint32_t bytes = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(rows) * 128u) +
-                               ((p.test_stall && blockIdx.x == 0 && i == 0) ? 16u : 0u);
+        const uint32_t bytes_k =
+            __reduce_add_sync(0xffffffffu, kv == 0 ? static_cast<uint32_t>(rows) * 128u : 0u) +
+            ((p.test_stall && blockIdx.x == 0 && i == 0) ? 16u : 0u);
+        const uint32_t bytes_v =
+            __reduce_add_sync(0xffffffffu, kv == 1 ? static_cast<uint32_t>(rows) * 128u : 0u);
+        uint8_t *dst = smem + s * kStageBytes + kv * 2 * kChunkBytes + half * kChunkBytes + row0 * 128;
         if (lane == 0) {
-            TileMeta &mt = c.meta[s];
+            TileMeta &mt = c.meta[i % kMetaRing];
             mt.unit = cl_u;
             mt.tile = t;
             mt.flags = (i == 0 ? kFlagFirst : 0) | (i == cl_n - 1 ? kFlagLast : 0);
 #pragma unroll
             for (int w = 0; w < 4; ++w)
                 mt.valid[w] = vw[w];
-            mbar_arrive(&c.meta_full[s]);  // releases the metadata
+            mbar_arrive(&c.meta_full[i % kMetaRing]);  // releases the metadata
             if (issue)
-                mbar_arrive_expect_tx(&c.full[s], bytes);
+                mbar_arrive_expect_tx(&c.fullK[s], bytes_k);
         }
         __syncwarp();
-        if (issue && rows > 0)
-            tma_load_2d(smem + s * kStageBytes + kv * 2 * kChunkBytes + half * kChunkBytes + row0 * 128,
-                        map, &c.full[s], 64 * half, y);
+        if (!issue)
+            return true;
+        if (rows > 0 && kv == 0)
+            tma_load_2d(dst, map, &c.fullK[s], 64 * half, y);
+        // the V half: free once the P.V MMA of this stage's previous tile is done
+        bool okv = true;
+        if (lane == 0)
+            okv = mbar_wait(&c.emptyV[s], ((i / kStages) & 1) ^ 1, &c.abort);
+        if (!__shfl_sync(0xffffffffu, okv ? 1 : 0, 0))
+            return false;
+        if (lane == 0)
+            mbar_arrive_expect_tx(&c.fullV[s], bytes_v);
+        __syncwarp();
+        if (rows > 0 && kv == 1)
+            tma_load_2d(dst, map, &c.fullV[s], 64 * half, y);
+        return true;
     };
-    // The packed memory is complete before this launch starts (sfi_compact and sfi_select let
-    // their dependents start only after their writes), so the slice's first tiles of packed
-    // rows are requested before the wait on the preceding grid: every box of them, since the
-    // unit's packed row count is known only after the wait (rows past it are masked then).
-    // Their arrival on full lets the score MMAs start as soon as the query lands.
-    if (clustered && warp == 0) {
-        const int packed_tiles = 64 * p.n_cbox / kTile;   // tiles of packed rows only
-        cl_pre = max(0, min(min(kStages, cl_n), packed_tiles - cl_t0));
-        const int h2 = lane >> 4, j16 = lane & 15;
-        for (int i = 0; i < cl_pre; ++i) {
-            if (lane == 0)
-                mbar_arrive_expect_tx(&c.full[i], 4u * 2u * 64u * 128u +
-                                                      ((p.test_stall && blockIdx.x == 0 && i == 0) ? 16u : 0u));
-            __syncwarp();
-            if (j16 < 4) {
-                const int k = ((cl_t0 + i) * kTile + 64 * h2) >> 6;
-                const int kv = j16 >> 1, half = j16 & 1;
-                tma_load_2d(smem + i * kStageBytes + kv * 2 * kChunkBytes + half * kChunkBytes +
-                                64 * h2 * 128,
-                            kv ? &tm_vc : &tm_kc, &c.full[i], 64 * half, cl_u * p.comp_cap + 64 * k);
-            }
-        }
-    }
-
     // ---- tile space: per-sequence tile counts and this CTA's range --------------------
-    pdl_wait();
     long long g0 = 0, g1 = 0;
     int n_tiles = 0;
-    if (!clustered) {
-        for (int b = tid; b < B; b += kAttnThreads) {
-            const int L0 = p.seq_len[b];
-            const int L = fused ? L0 + 1 : L0;  // with the fused append: the new row included
-            int act = p.active ? p.active[b] : 1;
-            if (act && (L0 < 0 || L0 > p.max_len || L > p.capacity)) {
-                raise_error(p.err, 0x8u);  // SFI_DEVERR_LENGTH
-                act = 0;
+    // exclusive prefix sum of the per-sequence tile counts c.nt, one warp (each lane sums a
+    // contiguous run of up to 8 sequences, batch <= 256, then a warp scan), and this CTA's
+    // stream-K range: equal contiguous tile ranges (balances ragged lengths and unit counts
+    // that are not a multiple of the CTA count); all threads, ends with a CTA barrier
+    auto tile_space = [&]() {
+        if (warp == 0) {
+            const int per = (B + 31) / 32, b0 = lane * per;
+            int run = 0;
+            for (int j = 0; j < per; ++j)
+                run += (b0 + j < B) ? c.nt[b0 + j] : 0;
+            int incl = run;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o)
+                    incl += y;
             }
-            c.nt[b] = (act && L > 0) ? (DENSE ? (L + kTile - 1) / kTile : p.tiles_per_unit) : 0;
-            c.len[b] = L;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            long long acc = 0;
-            for (int b = 0; b < B; ++b) {
-                c.pre[b] = static_cast<int>(acc * Hkv);
-                acc += c.nt[b];
+            int acc = incl - run;
+            for (int j = 0; j < per && b0 + j < B; ++j) {
+                c.pre[b0 + j] = acc * Hkv;
+                acc += c.nt[b0 + j];
             }
-            c.TL = acc * Hkv;
-            c.T = c.TL * p.n_layers;
-            c.P = static_cast<int>(c.T < gridDim.x ? c.T : gridDim.x);
-            const long long P = c.P > 0 ? c.P : 1;
-            // stream-K: equal contiguous tile ranges (balances ragged lengths and unit counts
-            // that are not a multiple of the CTA count)
-            c.g0 = static_cast<long long>(blockIdx.x) * c.T / P;
-            c.g1 = static_cast<long long>(blockIdx.x + 1) * c.T / P;
+            const int total = __shfl_sync(0xffffffffu, incl, 31);
+            if (lane == 0) {
+                c.TL = static_cast<long long>(total) * Hkv;
+                c.T = c.TL * p.n_layers;
+                c.P = static_cast<int>(c.T < gridDim.x ? c.T : gridDim.x);
+                const long long P = c.P > 0 ? c.P : 1;
+                c.g0 = static_cast<long long>(blockIdx.x) * c.T / P;
+                c.g1 = static_cast<long long>(blockIdx.x + 1) * c.T / P;
+            }
         }
         tc_fence_before();
         __syncthreads();
@@ -399,6 +460,64 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         g0 = c.g0;
         g1 = c.g1;
         n_tiles = static_cast<int>(blockIdx.x) < c.P ? static_cast<int>(g1 - g0) : 0;
+    };
+    // the first tile of the range: (layer, sequence, kv head, tile of the unit)
+    auto first_tile = [&](int &layer, int &b, int &kvh, int &t) {
+        layer = static_cast<int>(g0 / c.TL);
+        const int r = static_cast<int>(g0 - static_cast<long long>(layer) * c.TL);
+        b = 0;
+        while (b + 1 < B && (c.nt[b] == 0 || c.pre[b] + Hkv * c.nt[b] <= r))
+            ++b;
+        kvh = (r - c.pre[b]) / c.nt[b];
+        t = (r - c.pre[b]) - kvh * c.nt[b];
+    };
+    // Sparse step over tile ranges: every active sequence has tiles_per_unit tiles, so the
+    // tile space depends only on `active` (an input complete at launch) and is laid out before
+    // the wait on the preceding grid; the lengths read after it only decide which units give
+    // output (c.len[b] <= 0: none). The packed counts of the range's first unit (packed
+    // memory, complete at launch) are loaded before the wait as well: lane 0 the packed row
+    // count, lane 1 the selection count. (Requesting the first tiles' boxes here too was
+    // measured slower on the ragged batch-32 workload: the late CTAs' set-up is not hidden.)
+    int tr_meta = 0;
+    if (!clustered && !DENSE) {
+        for (int b = tid; b < B; b += kAttnThreads)
+            c.nt[b] = (p.active ? p.active[b] : 1) ? p.tiles_per_unit : 0;
+        __syncthreads();
+        tile_space();
+        if (warp == 0 && n_tiles > 0) {
+            int layer, b, kvh, t;
+            first_tile(layer, b, kvh, t);
+            const int u = (layer * B + b) * Hkv + kvh;
+            tr_meta = lane == 0 ? __ldg(p.comp_rows + u) : lane == 1 ? __ldg(p.sel_cnt + u) : 0;
+        }
+    }
+    pdl_wait();
+    if (!clustered && !DENSE) {
+        for (int b = tid; b < B; b += kAttnThreads) {
+            const int L0 = p.seq_len[b];
+            const int L = fused ? L0 + 1 : L0;  // with the fused append: the new row included
+            int act = c.nt[b] > 0;
+            if (act && (L0 < 0 || L0 > p.max_len || L > p.capacity)) {
+                raise_error(p.err, 0x8u);  // SFI_DEVERR_LENGTH
+                act = 0;
+            }
+            c.len[b] = act ? L : 0;
+        }
+        __syncthreads();
+    } else if (!clustered) {
+        for (int b = tid; b < B; b += kAttnThreads) {
+            const int L0 = p.seq_len[b];
+            const int L = fused ? L0 + 1 : L0;
+            int act = p.active ? p.active[b] : 1;
+            if (act && (L0 < 0 || L0 > p.max_len || L > p.capacity)) {
+                raise_error(p.err, 0x8u);  // SFI_DEVERR_LENGTH
+                act = 0;
+            }
+            c.nt[b] = (act && L > 0) ? (L + kTile - 1) / kTile : 0;
+            c.len[b] = L;
+        }
+        __syncthreads();
+        tile_space();
     } else {
         n_tiles = cl_n;
         g0 = cl_t0;
@@ -496,7 +615,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (; cl_i < cl_n; ++cl_i) {
             const int st = cl_i % kStages, t = cl_t0 + cl_i;
             if (lane == 0)
-                ok = mbar_wait(&c.empty[st], ((cl_i / kStages) & 1) ^ 1, &c.abort);
+                ok = mbar_wait(&c.emptyK[st], ((cl_i / kStages) & 1) ^ 1, &c.abort);
             if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
                 if (lane == 0)
                     fail(c, p.err);
@@ -511,12 +630,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             if (t == app)
                 append_new_row();
-            cl_tile(cl_i, t, has_win, L, ws, wpg, true);
+            if (!cl_tile(cl_i, t, has_win, L, ws, wpg, true)) {
+                // its K half may be in flight; its V half was never requested: complete that
+                // phase with a bare arrival so the drain below does not wait for it
+                if (lane == 0) {
+                    mbar_arrive(&c.fullV[st]);
+                    fail(c, p.err);
+                }
+                ++cl_i;
+                break;
+            }
         }
         // Never leave a copy in flight into shared memory we are about to give up.
         if (lane == 0) {
-            for (int j = max(0, cl_i - kStages); j < cl_i; ++j)
-                mbar_wait(&c.full[j % kStages], (j / kStages) & 1, nullptr);
+            for (int j = max(0, cl_i - kStages); j < cl_i; ++j) {
+                mbar_wait(&c.fullK[j % kStages], (j / kStages) & 1, nullptr);
+                mbar_wait(&c.fullV[j % kStages], (j / kStages) & 1, nullptr);
+            }
             mbar_wait(&c.q_full, 0, nullptr);
         }
         // Fused append: the last CTA of the grid to get here advances the lengths.
@@ -544,16 +674,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         int issued = 0;
         if (n_tiles > 0) {
             const uint64_t pol = policy_evict_first();
-            // decode the first tile of the range
             long long g = g0;
-            int layer = static_cast<int>(g / c.TL), b = 0, kvh, t;
-            {
-                const int r = static_cast<int>(g - static_cast<long long>(layer) * c.TL);
-                while (b + 1 < B && (c.nt[b] == 0 || c.pre[b] + Hkv * c.nt[b] <= r))
-                    ++b;
-                kvh = (r - c.pre[b]) / c.nt[b];
-                t = (r - c.pre[b]) - kvh * c.nt[b];
-            }
+            int layer, b, kvh, t;
+            first_tile(layer, b, kvh, t);
             auto ntiles_of = [&](int bb) { return c.nt[bb]; };
             int seg = -1;
             int seg_len = 0, seg_rows_c = 0, seg_ws = 0;
@@ -620,7 +743,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 const int s = i % kStages;
                 if (lane == 0)
-                    ok = mbar_wait(&c.empty[s], ((i / kStages) & 1) ^ 1, &c.abort);
+                    ok = mbar_wait(&c.emptyK[s], ((i / kStages) & 1) ^ 1, &c.abort);
                 const int u = (layer * B + b) * Hkv + kvh;
                 const bool first = (i == 0) || (t == 0);
                 const bool last = (i == n_tiles - 1) || (t == ntiles_of(b) - 1);
@@ -632,9 +755,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     if (!DENSE) {
                         int rows_c, sel;
                         {
-                            cur_meta = seg == 0 ? (lane == 0 ? __ldg(p.comp_rows + u)
-                                                   : lane == 1 ? __ldg(p.sel_cnt + u) : 0)
-                                                : nxt_meta;
+                            cur_meta = seg == 0 ? tr_meta : nxt_meta;
                             // the next segment of the range, if any: its counts, loaded now
                             if (i + (ntiles_of(b) - t) < n_tiles) {
                                 int nl = layer, nb = b, nk = kvh;
@@ -795,33 +916,56 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     vw[w] = __reduce_or_sync(0xffffffffu, valid[w]);
                 // test hook: CTA 0's first tile expects 16 bytes that never come, so the waits
                 // on it run out (see sfi_test_inject_stall)
-                const uint32_t bytes =
-                    __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(rows) * 128u) +
+                const uint32_t bytes_k =
+                    __reduce_add_sync(0xffffffffu, kv == 0 ? static_cast<uint32_t>(rows) * 128u : 0u) +
                     (first ? 2u * G * 128u : 0u) +
                     ((p.test_stall && blockIdx.x == 0 && i == 0) ? 16u : 0u);
-                uint64_t *bar = &c.full[s];
+                const uint32_t bytes_v =
+                    __reduce_add_sync(0xffffffffu, kv == 1 ? static_cast<uint32_t>(rows) * 128u : 0u);
                 if (lane == 0) {
-                    TileMeta &mt = c.meta[s];
+                    TileMeta &mt = c.meta[i % kMetaRing];
                     mt.unit = u;
                     mt.tile = t;
                     mt.flags = (first ? kFlagFirst : 0) | (last ? kFlagLast : 0);
 #pragma unroll
                     for (int w = 0; w < 4; ++w)
                         mt.valid[w] = vw[w];
-                    mbar_arrive_expect_tx(bar, bytes);  // releases the metadata
+                    mbar_arrive(&c.meta_full[i % kMetaRing]);  // releases the metadata
+                    mbar_arrive_expect_tx(&c.fullK[s], bytes_k);  // (and for the MMA's flags)
                 }
                 __syncwarp();
                 if (first && lane < 2) {
                     uint8_t *qb = smem + kQOff + (seg & 1) * kOpBytes;
-                    tma_load_2d(qb + lane * kOpChunk, &tm_q, bar, 64 * lane, u * G);
+                    tma_load_2d(qb + lane * kOpChunk, &tm_q, &c.fullK[s], 64 * lane, u * G);
                 }
-                if (rows > 0) {
-                    uint8_t *dst = smem + s * kStageBytes + kv * 2 * kChunkBytes +
-                                   half * kChunkBytes + row0 * 128;
+                uint8_t *dst = smem + s * kStageBytes + kv * 2 * kChunkBytes + half * kChunkBytes +
+                               row0 * 128;
+                // K half now; the V half once the P.V MMA of this stage's previous tile is done
+                if (rows > 0 && kv == 0) {
                     if (DENSE)  // streamed once per slow step: do not displace reusable lines
-                        tma_load_2d_hint(dst, map, bar, 64 * half, y, pol);
+                        tma_load_2d_hint(dst, map, &c.fullK[s], 64 * half, y, pol);
                     else
-                        tma_load_2d(dst, map, bar, 64 * half, y);
+                        tma_load_2d(dst, map, &c.fullK[s], 64 * half, y);
+                }
+                bool okv = true;
+                if (lane == 0)
+                    okv = mbar_wait(&c.emptyV[s], ((i / kStages) & 1) ^ 1, &c.abort);
+                if (!__shfl_sync(0xffffffffu, okv ? 1 : 0, 0)) {
+                    if (lane == 0) {   // no V requested: complete its phase for the drain
+                        mbar_arrive(&c.fullV[s]);
+                        fail(c, p.err);
+                    }
+                    ++issued;
+                    break;
+                }
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&c.fullV[s], bytes_v);
+                __syncwarp();
+                if (rows > 0 && kv == 1) {
+                    if (DENSE)
+                        tma_load_2d_hint(dst, map, &c.fullV[s], 64 * half, y, pol);
+                    else
+                        tma_load_2d(dst, map, &c.fullV[s], 64 * half, y);
                 }
                 if (fused && app_tile >= 0 && !appended) {  // a later tile holds it
                     append_row(u, layer, b, kvh, L - 1);
@@ -845,8 +989,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         // Never leave a copy in flight into shared memory we are about to give up.
         if (lane == 0)
-            for (int j = max(0, issued - kStages); j < issued; ++j)
-                mbar_wait(&c.full[j % kStages], (j / kStages) & 1, nullptr);
+            for (int j = max(0, issued - kStages); j < issued; ++j) {
+                mbar_wait(&c.fullK[j % kStages], (j / kStages) & 1, nullptr);
+                mbar_wait(&c.fullV[j % kStages], (j / kStages) & 1, nullptr);
+            }
         // Fused append: this CTA has read seq_len (set-up); the last CTA of the grid to get
         // here advances the length of every sequence whose new row was appended.
         if (fused) {
@@ -882,13 +1028,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (ns < n_tiles) {
                     const int s = ns % kStages, bb = ns & 1, use = ns >> 1;
                     // (clustered: the query has its own barrier, awaited before the first S)
-                    if (mbar_test_wait(&c.full[s], (ns / kStages) & 1) &&
+                    if (mbar_test_wait(&c.fullK[s], (ns / kStages) & 1) &&
                         mbar_test_wait(&c.s_free[bb], (use & 1) ^ 1) &&
                         (!clustered || ns > 0 || mbar_test_wait(&c.q_full, 0))) {
                         // clustered: the row masks may still be in flight; the flags are static
                         const int flags = clustered ? ((ns == 0 ? kFlagFirst : 0) |
                                                        (ns == n_tiles - 1 ? kFlagLast : 0))
-                                                    : c.meta[s].flags;
+                                                    : c.meta[ns % kMetaRing].flags;
                         if (flags & kFlagFirst)
                             ++seg;
                         tc_fence_after();
@@ -901,6 +1047,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             umma_bf16(tmem + bb * 16, a, bd, idesc_s, kk > 0 ? 1u : 0u);
                         }
                         umma_commit(&c.s_full[bb]);
+                        umma_commit(&c.emptyK[s]);   // the K half is free once S is done
                         if (flags & kFlagLast)
                             umma_commit(&c.q_free[seg & 1]);
                         ++ns;
@@ -910,7 +1057,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (np < ns) {
                     const int s = np % kStages, bb = np & 1, use = np >> 1;
                     if (mbar_test_wait(&c.p_full[bb], use & 1) &&
-                        mbar_test_wait(&c.o_free[bb], (use & 1) ^ 1)) {
+                        mbar_test_wait(&c.o_free[bb], (use & 1) ^ 1) &&
+                        mbar_test_wait(&c.fullV[s], (np / kStages) & 1)) {
                         tc_fence_after();
                         const uint32_t va = smem_u32(smem + s * kStageBytes + 2 * kChunkBytes);
                         const uint32_t pa = smem_u32(smem + kPOff + bb * kOpBytes);
@@ -921,7 +1069,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             umma_bf16(tmem + 32 + bb * 16, a, bd, idesc_o, kk > 0 ? 1u : 0u);
                         }
                         umma_commit(&c.o_full[bb]);
-                        umma_commit(&c.empty[s]);
+                        umma_commit(&c.emptyV[s]);
                         ++np;
                         prog = true;
                     }
@@ -977,6 +1125,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
         auto finalize = [&](int u, const float (&fm)[G], const float (&fle)[G]) -> bool {
             const int kvh = u % Hkv, b = (u / Hkv) % B, layer = u / (Hkv * B);
+            // sparse: an active sequence found with an invalid or empty length gives no output
+            // (every CTA of the unit sees the same length, so none takes part in its merge)
+            if (!DENSE && c.len[b] <= 0)
+                return true;
             const long long su = layer * c.TL + c.pre[b] + static_cast<long long>(kvh) * c.nt[b];
             const long long eu = su + c.nt[b];
             const long long P = c.P, T = c.T;
@@ -995,9 +1147,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             const int slot = (su <= g0) ? 0 : 1;
             float *part = p.partials + (2 * static_cast<size_t>(blockIdx.x) + slot) * kPartialFloats(G);
+            // dim-major [128][G]: one 16-byte store (and load in the merge) per dim for G >= 4
+            if constexpr (G >= 4) {
 #pragma unroll
-            for (int h = 0; h < G; ++h)
-                part[h * kHeadDim + row] = acc[h];
+                for (int h = 0; h < G; h += 4)
+                    *reinterpret_cast<float4 *>(part + row * G + h) =
+                        make_float4(acc[h], acc[h + 1], acc[h + 2], acc[h + 3]);
+            } else {
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+                    part[row * G + h] = acc[h];
+            }
             if (row < G) {
                 part[G * kHeadDim + row] = pick<G>(fm, row);
                 part[G * kHeadDim + G + row] = pick<G>(fle, row);
@@ -1021,17 +1181,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 return false;
             if (!c.last_flag)
                 return true;
-            // One-pass online merge starting from this CTA's own partial (in registers);
-            // the other contributors are read in batches (8 for groups up to 4, else 4) so
-            // that their loads overlap: a unit split over ~20 CTAs then takes 3 rounds of
-            // L2 latency instead of 5.
+            // One-pass online merge over the contributors in CTA order (this CTA's own
+            // partial from registers at its place), so the rounding does not depend on which
+            // contributor arrived last; the others are read in batches (8 for groups up to 4,
+            // else 4) so that their loads overlap: a unit split over ~20 CTAs then takes 3
+            // rounds of L2 latency instead of 5.
             constexpr int kMB = G <= 4 ? 8 : 4;
             float M[G], Le[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                M[h] = fm[h];
-                Le[h] = fle[h];
-                o[h] = acc[h];
+                M[h] = -INFINITY;
+                Le[h] = 0.f;
+                o[h] = 0.f;
             }
             // u may be the last segment of cf's range (slot 1)
             const bool cf_tail = static_cast<long long>(cf) * T / P < su;
@@ -1046,11 +1207,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const float *pc = p.partials +
                                       (2 * static_cast<size_t>(use[k] ? cc : blockIdx.x) + sl) *
                                           kPartialFloats(G);
+                    if constexpr (G >= 4) {
 #pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        mc[k][h] = use[k] ? __ldcg(pc + G * kHeadDim + h) : -INFINITY;
-                        lc[k][h] = use[k] ? __ldcg(pc + G * kHeadDim + G + h) : 0.f;
-                        ac[k][h] = use[k] ? __ldcg(pc + h * kHeadDim + row) : 0.f;
+                        for (int h = 0; h < G; h += 4) {
+                            float4 m4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                            float4 l4 = make_float4(0.f, 0.f, 0.f, 0.f), a4 = l4;
+                            if (use[k]) {
+                                m4 = __ldcg(reinterpret_cast<const float4 *>(pc + G * kHeadDim + h));
+                                l4 = __ldcg(reinterpret_cast<const float4 *>(pc + G * kHeadDim + G + h));
+                                a4 = __ldcg(reinterpret_cast<const float4 *>(pc + row * G + h));
+                            }
+                            mc[k][h] = m4.x; mc[k][h + 1] = m4.y; mc[k][h + 2] = m4.z; mc[k][h + 3] = m4.w;
+                            lc[k][h] = l4.x; lc[k][h + 1] = l4.y; lc[k][h + 2] = l4.z; lc[k][h + 3] = l4.w;
+                            ac[k][h] = a4.x; ac[k][h + 1] = a4.y; ac[k][h + 2] = a4.z; ac[k][h + 3] = a4.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < G; ++h) {
+                            mc[k][h] = use[k] ? __ldcg(pc + G * kHeadDim + h) : -INFINITY;
+                            lc[k][h] = use[k] ? __ldcg(pc + G * kHeadDim + G + h) : 0.f;
+                            ac[k][h] = use[k] ? __ldcg(pc + row * G + h) : 0.f;
+                        }
+                    }
+                    if (c0 + k == static_cast<int>(blockIdx.x)) {
+#pragma unroll
+                        for (int h = 0; h < G; ++h) {
+                            mc[k][h] = fm[h];
+                            lc[k][h] = fle[h];
+                            ac[k][h] = acc[h];
+                        }
                     }
                 }
 #pragma unroll
@@ -1111,17 +1296,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
         for (int i = 0; i < n_tiles && ok; ++i) {
             const int s = i % kStages, bb = i & 1, use = i >> 1;
-            // the tile's scores, then its row mask (clustered: published on its own barrier,
-            // possibly after the data)
+            // the tile's scores, then its metadata (row mask), published on the ring's own
+            // barrier (for a clustered step possibly after the data)
             if (!mbar_wait(&c.s_full[bb], use & 1, &c.abort) ||
-                !mbar_wait(clustered ? &c.meta_full[s] : &c.full[s], (i / kStages) & 1, &c.abort)) {
+                !mbar_wait(&c.meta_full[i % kMetaRing], (i / kMetaRing) & 1, &c.abort)) {
                 ok = false;
                 break;
             }
-            const int u = c.meta[s].unit;
-            const int tile = c.meta[s].tile;
-            const int flags = c.meta[s].flags;
-            const bool valid = (c.meta[s].valid[row >> 5] >> (row & 31)) & 1u;
+            const TileMeta &mt = c.meta[i % kMetaRing];
+            const int u = mt.unit;
+            const int tile = mt.tile;
+            const int flags = mt.flags;
+            const bool valid = (mt.valid[row >> 5] >> (row & 31)) & 1u;
             if (flags & kFlagFirst) {
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
@@ -1183,14 +1369,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 *reinterpret_cast<__nv_bfloat16 *>(pb + base + (G + h) * 128 +
                                                    ((sw ^ ((G + h) & 7)) << 4)) = plo;
             }
+            bool vok = true;
             if (!valid) {
-                // keep P = 0 rows from meeting stale (possibly non-finite) V data
+                // keep P = 0 rows from meeting stale (possibly non-finite) V data, once the
+                // tile's V half has landed (it may follow the K half)
+                vok = mbar_wait(&c.fullV[s], (i / kStages) & 1, &c.abort);
                 uint8_t *vrow = smem + s * kStageBytes + 2 * kChunkBytes + row * 128;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     reinterpret_cast<uint4 *>(vrow)[k] = make_uint4(0u, 0u, 0u, 0u);
                     reinterpret_cast<uint4 *>(vrow + kChunkBytes)[k] = make_uint4(0u, 0u, 0u, 0u);
                 }
+            }
+            if (!__all_sync(0xffffffffu, vok)) {
+                ok = false;
+                break;
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -1240,39 +1433,46 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             ok = false;
         if (clustered && meta_ok && c.cl_live) {
             // ---- merge the cluster's partials through distributed shared memory ----------
-            // CTA r owns dims [r 128/C, (r+1) 128/C). Every CTA pushes, with remote stores,
-            // its (max, sum) and its unnormalised outputs of each owner's dims into that
-            // owner's receive area (the second Q buffer: a clustered CTA has one segment and
-            // uses only the first), then one lane per owner arrives on the owner's cl_ready
-            // with release semantics. An owner that has seen all C arrivals merges from its
-            // own shared memory; after that no peer touches it, so it may exit. Every CTA of
-            // a live cluster pushes and arrives even after a failed wait, so no peer waits for
-            // it; outputs are written only when everything succeeded.
+            // CTA r owns dims [r 128/C, (r+1) 128/C). Every CTA pushes, with asynchronous
+            // remote stores that count their bytes on the owner's cl_ready, its (max, sum)
+            // and its unnormalised outputs of each owner's dims into that owner's receive area
+            // (the second Q buffer: a clustered CTA has one segment and uses only the first);
+            // each owner expects all C sources' bytes on its own barrier. An owner whose
+            // barrier has completed merges from its own shared memory; after that no peer
+            // touches it, so it may exit. Every CTA of a live cluster pushes even after a
+            // failed wait, so no peer waits for it; outputs are written only when everything
+            // succeeded.
             cluster_wait_acquire();            // the peers' barriers are initialised
             const int C = p.cluster;           // 2, 4 or 8 (group <= 4: see the host)
             const int nd = kHeadDim / C;       // dims per owner
             const int rank = static_cast<int>(blockIdx.x) % C;
             const int u = static_cast<int>(blockIdx.x) / C;
             float *recv = reinterpret_cast<float *>(smem + kQOff + kOpBytes);
-            // receive layout: acc [src][G][nd], then stats [src][G][2] (max, sum)
+            // receive layout: acc [src][nd][G], then stats [src][G][2] (max, sum)
             const int acc_floats = C * G * nd;
+            if (row == 0)   // every byte the C sources push here
+                mbar_arrive_expect_tx(&c.cl_ready, static_cast<uint32_t>(C * (nd * G + 2 * G) * 4));
             {
                 const int owner = row / nd, j = row - owner * nd;
-                const uint32_t base = map_to_rank(recv, static_cast<uint32_t>(owner));
+                const uint32_t rb = map_to_rank(&c.cl_ready, static_cast<uint32_t>(owner));
+                const uint32_t base = map_to_rank(recv, static_cast<uint32_t>(owner)) +
+                                      4u * ((rank * nd + j) * G);
+                if constexpr (G == 4) {
+                    st_async_f32x4(base, acc[0], acc[1], acc[2], acc[3], rb);
+                } else {
 #pragma unroll
-                for (int h = 0; h < G; ++h)
-                    st_cluster_f32(base + 4u * ((rank * G + h) * nd + j), acc[h]);
+                    for (int h = 0; h < G; ++h)
+                        st_async_f32(base + 4u * h, acc[h], rb);
+                }
                 if (row < C * G) {  // (max, sum) of head h to owner row / G
                     const int ow = row / G, h = row - ow * G;
-                    const uint32_t b2 = map_to_rank(recv, static_cast<uint32_t>(ow));
-                    const int o2 = acc_floats + (rank * G + h) * 2;
-                    st_cluster_f32(b2 + 4u * o2, pick<G>(fin_m, h));
-                    st_cluster_f32(b2 + 4u * (o2 + 1), pick<G>(fin_le, h));
+                    const uint32_t b2 = map_to_rank(recv, static_cast<uint32_t>(ow)) +
+                                        4u * (acc_floats + (rank * G + h) * 2);
+                    st_async_f32x2(b2, pick<G>(fin_m, h), pick<G>(fin_le, h),
+                                   map_to_rank(&c.cl_ready, static_cast<uint32_t>(ow)));
                 }
             }
-            bool good = group_sync(c, gphase, lane) && ok;  // every thread's pushes are issued
-            if (row < C)  // lanes 0..C-1 of one warp, one owner each, in parallel
-                mbar_arrive_cluster(map_to_rank(&c.cl_ready, static_cast<uint32_t>(row)));
+            bool good = ok;
             // A peer arrives within its own bounded waits even when it fails; this limit is
             // well above those, so no CTA leaves while a live peer may still push to it.
             good = mbar_wait_cluster(&c.cl_ready, 0, 8 * kWaitTimeoutNs) && good;
@@ -1287,7 +1487,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const float mq = recv[acc_floats + (q * G + h) * 2];
                         const float w = (mq == -INFINITY) ? 0.f : exp2f(mq - M);
                         Lsum = fmaf(w, recv[acc_floats + (q * G + h) * 2 + 1], Lsum);
-                        O = fmaf(w, recv[(q * G + h) * nd + j], O);
+                        O = fmaf(w, recv[(q * nd + j) * G + h], O);
                     }
                     const float v = Lsum > 0.f ? O / Lsum : 0.f;
                     const size_t idx = (static_cast<size_t>(u) * G + h) * kHeadDim + rank * nd + j;

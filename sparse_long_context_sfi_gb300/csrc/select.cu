@@ -418,6 +418,7 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
 // all candidates kept) are taken by all of them together.
 
 constexpr int kClusterKeyCap = 33280;  // candidates per CTA (a 131K context in 4 CTAs)
+constexpr int kMergeCap = 4096;        // threshold-bin keys exchanged as lists (else radix)
 
 size_t select_cluster_smem_bytes()
 {
@@ -431,7 +432,9 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
     __shared__ int scratch[2 * kWarps + 2];
     __shared__ uint32_t sh_digit;
     __shared__ int sh_above;
-    __shared__ int sh_counts[2];  // this CTA's (greater, equal) keys for the ordered output
+    __shared__ int sh_counts[2];  // this CTA's (greater, equal) keys for the ordered output,
+                                  // or (keys above the threshold bin, its list length)
+    __shared__ int sh_lcnt;
     __shared__ float sh_c[3];
 
     // dependents start only once the selection is written (see select_kernel)
@@ -509,8 +512,27 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
         ks[i] = k;
         atomicAdd(&hbuf0[k >> 20], 1u);
     }
-    // digit of the cluster histogram (nb bins) where the running count from the top first
-    // reaches krem; every CTA computes the same one
+    // digit of the histogram hist (nb bins) where the running count from the top first
+    // reaches krem (sh_digit, and the count above it in sh_above)
+    auto find_digit = [&](const uint32_t *hist, int nb, int krem_now) {
+        const int per = nb / NT;
+        int mine_cnt = 0;
+        for (int j = 0; j < per; ++j)
+            mine_cnt += static_cast<int>(hist[nb - 1 - (per * tid + j)]);
+        int total;
+        int before = block_exclusive_scan(mine_cnt, scratch, &total);
+        for (int j = 0; j < per; ++j) {
+            const int bin = nb - 1 - (per * tid + j);
+            const int h = static_cast<int>(hist[bin]);
+            if (before < krem_now && before + h >= krem_now) {
+                sh_digit = static_cast<uint32_t>(bin);
+                sh_above = before;
+            }
+            before += h;
+        }
+        __syncthreads();
+    };
+    // the same over the cluster's summed histogram; every CTA computes the same digit
     auto merged_digit = [&](const uint32_t *mine, int nb, int krem_now) {
         cluster_sync_all();  // every CTA's local histogram of this pass is complete
         for (int bin = tid; bin < nb; bin += NT) {
@@ -520,51 +542,120 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
             gsum[bin] = h;
         }
         __syncthreads();
-        const int per = nb / NT;
-        int mine_cnt = 0;
-        for (int j = 0; j < per; ++j)
-            mine_cnt += static_cast<int>(gsum[nb - 1 - (per * tid + j)]);
-        int total;
-        int before = block_exclusive_scan(mine_cnt, scratch, &total);
-        for (int j = 0; j < per; ++j) {
-            const int bin = nb - 1 - (per * tid + j);
-            const int h = static_cast<int>(gsum[bin]);
-            if (before < krem_now && before + h >= krem_now) {
-                sh_digit = static_cast<uint32_t>(bin);
-                sh_above = before;
-            }
-            before += h;
-        }
-        __syncthreads();
+        find_digit(gsum, nb, krem_now);
     };
     int krem = K;
     merged_digit(hbuf0, 4096, krem);
-    uint32_t prefix = sh_digit << 20, pmask = 0xFFF00000u;
+    const uint32_t d0 = sh_digit;
+    uint32_t prefix = d0 << 20, pmask = 0xFFF00000u;
     krem -= sh_above;
-    // passes 1 and 2: 10-bit digits over this CTA's keys that share the prefix
-#pragma unroll 1
-    for (int pass = 1; pass < 3; ++pass) {
-        const int shift = pass == 1 ? 10 : 0;
-        uint32_t *hb = (pass & 1) ? hbuf1 : hbuf0;
-        for (int i = tid; i < 1024; i += NT)
-            hb[i] = 0u;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    // The unit's keys in the threshold's 12-bit bin: usually few. Then every CTA gathers its
+    // own into a list, the lists are exchanged once, and each CTA finishes the exact
+    // threshold on the merged list alone (the same result in every CTA), and takes the
+    // counts of the CTAs before it from the lists too. Otherwise (many ties) the remaining
+    // two 10-bit digits are found over the cluster's summed histograms.
+    const bool listed = static_cast<int>(gsum[d0]) <= kMergeCap;   // the same in every CTA
+    int gt_before = 0, eq_before = 0;  // keys above / equal to the threshold in earlier CTAs
+    if (listed) {
+        if (tid == 0)
+            sh_lcnt = 0;
         __syncthreads();
-        for (int i = tid; i < nloc; i += NT) {
-            const uint32_t k = ks[i];
-            if ((k & pmask) == prefix)
-                atomicAdd(&hb[(k >> shift) & 1023u], 1u);
+        int above = 0;  // this thread's keys above the threshold bin
+        for (int i0 = 0; i0 < nloc; i0 += NT) {
+            const int i = i0 + tid;
+            const uint32_t k = i < nloc ? ks[i] : 0u;
+            const bool in = i < nloc && (k >> 20) == d0;
+            above += (i < nloc && (k >> 20) > d0) ? 1 : 0;
+            const unsigned bal = __ballot_sync(0xffffffffu, in);
+            int wbase = 0;
+            if (lane == 0 && bal)
+                wbase = atomicAdd(&sh_lcnt, __popc(bal));
+            wbase = __shfl_sync(0xffffffffu, wbase, 0);
+            if (in)
+                hbuf1[wbase + __popc(bal & lt_mask)] = k;
         }
-        merged_digit(hb, 1024, krem);
-        prefix |= sh_digit << shift;
-        pmask |= 1023u << shift;
-        krem -= sh_above;
+        int tot_above;
+        block_exclusive_scan(above, scratch, &tot_above);
+        if (tid == 0) {
+            sh_counts[0] = tot_above;
+            sh_counts[1] = sh_lcnt;
+        }
+        cluster_sync_all();  // every CTA's list and counts are in place
+        // the merged list in hbuf0 (free now: the peers read it before this barrier), the
+        // CTAs' lists in rank order; the lists before this CTA's end at `mine0`
+        int n_all = 0, mine0 = 0;
+        for (int r = 0; r < C; ++r) {
+            const int len = static_cast<int>(ld_cluster_u32(map_to_rank(&sh_counts[1], static_cast<uint32_t>(r))));
+            if (r < rank)
+                gt_before += static_cast<int>(ld_cluster_u32(map_to_rank(&sh_counts[0], static_cast<uint32_t>(r))));
+            for (int i = tid; i < len; i += NT)
+                hbuf0[n_all + i] = ld_cluster_u32(map_to_rank(hbuf1 + i, static_cast<uint32_t>(r)));
+            if (r == rank)
+                mine0 = n_all;
+            n_all += len;
+        }
         __syncthreads();
+        // passes 1 and 2 (10-bit digits) over the merged list, in gsum as a 1024-bin histogram
+#pragma unroll 1
+        for (int pass = 1; pass < 3; ++pass) {
+            const int shift = pass == 1 ? 10 : 0;
+            for (int i = tid; i < 1024; i += NT)
+                gsum[i] = 0u;
+            __syncthreads();
+            for (int i = tid; i < n_all; i += NT) {
+                const uint32_t k = hbuf0[i];
+                if ((k & pmask) == prefix)
+                    atomicAdd(&gsum[(k >> shift) & 1023u], 1u);
+            }
+            __syncthreads();
+            find_digit(gsum, 1024, krem);
+            prefix |= sh_digit << shift;
+            pmask |= 1023u << shift;
+            krem -= sh_above;
+            __syncthreads();
+        }
+        // keys above and equal to the threshold in the lists of the CTAs before this one
+        int cg = 0, ce = 0;
+        for (int i = tid; i < mine0; i += NT) {
+            const uint32_t k = hbuf0[i];
+            cg += k > prefix ? 1 : 0;
+            ce += k == prefix ? 1 : 0;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            cg += __shfl_xor_sync(0xffffffffu, cg, o);
+            ce += __shfl_xor_sync(0xffffffffu, ce, o);
+        }
+        int2 tot2;
+        warp_totals_exclusive_scan(cg, ce, scratch, &tot2);
+        gt_before += tot2.x;
+        eq_before += tot2.y;
+    } else {
+        // passes 1 and 2: 10-bit digits over this CTA's keys that share the prefix
+#pragma unroll 1
+        for (int pass = 1; pass < 3; ++pass) {
+            const int shift = pass == 1 ? 10 : 0;
+            uint32_t *hb = (pass & 1) ? hbuf1 : hbuf0;
+            for (int i = tid; i < 1024; i += NT)
+                hb[i] = 0u;
+            __syncthreads();
+            for (int i = tid; i < nloc; i += NT) {
+                const uint32_t k = ks[i];
+                if ((k & pmask) == prefix)
+                    atomicAdd(&hb[(k >> shift) & 1023u], 1u);
+            }
+            merged_digit(hb, 1024, krem);
+            prefix |= sh_digit << shift;
+            pmask |= 1023u << shift;
+            krem -= sh_above;
+            __syncthreads();
+        }
     }
     const uint32_t thr = prefix;  // exact key of the K-th largest score
     const int need_eq = krem;     // how many keys equal to thr are taken (lowest first)
 
     // ---- ordered compaction (as in select_kernel, offset by the CTAs before this one) ----
-    const unsigned lt_mask = (1u << lane) - 1u;
     const int span = (nloc + kWarps * 32 - 1) / (kWarps * 32) * 32;
     const int w0 = warp * span, w1 = min(nloc, w0 + span);
     int n_gt = 0, n_eq = 0;
@@ -577,16 +668,19 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
     }
     int2 tot;
     const int2 before = warp_totals_exclusive_scan(n_gt, n_eq, scratch, &tot);
-    if (tid == 0) {
-        sh_counts[0] = tot.x;
-        sh_counts[1] = tot.y;
+    if (!listed) {
+        if (tid == 0) {
+            sh_counts[0] = tot.x;
+            sh_counts[1] = tot.y;
+        }
+        cluster_sync_all();  // every CTA's counts are in place
+        for (int r = 0; r < rank; ++r) {
+            gt_before += static_cast<int>(ld_cluster_u32(map_to_rank(&sh_counts[0], static_cast<uint32_t>(r))));
+            eq_before += static_cast<int>(ld_cluster_u32(map_to_rank(&sh_counts[1], static_cast<uint32_t>(r))));
+        }
     }
-    cluster_sync_all();  // every CTA's counts are in place
-    int gt_before = before.x, eq_before = before.y;
-    for (int r = 0; r < rank; ++r) {
-        gt_before += static_cast<int>(ld_cluster_u32(map_to_rank(&sh_counts[0], static_cast<uint32_t>(r))));
-        eq_before += static_cast<int>(ld_cluster_u32(map_to_rank(&sh_counts[1], static_cast<uint32_t>(r))));
-    }
+    gt_before += before.x;
+    eq_before += before.y;
     for (int i0 = w0; i0 < w1; i0 += 32) {
         const int i = i0 + lane;
         const bool in = i < w1;

@@ -14,8 +14,9 @@ constexpr int kMaxBatch = 256;
 constexpr int kAttnThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2-5 softmax/epilogue
 constexpr int kSelectThreads = 1024;
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // bounded pipeline waits: 1 s
-// split-KV partial: G x 128 unnormalised outputs, then per head the running max and the
-// weight sum (base-2 logits)
+// split-KV partial: 128 x G unnormalised outputs (dim-major), then per head the running max
+// and the weight sum (base-2 logits); 16-byte aligned for G >= 2 (the merge reads it in
+// 16-byte pieces for G >= 4)
 constexpr int kPartialFloats(int G) { return G * kHeadDim + 2 * G; }
 
 // Everything the attention kernels read besides the tensor maps.

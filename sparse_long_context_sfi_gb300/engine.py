@@ -136,13 +136,14 @@ class SfiState:
         return self._side
 
     def make_plan(self, slow: np.ndarray, q, k_new, v_new, out, out_fp32=True, out_per_step=True,
-                  dense_only=False, events=None, t0=0, t1=None, pipeline=False):
+                  dense_only=False, events=None, t0=0, t1=None, pipeline=False, pipeline_group=0):
         """slow: uint8 [steps][B]; q/k_new/v_new/out: device tensors with a leading step axis.
         events: optional list of 2 * (t1 - t0) torch.cuda.Event(enable_timing=True) or None,
         recorded before (2 t) and after (2 t + 1) step t's attention kernel (None: not
         recorded). [t0, t1): the steps this plan covers (a run can be issued as several
-        consecutive plans). pipeline: run slow steps layer by layer, with the Selector and
-        compaction of each layer on a side stream beside the next layer's attention."""
+        consecutive plans). pipeline: run slow steps group of layers by group, with the
+        Selector and compaction of each group on a side stream beside the next group's
+        attention; pipeline_group: layers per group (0: about a quarter of the layers)."""
         t1 = slow.shape[0] if t1 is None else t1
         q, k_new, v_new = q[t0:t1], k_new[t0:t1], v_new[t0:t1]
         if out_per_step:
@@ -164,6 +165,7 @@ class SfiState:
             side, fork, join = self.side_stream()
             plan.side_stream, plan.fork_event, plan.join_event = (side.cuda_stream, fork.cuda_event,
                                                                   join.cuda_event)
+            plan.pipeline_group = int(pipeline_group)
         ev_arr = None
         if events is not None:
             assert len(events) == 2 * steps

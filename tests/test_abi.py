@@ -86,7 +86,8 @@ def test_decode_plan_layout_matches_header(lib):
     assert C.sizeof(sfi.SfiSparseMem) == 5 * 8
     assert sfi.SfiDecodePlan.masks.offset == 64 and sfi.SfiDecodePlan.events.offset == 80
     assert sfi.SfiDecodePlan.side_stream.offset == 88 and sfi.SfiDecodePlan.join_event.offset == 104
-    assert C.sizeof(sfi.SfiDecodePlan) == 112
+    assert sfi.SfiDecodePlan.pipeline_group.offset == 112
+    assert C.sizeof(sfi.SfiDecodePlan) == 120
 
 
 def test_layer_pipeline_needs_both_events(lib):

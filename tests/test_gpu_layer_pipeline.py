@@ -79,7 +79,7 @@ def issue(wl, steps, pipeline, graph=False):
     return st, slow, eager, out.cpu().numpy()
 
 
-def issue_stepwise(wl, steps, units, pipeline=True):
+def issue_stepwise(wl, steps, units, pipeline=True, pipeline_group=0):
     """The run issued one step per plan (with the pipeline, each slow step still forks and
     joins its side stream), reading back the GPU's selection for `units` after every slow
     step."""
@@ -92,7 +92,7 @@ def issue_stepwise(wl, steps, units, pipeline=True):
     run = sdev.DriftingRun(wl, st, slow, ins.q, ins.k_new, ins.v_new, out, ins.model,
                            pipeline=pipeline)
     plans = [st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, t0=t, t1=t + 1,
-                          pipeline=pipeline) for t in range(steps)]
+                          pipeline=pipeline, pipeline_group=pipeline_group) for t in range(steps)]
     stream = torch.cuda.Stream()
     s = stream.cuda_stream
     if 0 in run.edits:
@@ -113,11 +113,11 @@ def issue_stepwise(wl, steps, units, pipeline=True):
     return st, slow, out.cpu().numpy(), gpu_sel
 
 
-def check_run(wl, steps, units=None, check_steps=None, pipeline=True):
+def check_run(wl, steps, units=None, check_steps=None, pipeline=True, pipeline_group=0):
     cfg = wl.cfg
     all_units = list(range(cfg.n_layers * cfg.batch * cfg.n_kv_heads))
     units = all_units if units is None else units
-    st, slow, got, gpu_sel = issue_stepwise(wl, steps, units, pipeline)
+    st, slow, got, gpu_sel = issue_stepwise(wl, steps, units, pipeline, pipeline_group)
     del st
     torch.cuda.empty_cache()
     own = odecode.run(wl, steps=steps, units=units)
@@ -142,10 +142,12 @@ def check_run(wl, steps, units=None, check_steps=None, pipeline=True):
     return gpu_sel, slow
 
 
-def test_pipelined_four_layers_vs_oracle():
-    """128K-workload shape scaled to 3000 positions and 4 layers: every step, every unit."""
+@pytest.mark.parametrize("group", [1, 3, 4], ids=["layer_by_layer", "groups_3_1", "one_group"])
+def test_pipelined_four_layers_vs_oracle(group):
+    """128K-workload shape scaled to 3000 positions and 4 layers: every step, every unit; the
+    dense step launched per layer, in groups of 3 and 1 layers, and as one group."""
     wl = small("llama8b_ctx128k_l32", ctx=3000, ctx_lo=3000, n_layers=4, steps=40, mask_param=6)
-    sel, _ = check_run(wl, 40)
+    sel, _ = check_run(wl, 40, pipeline_group=group)
     assert len({t for t, _ in sel}) > 3
 
 

@@ -143,6 +143,31 @@ def test_dense_bf16_output():
     np.testing.assert_allclose(o16, o32, rtol=2 ** -8, atol=1e-6)
 
 
+def test_split_kv_merge_independent_of_arrival_order():
+    """One sequence of 20,000 positions: each unit's tiles are cut over ~19 CTAs, and the
+    contributor that takes the unit's last ticket (and merges) differs from launch to launch.
+    The merge runs over the contributors in CTA order, so repeated launches on the same
+    inputs give the same outputs and evidence bit for bit."""
+    import sparse_long_context_sfi_gb300 as sfi
+    wl = small("llama8b_ctx32k_b4", ctx=20000, batch=1, steps=2)
+    cfg = wl.cfg
+    st = sdev.make_state(wl, on_device=True)
+    ins = sdev.DeviceInputs(wl, 1, st.k.device, on_device=True)
+    out = torch.zeros((cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
+                      dtype=torch.float32, device=st.k.device)
+    first = None
+    for _ in range(24):
+        sfi.sfi_dense_decode_attn(st.kv, ins.q[0], out, True, st.scores, st.ws, st.ws_bytes)
+        torch.cuda.synchronize()
+        assert sfi.sfi_read_error(st.kv) == 0
+        got = (out.cpu().numpy().copy(), st.scores.cpu().numpy().copy())
+        if first is None:
+            first = got
+            continue
+        np.testing.assert_array_equal(got[0].view(np.uint32), first[0].view(np.uint32))
+        np.testing.assert_array_equal(got[1].view(np.uint32), first[1].view(np.uint32))
+
+
 def test_competing_heavy_positions_with_cancelling_values():
     """Two heavy positions (softmax weights about 0.59 and 0.29 against 599 flat ones) whose
     V rows cancel (+3 and -6 in every dimension): o = 0.0245, tolerance 2.25e-3. Rounding the

@@ -1,12 +1,13 @@
-"""Selector bit-exactness on the single-CTA kernel, against the oracle.
+"""Selector bit-exactness on both Selector kernels, against the oracle.
 
 sfi_select runs a cluster of CTAs per unit when the launch stays within about two waves
 (few units), and one 1024-thread CTA per unit otherwise: with the evidence of the unit's
 candidates staged in shared memory when they fit (up to 36,864), streamed from global
 memory when they do not. The ragged and multi-layer workloads run the one-CTA kernel in
-both modes, so it is held to the same bar as the clustered one: given identical evidence
-the selected positions equal the oracle's bit for bit (Top-K by fused score, ties to the
-lower position, written ascending; gist.science technical summary, section 2B).
+both modes, the 32K batch-4 workload the clustered one; each is held to the same bar:
+given identical evidence the selected positions equal the oracle's bit for bit (Top-K by
+fused score, ties to the lower position, written ascending; gist.science technical
+summary, section 2B).
 
 The evidence is written straight into the score buffer, in distributions that stress the
 radix select: heavy-tailed, all equal, two-valued, coarsely quantised (many ties at the
@@ -25,6 +26,7 @@ pytestmark = pytest.mark.gpu
 
 BATCH = 12                     # 12 sequences x 8 kv heads = 96 units: more than the clustered
                                # Selector takes on a 152-SM part (76)
+CL_BATCH = 4                   # 32 units: the clustered Selector (4 CTAs per unit)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -55,12 +57,12 @@ def evidence(kind: str, L: int, rng) -> np.ndarray:
 KINDS = ["heavy", "tie", "two", "quant", "signed"]
 
 
-def make_state(lo: int, hi: int, n_select: int, seed: int):
+def make_state(lo: int, hi: int, n_select: int, seed: int, batch: int = BATCH):
     from sparse_long_context_sfi_gb300.engine import SfiState
-    cfg = WORKLOADS["llama8b_ctx32k_b4"].scaled(batch=BATCH, ctx=hi, ctx_lo=lo, steps=2,
+    cfg = WORKLOADS["llama8b_ctx32k_b4"].scaled(batch=batch, ctx=hi, ctx_lo=lo, steps=2,
                                                  n_select=n_select)
     rng = np.random.default_rng(seed)
-    len0 = rng.integers(lo, hi + 1, BATCH)
+    len0 = rng.integers(lo, hi + 1, batch)
     S, W, K = cfg.n_sink, cfg.n_window, cfg.n_select
     len0[1] = S + W + K - 3      # fewer candidates than the budget: all kept
     len0[2] = S + W + K          # exactly as many
@@ -85,13 +87,18 @@ def run_select(cfg, st, rng, budget=None, scores=None):
     return f, st.sel_idx.cpu().numpy(), st.sel_cnt.cpu().numpy()
 
 
-@pytest.mark.parametrize("lo,hi,n_select", [
-    (12000, 36000, 1980),        # staged: every unit's candidates fit in shared memory
-    (37000, 41000, 1980),        # streamed: more than 36,864 candidates
-    (8192, 32768, 956),          # the ragged workload's budget and length range (staged)
-], ids=["staged", "streaming", "ragged_budget"])
-def test_single_cta_selector_bit_exact(lo, hi, n_select):
-    cfg, st, rng = make_state(lo, hi, n_select, seed=lo)
+@pytest.mark.parametrize("lo,hi,n_select,batch", [
+    (12000, 36000, 1980, BATCH),      # one CTA per unit, staged: candidates in shared memory
+    (37000, 41000, 1980, BATCH),      # one CTA per unit, streamed: more than 36,864 candidates
+    (8192, 32768, 956, BATCH),        # the ragged workload's budget and length range (staged)
+    (12000, 36000, 1980, CL_BATCH),   # clustered: threshold-bin lists, or radix on many ties
+    (37000, 41000, 956, CL_BATCH),    # clustered, long units
+], ids=["staged", "streaming", "ragged_budget", "clustered", "clustered_long"])
+def test_selector_bit_exact(lo, hi, n_select, batch):
+    """Both Selector kernels against the oracle on evidence of every distribution: heavy
+    tails (the clustered kernel exchanges the threshold bin's keys as lists), all equal and
+    two-valued (its fallback to radix passes over the cluster's histograms)."""
+    cfg, st, rng = make_state(lo, hi, n_select, seed=lo + batch, batch=batch)
     f, sel, cnt = run_select(cfg, st, rng)
     S, W, K = cfg.n_sink, cfg.n_window, cfg.n_select
     H = cfg.n_kv_heads
