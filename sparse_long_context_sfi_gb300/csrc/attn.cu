@@ -474,22 +474,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // Sparse step over tile ranges: every active sequence has tiles_per_unit tiles, so the
     // tile space depends only on `active` (an input complete at launch) and is laid out before
     // the wait on the preceding grid; the lengths read after it only decide which units give
-    // output (c.len[b] <= 0: none). The packed counts of the range's first unit (packed
-    // memory, complete at launch) are loaded before the wait as well: lane 0 the packed row
-    // count, lane 1 the selection count. (Requesting the first tiles' boxes here too was
-    // measured slower on the ragged batch-32 workload: the late CTAs' set-up is not hidden.)
-    int tr_meta = 0;
+    // output (c.len[b] <= 0: none). Nothing else is read before the wait: loading the first
+    // unit's packed counts, or requesting its first packed tiles, there as well was measured
+    // slower on the ragged batch-32 workload (by 2.1 and 0.4 us): the CTAs that enter last
+    // carry their set-up on the critical path.
     if (!clustered && !DENSE) {
         for (int b = tid; b < B; b += kAttnThreads)
             c.nt[b] = (p.active ? p.active[b] : 1) ? p.tiles_per_unit : 0;
         __syncthreads();
         tile_space();
-        if (warp == 0 && n_tiles > 0) {
-            int layer, b, kvh, t;
-            first_tile(layer, b, kvh, t);
-            const int u = (layer * B + b) * Hkv + kvh;
-            tr_meta = lane == 0 ? __ldg(p.comp_rows + u) : lane == 1 ? __ldg(p.sel_cnt + u) : 0;
-        }
     }
     pdl_wait();
     if (!clustered && !DENSE) {
@@ -755,7 +748,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     if (!DENSE) {
                         int rows_c, sel;
                         {
-                            cur_meta = seg == 0 ? tr_meta : nxt_meta;
+                            cur_meta = seg == 0 ? (lane == 0 ? __ldg(p.comp_rows + u)
+                                                   : lane == 1 ? __ldg(p.sel_cnt + u) : 0)
+                                                : nxt_meta;
                             // the next segment of the range, if any: its counts, loaded now
                             if (i + (ntiles_of(b) - t) < n_tiles) {
                                 int nl = layer, nb = b, nk = kvh;

@@ -419,6 +419,7 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
 
 constexpr int kClusterKeyCap = 33280;  // candidates per CTA (a 131K context in 4 CTAs)
 constexpr int kMergeCap = 4096;        // threshold-bin keys exchanged as lists (else radix)
+constexpr int kMaxCluster = 4;         // CTAs per unit (the host picks 4 or 2)
 
 size_t select_cluster_smem_bytes()
 {
@@ -533,13 +534,27 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
         __syncthreads();
     };
     // the same over the cluster's summed histogram; every CTA computes the same digit
+    // (this thread's nb / NT <= 4 bins from each of the C <= 4 CTAs: every remote load is
+    // issued before the first is used, so the sum costs one round trip, not C x nb / NT)
     auto merged_digit = [&](const uint32_t *mine, int nb, int krem_now) {
         cluster_sync_all();  // every CTA's local histogram of this pass is complete
-        for (int bin = tid; bin < nb; bin += NT) {
+        const int per = nb / NT;
+        uint32_t v[kMaxCluster][4];
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                v[r][j] = (r < C && j < per)
+                              ? ld_cluster_u32(map_to_rank(mine + tid + j * NT, static_cast<uint32_t>(r)))
+                              : 0u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
             uint32_t h = 0;
-            for (int r = 0; r < C; ++r)
-                h += ld_cluster_u32(map_to_rank(mine + bin, static_cast<uint32_t>(r)));
-            gsum[bin] = h;
+#pragma unroll
+            for (int r = 0; r < kMaxCluster; ++r)
+                h += v[r][j];
+            if (j < per)
+                gsum[tid + j * NT] = h;
         }
         __syncthreads();
         find_digit(gsum, nb, krem_now);
@@ -584,16 +599,32 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
         cluster_sync_all();  // every CTA's list and counts are in place
         // the merged list in hbuf0 (free now: the peers read it before this barrier), the
         // CTAs' lists in rank order; the lists before this CTA's end at `mine0`
-        int n_all = 0, mine0 = 0;
-        for (int r = 0; r < C; ++r) {
-            const int len = static_cast<int>(ld_cluster_u32(map_to_rank(&sh_counts[1], static_cast<uint32_t>(r))));
+        int lens[kMaxCluster], gts[kMaxCluster];
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) {
+            lens[r] = r < C ? static_cast<int>(ld_cluster_u32(map_to_rank(&sh_counts[1], static_cast<uint32_t>(r)))) : 0;
+            gts[r] = r < C ? static_cast<int>(ld_cluster_u32(map_to_rank(&sh_counts[0], static_cast<uint32_t>(r)))) : 0;
+        }
+        int n_all = 0, mine0 = 0, longest = 0, starts[kMaxCluster];
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) {
+            starts[r] = n_all;
             if (r < rank)
-                gt_before += static_cast<int>(ld_cluster_u32(map_to_rank(&sh_counts[0], static_cast<uint32_t>(r))));
-            for (int i = tid; i < len; i += NT)
-                hbuf0[n_all + i] = ld_cluster_u32(map_to_rank(hbuf1 + i, static_cast<uint32_t>(r)));
+                gt_before += gts[r];
             if (r == rank)
                 mine0 = n_all;
-            n_all += len;
+            n_all += lens[r];
+            longest = max(longest, lens[r]);
+        }
+        for (int i = tid; i < longest; i += NT) {
+            uint32_t x[kMaxCluster];
+#pragma unroll
+            for (int r = 0; r < kMaxCluster; ++r)
+                x[r] = i < lens[r] ? ld_cluster_u32(map_to_rank(hbuf1 + i, static_cast<uint32_t>(r))) : 0u;
+#pragma unroll
+            for (int r = 0; r < kMaxCluster; ++r)
+                if (i < lens[r])
+                    hbuf0[starts[r] + i] = x[r];
         }
         __syncthreads();
         // passes 1 and 2 (10-bit digits) over the merged list, in gsum as a 1024-bin histogram
@@ -674,9 +705,16 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
             sh_counts[1] = tot.y;
         }
         cluster_sync_all();  // every CTA's counts are in place
-        for (int r = 0; r < rank; ++r) {
-            gt_before += static_cast<int>(ld_cluster_u32(map_to_rank(&sh_counts[0], static_cast<uint32_t>(r))));
-            eq_before += static_cast<int>(ld_cluster_u32(map_to_rank(&sh_counts[1], static_cast<uint32_t>(r))));
+        uint32_t g4[kMaxCluster], e4[kMaxCluster];
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) {
+            g4[r] = r < rank ? ld_cluster_u32(map_to_rank(&sh_counts[0], static_cast<uint32_t>(r))) : 0u;
+            e4[r] = r < rank ? ld_cluster_u32(map_to_rank(&sh_counts[1], static_cast<uint32_t>(r))) : 0u;
+        }
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) {
+            gt_before += static_cast<int>(g4[r]);
+            eq_before += static_cast<int>(e4[r]);
         }
     }
     gt_before += before.x;
