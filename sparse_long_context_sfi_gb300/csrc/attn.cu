@@ -25,6 +25,7 @@
 //   * Every wait is bounded; a wait that gives up flags SFI_DEVERR_TIMEOUT, drains the
 //     CTA's copies and MMAs, frees TMEM and returns.
 #include <math.h>
+#include <cstddef>
 
 #include <mutex>
 
@@ -105,6 +106,18 @@ struct Ctrl {
 };
 
 constexpr int kSmemBytes = kCtrlOff + static_cast<int>(sizeof(Ctrl)) + 1024;
+
+// The mbarriers of Ctrl, fullK[0] through meta_full[kMetaRing - 1], lie back to back; the
+// softmax-group ones (s_free, p_full, o_free, gsync) expect one arrival per softmax warp,
+// the others one. Set up in one plain loop over that range.
+constexpr int kNBars = static_cast<int>(
+    (offsetof(Ctrl, meta_full) + kMetaRing * sizeof(uint64_t) - offsetof(Ctrl, fullK)) / sizeof(uint64_t));
+constexpr int bar_index(size_t off) { return static_cast<int>((off - offsetof(Ctrl, fullK)) / sizeof(uint64_t)); }
+constexpr uint64_t kFourArrivals = (3ull << bar_index(offsetof(Ctrl, s_free))) |
+                                   (3ull << bar_index(offsetof(Ctrl, p_full))) |
+                                   (3ull << bar_index(offsetof(Ctrl, o_free))) |
+                                   (1ull << bar_index(offsetof(Ctrl, gsync)));
+static_assert(kNBars == 4 * kStages + 12 + 5 + kMetaRing && kNBars <= 64, "mbarriers of Ctrl");
 
 // Warp-wide max of non-NaN floats in one redux: the float bits as a signed integer, with the
 // magnitude bits of negatives flipped, order like the floats (-inf lowest, -0 below +0).
@@ -226,69 +239,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int rank = static_cast<int>(blockIdx.x) % p.cluster;
         cl_t0 = rank * p.tiles_per_unit / p.cluster;
         cl_n = (rank + 1) * p.tiles_per_unit / p.cluster - cl_t0;
+        // tiles requested before the wait: those of packed rows only, at most kStages
+        cl_pre = max(0, min(min(kStages, cl_n), 64 * p.n_cbox / kTile - cl_t0));
     }
     if (warp == 0) {
         // the barriers of the set-up, spread over the warp's lanes (its fence then publishes
-        // them all): index -> (barrier, expected arrivals)
-        constexpr int kRing = 4 * kStages, kNBars = kRing + kMetaRing + 12 + 5;
-        for (int idx = lane; idx < kNBars; idx += 32) {
-            uint64_t *bar = nullptr;
-            uint32_t cnt = 1;
-            if (idx < kRing) {
-                const int r = idx / kStages, st = idx % kStages;
-                bar = r == 0 ? &c.fullK[st] : r == 1 ? &c.fullV[st] : r == 2 ? &c.emptyK[st] : &c.emptyV[st];
-            } else if (idx < kRing + kMetaRing) {
-                bar = &c.meta_full[idx - kRing];
-            } else if (idx < kRing + kMetaRing + 12) {
-                const int j = idx - kRing - kMetaRing, bb = j & 1;
-                switch (j >> 1) {
-                case 0: bar = &c.s_full[bb]; break;
-                case 1: bar = &c.s_free[bb]; cnt = 4; break;
-                case 2: bar = &c.p_full[bb]; cnt = 4; break;
-                case 3: bar = &c.o_full[bb]; break;
-                case 4: bar = &c.o_free[bb]; cnt = 4; break;
-                default: bar = &c.q_free[bb]; break;
-                }
-            } else {
-                switch (idx - kRing - kMetaRing - 12) {
-                case 0: bar = &c.gsync; cnt = 4; break;
-                case 1: bar = &c.drain; break;
-                case 2: bar = &c.unit_meta; break;
-                case 3: bar = &c.q_full; break;
-                default: bar = &c.cl_ready; cnt = 1; break;
-                }
-            }
-            mbar_init(bar, cnt);
-        }
+        // them all)
+        uint64_t *bars = &c.fullK[0];
+        for (int idx = lane; idx < kNBars; idx += 32)
+            mbar_init(bars + idx, ((kFourArrivals >> idx) & 1ull) ? 4u : 1u);
         mbar_fence_init();
         __syncwarp();
-        // The packed memory is complete before this launch starts (sfi_compact and
-        // sfi_select let their dependents start only after their writes), so the slice's
-        // first tiles of packed rows are requested here, before the rest of the set-up and
-        // the wait on the preceding grid: every box of them, since the unit's packed row
-        // count is known only after the wait (rows past it are masked then). Their arrival on
-        // full lets the score MMAs start as soon as the query lands.
-        if constexpr (clustered) {
-            const int packed_tiles = 64 * p.n_cbox / kTile;   // tiles of packed rows only
-            cl_pre = max(0, min(min(kStages, cl_n), packed_tiles - cl_t0));
-            const int h2 = lane >> 4, j16 = lane & 15;
-            for (int i = 0; i < cl_pre; ++i) {
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&c.fullK[i], 2u * 2u * 64u * 128u +
-                                                           ((p.test_stall && blockIdx.x == 0 && i == 0) ? 16u : 0u));
-                    mbar_arrive_expect_tx(&c.fullV[i], 2u * 2u * 64u * 128u);
-                }
-                __syncwarp();
-                if (j16 < 4) {
-                    const int k = ((cl_t0 + i) * kTile + 64 * h2) >> 6;
-                    const int kv = j16 >> 1, half = j16 & 1;
-                    tma_load_2d(smem + i * kStageBytes + kv * 2 * kChunkBytes + half * kChunkBytes +
-                                    64 * h2 * 128,
-                                kv ? &tm_vc : &tm_kc, kv ? &c.fullV[i] : &c.fullK[i], 64 * half,
-                                cl_u * p.comp_cap + 64 * k);
-                }
-            }
-        }
+        // clustered: the query's bytes, requested right after the wait
+        if (clustered && lane == 0)
+            mbar_arrive_expect_tx(&c.q_full, 2u * G * 128u);
     }
     if (tid == 0) {
         c.abort = 0;
@@ -303,14 +267,41 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         reinterpret_cast<uint4 *>(smem + kQOff)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
     // Clustered fast step: one unit per cluster, its tiles split evenly over the cluster's
-    // CTAs, which merge their partials through distributed shared memory. The cluster
-    // barrier publishes the mbarrier initialisation and the TMEM base cluster-wide.
+    // CTAs, which merge their partials through distributed shared memory. The peers need
+    // only this CTA's mbarrier initialisation, which fence.mbarrier_init has published, so
+    // the cluster arrival is relaxed; the CTA barrier publishes the TMEM base.
     if (clustered) {
         // arrive now, wait only before the first access to a peer's shared memory (the merge)
         tc_fence_before();
-        cluster_arrive_release();
+        cluster_arrive_relaxed();
         __syncthreads();
         tc_fence_after();
+    }
+    // The packed memory is complete before this launch starts (sfi_compact and
+    // sfi_select let their dependents start only after their writes), so the slice's
+    // first tiles of packed rows are requested before the wait on the preceding grid: every
+    // box of them, since the unit's packed row count is known only after the wait (rows
+    // past it are masked then). Their arrival on full lets the score MMAs start as soon as
+    // the query lands. A softmax warp issues them (it is idle until the first scores), so
+    // the producer warp reaches the wait, and the query load, without them.
+    if (clustered && warp == 2) {
+        const int h2 = lane >> 4, j16 = lane & 15;
+        for (int i = 0; i < cl_pre; ++i) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&c.fullK[i], 2u * 2u * 64u * 128u +
+                                                       ((p.test_stall && blockIdx.x == 0 && i == 0) ? 16u : 0u));
+                mbar_arrive_expect_tx(&c.fullV[i], 2u * 2u * 64u * 128u);
+            }
+            __syncwarp();
+            if (j16 < 4) {
+                const int k = ((cl_t0 + i) * kTile + 64 * h2) >> 6;
+                const int kv = j16 >> 1, half = j16 & 1;
+                tma_load_2d(smem + i * kStageBytes + kv * 2 * kChunkBytes + half * kChunkBytes +
+                                64 * h2 * 128,
+                            kv ? &tm_vc : &tm_kc, kv ? &c.fullV[i] : &c.fullK[i], 64 * half,
+                            cl_u * p.comp_cap + 64 * k);
+            }
+        }
     }
 
     // Tile t of the slice in ring stage i % kStages (producer warp, clustered): its row mask
@@ -520,17 +511,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     if (warp == 0 && clustered) {
         // ========================= TMA producer, clustered fast step =======================
-        // After the wait: the query first (its own barrier: it may come from the preceding
-        // kernel), then the unit's length, activity and packed counts in one round, then the
-        // row masks of the tiles requested before the wait and the rest of the slice; the
-        // window tile gets the new row written into the cache (fused append) before its boxes
-        // are issued.
-        const int layer = cl_u / (Hkv * B), b = (cl_u / Hkv) % B, kvh = cl_u % Hkv;
-        if (lane == 0)
-            mbar_arrive_expect_tx(&c.q_full, 2u * G * 128u);
-        __syncwarp();
+        // After the wait: the query first (its own barrier, armed before the wait: it may come
+        // from the preceding kernel), then the unit's length, activity and packed counts in
+        // one round, then the row masks of the tiles requested before the wait and the rest of
+        // the slice; the window tile gets the new row written into the cache (fused append)
+        // before its boxes are issued.
         if (lane < 2)
             tma_load_2d(smem + kQOff + lane * kOpChunk, &tm_q, &c.q_full, 64 * lane, cl_u * G);
+        const int layer = cl_u / (Hkv * B), b = (cl_u / Hkv) % B, kvh = cl_u % Hkv;
         int v = 0;
         if (lane == 0)
             v = p.seq_len[b];

@@ -420,6 +420,7 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
 constexpr int kClusterKeyCap = 33280;  // candidates per CTA (a 131K context in 4 CTAs)
 constexpr int kMergeCap = 4096;        // threshold-bin keys exchanged as lists (else radix)
 constexpr int kMaxCluster = 4;         // CTAs per unit (the host picks 4 or 2)
+static_assert(NT == 1024, "the cluster's histogram passes take 4096 and 1024 bins");
 
 size_t select_cluster_smem_bytes()
 {
@@ -534,27 +535,35 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
         __syncthreads();
     };
     // the same over the cluster's summed histogram; every CTA computes the same digit
-    // (this thread's nb / NT <= 4 bins from each of the C <= 4 CTAs: every remote load is
-    // issued before the first is used, so the sum costs one round trip, not C x nb / NT)
+    // (this thread's nb / NT bins, 4 consecutive ones for the 4096-bin pass, from each of the
+    // C <= 4 CTAs: one 16-byte remote load per CTA, all issued before the first is used)
     auto merged_digit = [&](const uint32_t *mine, int nb, int krem_now) {
         cluster_sync_all();  // every CTA's local histogram of this pass is complete
-        const int per = nb / NT;
-        uint32_t v[kMaxCluster][4];
+        if (nb == 4 * NT) {
+            uint4 v[kMaxCluster];
 #pragma unroll
-        for (int r = 0; r < kMaxCluster; ++r)
+            for (int r = 0; r < kMaxCluster; ++r)
+                v[r] = r < C ? ld_cluster_v4_u32(map_to_rank(mine + 4 * tid, static_cast<uint32_t>(r)))
+                             : make_uint4(0u, 0u, 0u, 0u);
+            uint4 h = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                v[r][j] = (r < C && j < per)
-                              ? ld_cluster_u32(map_to_rank(mine + tid + j * NT, static_cast<uint32_t>(r)))
-                              : 0u;
+            for (int r = 0; r < kMaxCluster; ++r) {
+                h.x += v[r].x;
+                h.y += v[r].y;
+                h.z += v[r].z;
+                h.w += v[r].w;
+            }
+            reinterpret_cast<uint4 *>(gsum)[tid] = h;
+        } else {
+            uint32_t v[kMaxCluster];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+            for (int r = 0; r < kMaxCluster; ++r)
+                v[r] = r < C ? ld_cluster_u32(map_to_rank(mine + tid, static_cast<uint32_t>(r))) : 0u;
             uint32_t h = 0;
 #pragma unroll
             for (int r = 0; r < kMaxCluster; ++r)
-                h += v[r][j];
-            if (j < per)
-                gsum[tid + j * NT] = h;
+                h += v[r];
+            gsum[tid] = h;
         }
         __syncthreads();
         find_digit(gsum, nb, krem_now);

@@ -368,6 +368,13 @@ __device__ __forceinline__ void cluster_arrive_release()
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
+// Arrival without release semantics: enough where the only thing the peers need from this
+// CTA is its mbarrier initialisation, published by fence.mbarrier_init before it.
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_wait_acquire()
 {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -422,6 +429,17 @@ __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_addr)
 {
     uint32_t v;
     asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+// Four consecutive 32-bit words of a cluster shared-memory address (16-byte aligned).
+__device__ __forceinline__ uint4 ld_cluster_v4_u32(uint32_t cluster_addr)
+{
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
     return v;
 }
 
