@@ -1164,12 +1164,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 return false;
             if (!c.last_flag)
                 return true;
-            // One-pass online merge over the contributors in CTA order (this CTA's own
-            // partial from registers at its place), so the rounding does not depend on which
-            // contributor arrived last; the others are read in batches (8 for groups up to 4,
-            // else 4) so that their loads overlap: a unit split over ~20 CTAs then takes 3
-            // rounds of L2 latency instead of 5.
-            constexpr int kMB = G <= 4 ? 8 : 4;
+            // Merge over the contributors in CTA order (this CTA's own partial from registers
+            // at its place), so the rounding does not depend on which contributor arrived
+            // last, in chunks of up to 32 contributors. Lane k of every softmax warp loads
+            // contributor c0 + k's maxima and weight sums; a warp max gives the chunk's
+            // maximum M, and each contributor's weight 2^(m_k - M) is computed once, in its
+            // lane, rather than by every thread. Each thread then sums its dim of the
+            // contributors' outputs with those weights (taken by shuffle), kSB contributors'
+            // loads at a time, the first kSB issued together with the maxima. (A per-thread
+            // online merge spent ~2.9 us per 8 contributors: a one-sequence launch, whose units
+            // are split over ~20 CTAs, ended ~9 us after its last tile.)
+            constexpr int kSB = G <= 4 ? 8 : 4;
             float M[G], Le[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) {
@@ -1179,58 +1184,84 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             // u may be the last segment of cf's range (slot 1)
             const bool cf_tail = static_cast<long long>(cf) * T / P < su;
-            for (int c0 = cf; c0 <= cl; c0 += kMB) {
-                float mc[kMB][G], lc[kMB][G], ac[kMB][G];
-                bool use[kMB];
+            auto part_of = [&](int cc) -> const float * {
+                const int sl = (cc == cf && cf_tail) ? 1 : 0;
+                return p.partials + (2 * static_cast<size_t>(cc) + sl) * kPartialFloats(G);
+            };
+            for (int c0 = cf; c0 <= cl; c0 += 32) {
+                const int nk = min(32, cl - c0 + 1);
+                // this dim of contributors c0 + k0 .. c0 + k0 + kSB - 1
+                float a[kSB][G];
+                auto load_out = [&](int k0) {
 #pragma unroll
-                for (int k = 0; k < kMB; ++k) {
-                    const int cc = c0 + k;
-                    use[k] = cc <= cl && cc != static_cast<int>(blockIdx.x);
-                    const int sl = (cc == cf && cf_tail) ? 1 : 0;
-                    const float *pc = p.partials +
-                                      (2 * static_cast<size_t>(use[k] ? cc : blockIdx.x) + sl) *
-                                          kPartialFloats(G);
-                    if constexpr (G >= 4) {
+                    for (int j = 0; j < kSB; ++j) {
+                        const int cc = c0 + k0 + j;
+                        if (k0 + j < nk && cc != static_cast<int>(blockIdx.x)) {
+                            const float *pc = part_of(cc);
+                            if constexpr (G >= 4) {
 #pragma unroll
-                        for (int h = 0; h < G; h += 4) {
-                            float4 m4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-                            float4 l4 = make_float4(0.f, 0.f, 0.f, 0.f), a4 = l4;
-                            if (use[k]) {
-                                m4 = __ldcg(reinterpret_cast<const float4 *>(pc + G * kHeadDim + h));
-                                l4 = __ldcg(reinterpret_cast<const float4 *>(pc + G * kHeadDim + G + h));
-                                a4 = __ldcg(reinterpret_cast<const float4 *>(pc + row * G + h));
+                                for (int h = 0; h < G; h += 4) {
+                                    const float4 x = __ldcg(reinterpret_cast<const float4 *>(pc + row * G + h));
+                                    a[j][h] = x.x;
+                                    a[j][h + 1] = x.y;
+                                    a[j][h + 2] = x.z;
+                                    a[j][h + 3] = x.w;
+                                }
+                            } else {
+#pragma unroll
+                                for (int h = 0; h < G; ++h)
+                                    a[j][h] = __ldcg(pc + row * G + h);
                             }
-                            mc[k][h] = m4.x; mc[k][h + 1] = m4.y; mc[k][h + 2] = m4.z; mc[k][h + 3] = m4.w;
-                            lc[k][h] = l4.x; lc[k][h + 1] = l4.y; lc[k][h + 2] = l4.z; lc[k][h + 3] = l4.w;
-                            ac[k][h] = a4.x; ac[k][h + 1] = a4.y; ac[k][h + 2] = a4.z; ac[k][h + 3] = a4.w;
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < G; ++h)
+                                a[j][h] = (k0 + j < nk) ? acc[h] : 0.f;
+                        }
+                    }
+                };
+                load_out(0);
+                // lane k: maxima and weight sums of contributor c0 + k
+                float mk[G], lk[G];
+                {
+                    const int ck = c0 + lane;
+                    if (lane < nk && ck != static_cast<int>(blockIdx.x)) {
+                        const float *pc = part_of(ck);
+#pragma unroll
+                        for (int h = 0; h < G; ++h) {
+                            mk[h] = __ldcg(pc + G * kHeadDim + h);
+                            lk[h] = __ldcg(pc + G * kHeadDim + G + h);
                         }
                     } else {
 #pragma unroll
                         for (int h = 0; h < G; ++h) {
-                            mc[k][h] = use[k] ? __ldcg(pc + G * kHeadDim + h) : -INFINITY;
-                            lc[k][h] = use[k] ? __ldcg(pc + G * kHeadDim + G + h) : 0.f;
-                            ac[k][h] = use[k] ? __ldcg(pc + row * G + h) : 0.f;
-                        }
-                    }
-                    if (c0 + k == static_cast<int>(blockIdx.x)) {
-#pragma unroll
-                        for (int h = 0; h < G; ++h) {
-                            mc[k][h] = fm[h];
-                            lc[k][h] = fle[h];
-                            ac[k][h] = acc[h];
+                            mk[h] = lane < nk ? fm[h] : -INFINITY;
+                            lk[h] = lane < nk ? fle[h] : 0.f;
                         }
                     }
                 }
+                float wk[G];
 #pragma unroll
-                for (int k = 0; k < kMB; ++k) {
+                for (int h = 0; h < G; ++h) {
+                    const float mn = fmaxf(M[h], warp_max(mk[h]));
+                    const float mb = (mn == -INFINITY) ? 0.f : mn;
+                    const float sc = ex2_approx(M[h] - mb);     // 0 while nothing is merged
+                    wk[h] = ex2_approx(mk[h] - mb);              // 0 for an empty contributor
+                    o[h] *= sc;
+                    Le[h] = fmaf(Le[h], sc, warp_sum(wk[h] * lk[h]));
+                    M[h] = mn;
+                }
+#pragma unroll 1
+                for (int k0 = 0; k0 < nk; k0 += kSB) {
+                    if (k0 > 0)
+                        load_out(k0);
 #pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        const float mn = fmaxf(M[h], mc[k][h]);
-                        const float a = (M[h] == -INFINITY) ? 0.f : exp2f(M[h] - mn);
-                        const float w = (mc[k][h] == -INFINITY) ? 0.f : exp2f(mc[k][h] - mn);
-                        Le[h] = Le[h] * a + w * lc[k][h];
-                        o[h] = o[h] * a + w * ac[k][h];
-                        M[h] = mn;
+                    for (int j = 0; j < kSB; ++j) {
+#pragma unroll
+                        for (int h = 0; h < G; ++h) {
+                            const float w = __shfl_sync(0xffffffffu, wk[h], (k0 + j) & 31);
+                            if (k0 + j < nk)
+                                o[h] = fmaf(w, a[j][h], o[h]);
+                        }
                     }
                 }
             }
