@@ -145,6 +145,102 @@ __device__ __forceinline__ int2 warp_totals_exclusive_scan(int a, int b, int *sc
     return r;
 }
 
+// Digit of the histogram hist (nb = 4 NT or NT bins) where the running count from the top
+// first reaches krem: the bin in *digit and the count above it in *above (shared memory).
+// Thread t sums its nb / NT consecutive bins from the top (one 16-byte load for 4 NT bins);
+// every warp then scans the 32 warp sums itself, so the search takes two barriers, the last
+// of which publishes the result. Uses scratch[0, kWarps).
+__device__ __forceinline__ void find_top_digit(const uint32_t *hist, int nb, int krem, int *scratch,
+                                               uint32_t *digit, int *above)
+{
+    static_assert(kWarps == 32, "one warp sum per lane");
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t hb[4] = {0u, 0u, 0u, 0u};   // this thread's bins, descending
+    if (nb == 4 * NT) {
+        const uint4 v = reinterpret_cast<const uint4 *>(hist)[NT - 1 - tid];
+        hb[0] = v.w;
+        hb[1] = v.z;
+        hb[2] = v.y;
+        hb[3] = v.x;
+    } else {
+        hb[0] = hist[NT - 1 - tid];
+    }
+    const int per = nb / NT;
+    const int mine = static_cast<int>(hb[0] + hb[1] + hb[2] + hb[3]);
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += y;
+    }
+    if (lane == 31)
+        scratch[warp] = incl;
+    __syncthreads();
+    const int ws = scratch[lane];
+    int wincl = ws;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wincl, o);
+        if (lane >= o)
+            wincl += y;
+    }
+    int before = __shfl_sync(0xffffffffu, wincl - ws, warp) + incl - mine;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int h = static_cast<int>(hb[j]);
+        if (j < per && before < krem && before + h >= krem) {
+            *digit = static_cast<uint32_t>(nb - 1 - (per * tid + j));
+            *above = before;
+        }
+        before += h;
+    }
+    __syncthreads();
+}
+
+// Block-wide sum of one int per thread, in one barrier. Uses scratch[0, kWarps); the caller
+// keeps the region untouched until every thread has returned.
+__device__ __forceinline__ int block_total(int x, int *scratch)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0)
+        scratch[warp] = x;
+    __syncthreads();
+    int t = scratch[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        t += __shfl_xor_sync(0xffffffffu, t, o);
+    return t;
+}
+
+// warp_totals_exclusive_scan in one barrier: every warp scans the 32 pairs itself. Uses
+// scratch[0, 2 kWarps); the caller keeps the region untouched until every thread has returned.
+__device__ __forceinline__ int2 warp_pairs_exclusive_scan(int a, int b, int *scratch, int2 *total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+        scratch[warp] = a;
+        scratch[kWarps + warp] = b;
+    }
+    __syncthreads();
+    const int x = scratch[lane], y = scratch[kWarps + lane];
+    int xi = x, yi = y;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int xu = __shfl_up_sync(0xffffffffu, xi, o);
+        const int yu = __shfl_up_sync(0xffffffffu, yi, o);
+        if (lane >= o) {
+            xi += xu;
+            yi += yu;
+        }
+    }
+    *total = make_int2(__shfl_sync(0xffffffffu, xi, 31), __shfl_sync(0xffffffffu, yi, 31));
+    return make_int2(__shfl_sync(0xffffffffu, xi - x, warp), __shfl_sync(0xffffffffu, yi - y, warp));
+}
+
 // At most 56 registers per thread: a 1024-thread CTA then takes 7/8 of the register file
 // instead of all of it, so a launch under a profiler, which may need a few more, still fits.
 __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
@@ -431,7 +527,8 @@ size_t select_cluster_smem_bytes()
 
 __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
 {
-    __shared__ int scratch[2 * kWarps + 2];
+    __shared__ int scratch[2 * kWarps + 2];    // digit searches and the compaction's scan
+    __shared__ int scratch2[2 * kWarps];       // the list path's totals and scan
     __shared__ uint32_t sh_digit;
     __shared__ int sh_above;
     __shared__ int sh_counts[2];  // this CTA's (greater, equal) keys for the ordered output,
@@ -515,24 +612,9 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
         atomicAdd(&hbuf0[k >> 20], 1u);
     }
     // digit of the histogram hist (nb bins) where the running count from the top first
-    // reaches krem (sh_digit, and the count above it in sh_above)
+    // reaches krem (sh_digit, and the count above it in sh_above; two barriers)
     auto find_digit = [&](const uint32_t *hist, int nb, int krem_now) {
-        const int per = nb / NT;
-        int mine_cnt = 0;
-        for (int j = 0; j < per; ++j)
-            mine_cnt += static_cast<int>(hist[nb - 1 - (per * tid + j)]);
-        int total;
-        int before = block_exclusive_scan(mine_cnt, scratch, &total);
-        for (int j = 0; j < per; ++j) {
-            const int bin = nb - 1 - (per * tid + j);
-            const int h = static_cast<int>(hist[bin]);
-            if (before < krem_now && before + h >= krem_now) {
-                sh_digit = static_cast<uint32_t>(bin);
-                sh_above = before;
-            }
-            before += h;
-        }
-        __syncthreads();
+        find_top_digit(hist, nb, krem_now, scratch, &sh_digit, &sh_above);
     };
     // the same over the cluster's summed histogram; every CTA computes the same digit
     // (this thread's nb / NT bins, 4 consecutive ones for the 4096-bin pass, from each of the
@@ -599,8 +681,7 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
             if (in)
                 hbuf1[wbase + __popc(bal & lt_mask)] = k;
         }
-        int tot_above;
-        block_exclusive_scan(above, scratch, &tot_above);
+        const int tot_above = block_total(above, scratch2);
         if (tid == 0) {
             sh_counts[0] = tot_above;
             sh_counts[1] = sh_lcnt;
@@ -635,25 +716,26 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
                 if (i < lens[r])
                     hbuf0[starts[r] + i] = x[r];
         }
+        // passes 1 and 2 (10-bit digits) over the merged list: 1024-bin histograms in
+        // gsum[0, 1024) and gsum[1024, 2048), zeroed together (the digit search's last barrier
+        // publishes each digit before the next pass reads it)
+        gsum[tid] = 0u;
+        gsum[NT + tid] = 0u;
         __syncthreads();
-        // passes 1 and 2 (10-bit digits) over the merged list, in gsum as a 1024-bin histogram
 #pragma unroll 1
         for (int pass = 1; pass < 3; ++pass) {
             const int shift = pass == 1 ? 10 : 0;
-            for (int i = tid; i < 1024; i += NT)
-                gsum[i] = 0u;
-            __syncthreads();
+            uint32_t *hp = gsum + (pass - 1) * NT;
             for (int i = tid; i < n_all; i += NT) {
                 const uint32_t k = hbuf0[i];
                 if ((k & pmask) == prefix)
-                    atomicAdd(&gsum[(k >> shift) & 1023u], 1u);
+                    atomicAdd(&hp[(k >> shift) & 1023u], 1u);
             }
             __syncthreads();
-            find_digit(gsum, 1024, krem);
+            find_digit(hp, 1024, krem);
             prefix |= sh_digit << shift;
             pmask |= 1023u << shift;
             krem -= sh_above;
-            __syncthreads();
         }
         // keys above and equal to the threshold in the lists of the CTAs before this one
         int cg = 0, ce = 0;
@@ -668,7 +750,7 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
             ce += __shfl_xor_sync(0xffffffffu, ce, o);
         }
         int2 tot2;
-        warp_totals_exclusive_scan(cg, ce, scratch, &tot2);
+        warp_pairs_exclusive_scan(cg, ce, scratch2, &tot2);
         gt_before += tot2.x;
         eq_before += tot2.y;
     } else {
@@ -707,7 +789,7 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
         n_eq += __popc(__ballot_sync(0xffffffffu, in && k == thr));
     }
     int2 tot;
-    const int2 before = warp_totals_exclusive_scan(n_gt, n_eq, scratch, &tot);
+    const int2 before = warp_pairs_exclusive_scan(n_gt, n_eq, scratch, &tot);
     if (!listed) {
         if (tid == 0) {
             sh_counts[0] = tot.x;

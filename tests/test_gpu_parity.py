@@ -96,6 +96,8 @@ def run_first_slow_step(wl, out_fp32=True):
     dict(name="llama8b_ctx32k_b4", ctx=1500, n_q_heads=16, n_kv_heads=8),  # group 2
     dict(name="llama8b_ctx32k_b4", ctx=1500, n_q_heads=64, n_kv_heads=8),  # group 8
     dict(name="ragged_paged_b32", batch=5, ctx=3000, ctx_lo=200),    # paged, ragged
+    # 2 units over every SM: each unit's split-KV merge takes ~76 contributors in 3 chunks
+    dict(name="llama8b_ctx32k_b4", ctx=20000, batch=1, n_q_heads=8, n_kv_heads=2),
 ])
 def test_dense_select_compact_vs_oracle(case):
     case = dict(case)
@@ -143,13 +145,16 @@ def test_dense_bf16_output():
     np.testing.assert_allclose(o16, o32, rtol=2 ** -8, atol=1e-6)
 
 
-def test_split_kv_merge_independent_of_arrival_order():
-    """One sequence of 20,000 positions: each unit's tiles are cut over ~19 CTAs, and the
-    contributor that takes the unit's last ticket (and merges) differs from launch to launch.
-    The merge runs over the contributors in CTA order, so repeated launches on the same
-    inputs give the same outputs and evidence bit for bit."""
+@pytest.mark.parametrize("heads", [(32, 8), (8, 2)], ids=["19_contributors", "76_contributors"])
+def test_split_kv_merge_independent_of_arrival_order(heads):
+    """One sequence of 20,000 positions: each unit's tiles are cut over ~19 CTAs (8 units) or
+    ~76 CTAs (2 units, three chunks of the merge), and the contributor that takes the unit's
+    last ticket (and merges) differs from launch to launch. The merge runs over the
+    contributors in CTA order, so repeated launches on the same inputs give the same outputs
+    and evidence bit for bit."""
     import sparse_long_context_sfi_gb300 as sfi
-    wl = small("llama8b_ctx32k_b4", ctx=20000, batch=1, steps=2)
+    wl = small("llama8b_ctx32k_b4", ctx=20000, batch=1, steps=2, n_q_heads=heads[0],
+               n_kv_heads=heads[1])
     cfg = wl.cfg
     st = sdev.make_state(wl, on_device=True)
     ins = sdev.DeviceInputs(wl, 1, st.k.device, on_device=True)
