@@ -1526,6 +1526,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
 }
 
+constexpr int kEvPer = 4;   // positions per thread of the evidence kernel
+
 // Evidence f_j = (1/G) sum_h exp2(z_hj - M_h) / L_h from the dense step's base-2 logits
 // and merged statistics; one pass over [units][positions].
 template <int G>
@@ -1553,20 +1555,42 @@ __global__ void __launch_bounds__(256) evidence_kernel(const float *__restrict__
     const float rg = 1.f / static_cast<float>(G);
     const float *zu = zbuf + static_cast<size_t>(u) * capacity * G;
     float *fu = f + static_cast<size_t>(u) * capacity;
-    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < L; j += gridDim.x * blockDim.x) {
-        float z[G];
-        if constexpr (G == 4) {
-            const float4 v = __ldcs(reinterpret_cast<const float4 *>(zu) + j);
-            z[0] = v.x; z[1] = v.y; z[2] = v.z; z[3] = v.w;
-        } else {
+    // The grid covers the longest sequence with kEvPer positions per thread: all of a
+    // thread's loads are issued before the first is used (one round trip, not kEvPer).
+    const int stride = gridDim.x * blockDim.x;
+    const int j0 = blockIdx.x * blockDim.x + threadIdx.x;
+    float z[kEvPer][G];
+#pragma unroll
+    for (int r = 0; r < kEvPer; ++r) {
+        const int j = j0 + r * stride;
+        if (j < L) {
+            if constexpr (G == 4) {
+                const float4 v = __ldcs(reinterpret_cast<const float4 *>(zu) + j);
+                z[r][0] = v.x; z[r][1] = v.y; z[r][2] = v.z; z[r][3] = v.w;
+            } else {
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+                    z[r][h] = __ldcs(zu + static_cast<size_t>(j) * G + h);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kEvPer; ++r) {
+        const int j = j0 + r * stride;
+        if (j < L) {
+            float acc = 0.f;
 #pragma unroll
             for (int h = 0; h < G; ++h)
-                z[h] = __ldcs(zu + static_cast<size_t>(j) * G + h);
+                acc += exp2f(z[r][h] - M[h]) * inv[h];
+            fu[j] = acc * rg;
         }
+    }
+    // (only a length above the launch's bound reaches here; the dense step flags it)
+    for (int j = j0 + kEvPer * stride; j < L; j += stride) {
         float acc = 0.f;
 #pragma unroll
         for (int h = 0; h < G; ++h)
-            acc += exp2f(z[h] - M[h]) * inv[h];
+            acc += exp2f(__ldcs(zu + static_cast<size_t>(j) * G + h) - M[h]) * inv[h];
         fu[j] = acc * rg;
     }
 }
@@ -1683,7 +1707,7 @@ cudaError_t launch_evidence(const float *zbuf, const float2 *stats, float *f, co
                             int capacity, int max_len, cudaStream_t stream)
 {
     const int units = n_layers * batch * n_kv_heads;
-    dim3 grid((max_len + 256 * 4 - 1) / (256 * 4), units);
+    dim3 grid((max_len + 256 * kEvPer - 1) / (256 * kEvPer), units);
     if (grid.x == 0)
         grid.x = 1;
     switch (group) {
