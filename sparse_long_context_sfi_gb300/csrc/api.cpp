@@ -181,10 +181,13 @@ uint64_t cache_rows(const sfi_kv_cache *kv)
 // ws_kv/unit0: the descriptor whose workspace layout `ws` follows and the first of its units
 // that kv covers (a one-layer view of a larger cache keeps the per-unit regions of the whole
 // cache, so the tickets and counters of every other launch stay where they are).
+// n_seq_active > 0: exactly that many sequences have active[b] set (the evidence pass then
+// launches only their units).
 sfi_status dense_impl(const sfi_kv_cache *kv, const void *q, void *out, int32_t out_fp32,
                       float *scores_f, const uint8_t *active, void *ws, size_t ws_bytes,
                       void *stream, cudaEvent_t e0, cudaEvent_t e1,
-                      const sfi_kv_cache *ws_kv = nullptr, long long unit0 = 0)
+                      const sfi_kv_cache *ws_kv = nullptr, long long unit0 = 0,
+                      int n_seq_active = 0)
 {
     sfi_status st = check_kv(kv);
     if (st != SFI_OK)
@@ -230,7 +233,8 @@ sfi_status dense_impl(const sfi_kv_cache *kv, const void *q, void *out, int32_t 
     if (scores_f) {
         e = launch_evidence(p.zbuf, p.stats, scores_f, kv->seq_len, active, kv->n_layers,
                             kv->batch, kv->n_kv_heads, g, kv->capacity, kv->max_len,
-                            as_stream(stream));
+                            as_stream(stream),
+                            (active && n_seq_active > 0 && n_seq_active < kv->batch) ? n_seq_active : 0);
         if (e != cudaSuccess)
             return SFI_ERR_CUDA;
     }
@@ -400,8 +404,12 @@ sfi_status sfi_dense_decode_attn(const sfi_kv_cache *kv, const void *q, void *ou
                       nullptr);
 }
 
-sfi_status sfi_select(const sfi_kv_cache *kv, const float *scores_f, const sfi_budget *budget,
-                      const sfi_sparse_mem *mem, const uint8_t *active, void *stream)
+// sfi_select, with n_seq_active > 0 when the caller knows that exactly that many sequences
+// have active[b] set (sfi_decode_run's slow subsets): the launch then covers only their units,
+// which lets a small subset take the clustered Selector.
+static sfi_status select_impl(const sfi_kv_cache *kv, const float *scores_f,
+                              const sfi_budget *budget, const sfi_sparse_mem *mem,
+                              const uint8_t *active, int n_seq_active, void *stream)
 {
     sfi_status st = check_kv(kv);
     if (st != SFI_OK)
@@ -415,7 +423,8 @@ sfi_status sfi_select(const sfi_kv_cache *kv, const float *scores_f, const sfi_b
     p.capacity = kv->capacity;
     p.batch = kv->batch;
     p.n_kv_heads = kv->n_kv_heads;
-    p.n_units = kv->n_layers * kv->batch * kv->n_kv_heads;
+    p.n_seq_active = (active && n_seq_active > 0 && n_seq_active < kv->batch) ? n_seq_active : 0;
+    p.n_units = kv->n_layers * (p.n_seq_active > 0 ? p.n_seq_active : kv->batch) * kv->n_kv_heads;
     p.seq_len = kv->seq_len;
     p.active = active;
     p.n_sink = budget->n_sink;
@@ -441,6 +450,12 @@ sfi_status sfi_select(const sfi_kv_cache *kv, const float *scores_f, const sfi_b
             p.cluster = C;  // at most about two waves of CTAs
     }
     return launch_status(launch_select(p, as_stream(stream)));
+}
+
+sfi_status sfi_select(const sfi_kv_cache *kv, const float *scores_f, const sfi_budget *budget,
+                      const sfi_sparse_mem *mem, const uint8_t *active, void *stream)
+{
+    return select_impl(kv, scores_f, budget, mem, active, 0, stream);
 }
 
 sfi_status sfi_key_norms(const sfi_kv_cache *kv, float *norms, const uint8_t *active,
@@ -497,8 +512,11 @@ sfi_status sfi_refine_scores(const sfi_kv_cache *kv, const float *scores_f,
         launch_refine(p, kv->n_layers * kv->batch, max_cand > 0 ? max_cand : 1, as_stream(stream)));
 }
 
-sfi_status sfi_compact(const sfi_kv_cache *kv, const sfi_budget *budget,
-                       const sfi_sparse_mem *mem, const uint8_t *active, void *stream)
+// sfi_compact, with n_seq_active > 0 when exactly that many sequences have active[b] set (as
+// for select_impl).
+static sfi_status compact_impl(const sfi_kv_cache *kv, const sfi_budget *budget,
+                               const sfi_sparse_mem *mem, const uint8_t *active,
+                               int n_seq_active, void *stream)
 {
     sfi_status st = check_kv(kv);
     if (st != SFI_OK)
@@ -512,7 +530,14 @@ sfi_status sfi_compact(const sfi_kv_cache *kv, const sfi_budget *budget,
         kv->k, kv->v, mem->kc, mem->vc, mem->sel_idx, mem->sel_cnt, mem->rows, kv->seq_len, active,
         kv->page_table, kv->n_layers, kv->batch, kv->n_kv_heads, kv->capacity, kv->page_size,
         kv->n_pages, kv->max_pages_per_seq, budget->n_sink, budget->n_select, kv->err,
-        as_stream(stream)));
+        as_stream(stream),
+        (active && n_seq_active > 0 && n_seq_active < kv->batch) ? n_seq_active : 0));
+}
+
+sfi_status sfi_compact(const sfi_kv_cache *kv, const sfi_budget *budget,
+                       const sfi_sparse_mem *mem, const uint8_t *active, void *stream)
+{
+    return compact_impl(kv, budget, mem, active, 0, stream);
 }
 
 sfi_status sfi_sparse_decode_attn(const sfi_kv_cache *kv, const sfi_sparse_mem *mem,
@@ -601,7 +626,7 @@ sfi_status sfi_schedule(int32_t steps, const uint8_t *mask, int32_t t_max, uint8
 // of the step. Groups of several layers keep each dense launch long enough to fill the GPU.
 static sfi_status slow_step_layers(const sfi_kv_cache *k, const sfi_budget *budget,
                                    const sfi_sparse_mem *mem, const sfi_decode_plan *plan,
-                                   const void *q, void *out, const uint8_t *m_slow, void *ws,
+                                   const void *q, void *out, const uint8_t *m_slow, int n_slow_seq, void *ws,
                                    size_t ws_bytes, void *stream, cudaEvent_t e0, cudaEvent_t e1)
 {
     cudaStream_t main_s = as_stream(stream), side = as_stream(plan->side_stream);
@@ -625,7 +650,7 @@ static sfi_status slow_step_layers(const sfi_kv_cache *k, const sfi_budget *budg
         void *ol = static_cast<char *>(out) + l * q_layer * (plan->out_fp32 ? 4 : 2);
         float *fl = plan->scores_f + l * units * k->capacity;
         st = dense_impl(&kl, ql, ol, plan->out_fp32, fl, m_slow, ws, ws_bytes, stream, nullptr,
-                        nullptr, k, static_cast<long long>(l) * units);
+                        nullptr, k, static_cast<long long>(l) * units, n_slow_seq);
         if (st != SFI_OK)
             break;
         if (cudaEventRecord(fork, main_s) != cudaSuccess ||
@@ -634,8 +659,8 @@ static sfi_status slow_step_layers(const sfi_kv_cache *k, const sfi_budget *budg
             break;
         }
         forked = true;
-        if ((st = sfi_select(&kl, fl, budget, &ml, m_slow, plan->side_stream)) == SFI_OK)
-            st = sfi_compact(&kl, budget, &ml, m_slow, plan->side_stream);
+        if ((st = select_impl(&kl, fl, budget, &ml, m_slow, n_slow_seq, plan->side_stream)) == SFI_OK)
+            st = compact_impl(&kl, budget, &ml, m_slow, n_slow_seq, plan->side_stream);
     }
     // joined on every path once forked, so a stream capture around the call stays joinable
     if (forked && (cudaEventRecord(join, side) != cudaSuccess ||
@@ -700,14 +725,15 @@ sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
             continue;
         }
         if (n_slow > 0 && pipe) {
-            if ((st = slow_step_layers(&k, budget, mem, plan, q, out, m_slow, ws, ws_bytes,
+            if ((st = slow_step_layers(&k, budget, mem, plan, q, out, m_slow, mixed ? n_slow : 0, ws, ws_bytes,
                                        stream, e0, e1)) != SFI_OK)
                 return st;
         } else if (n_slow > 0) {
             if ((st = dense_impl(&k, q, out, plan->out_fp32, plan->scores_f, m_slow, ws, ws_bytes,
-                                 stream, e0, e1)) != SFI_OK ||
-                (st = sfi_select(&k, plan->scores_f, budget, mem, m_slow, stream)) != SFI_OK ||
-                (st = sfi_compact(&k, budget, mem, m_slow, stream)) != SFI_OK)
+                                 stream, e0, e1, nullptr, 0, mixed ? n_slow : 0)) != SFI_OK ||
+                (st = select_impl(&k, plan->scores_f, budget, mem, m_slow, mixed ? n_slow : 0,
+                                  stream)) != SFI_OK ||
+                (st = compact_impl(&k, budget, mem, m_slow, mixed ? n_slow : 0, stream)) != SFI_OK)
                 return st;
         }
         if (n_slow < B) {

@@ -1536,11 +1536,15 @@ __global__ void __launch_bounds__(256) evidence_kernel(const float *__restrict__
                                                        float *__restrict__ f,
                                                        const int32_t *__restrict__ seq_len,
                                                        const uint8_t *__restrict__ active,
-                                                       int batch, int n_kv_heads, int capacity)
+                                                       int batch, int n_kv_heads, int capacity,
+                                                       int n_seq_active)
 {
     pdl_trigger();
     pdl_wait();
-    const int u = blockIdx.y;
+    // (with n_seq_active > 0 the grid covers only the active sequences' units)
+    const int u = launched_unit(static_cast<int>(blockIdx.y), n_seq_active, active, batch, n_kv_heads);
+    if (u < 0)
+        return;
     const int b = (u / n_kv_heads) % batch;
     if (active && !active[b])
         return;
@@ -1704,17 +1708,17 @@ cudaError_t launch_attention(bool dense, int group, const CUtensorMap &tm_k, con
 
 cudaError_t launch_evidence(const float *zbuf, const float2 *stats, float *f, const int32_t *seq_len,
                             const uint8_t *active, int n_layers, int batch, int n_kv_heads, int group,
-                            int capacity, int max_len, cudaStream_t stream)
+                            int capacity, int max_len, cudaStream_t stream, int n_seq_active)
 {
-    const int units = n_layers * batch * n_kv_heads;
+    const int units = n_layers * (n_seq_active > 0 ? n_seq_active : batch) * n_kv_heads;
     dim3 grid((max_len + 256 * kEvPer - 1) / (256 * kEvPer), units);
     if (grid.x == 0)
         grid.x = 1;
     switch (group) {
-    case 1: return launch_pdl(evidence_kernel<1>, grid, dim3(256), 0, stream, zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity);
-    case 2: return launch_pdl(evidence_kernel<2>, grid, dim3(256), 0, stream, zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity);
-    case 4: return launch_pdl(evidence_kernel<4>, grid, dim3(256), 0, stream, zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity);
-    case 8: return launch_pdl(evidence_kernel<8>, grid, dim3(256), 0, stream, zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity);
+    case 1: return launch_pdl(evidence_kernel<1>, grid, dim3(256), 0, stream, zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity, n_seq_active);
+    case 2: return launch_pdl(evidence_kernel<2>, grid, dim3(256), 0, stream, zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity, n_seq_active);
+    case 4: return launch_pdl(evidence_kernel<4>, grid, dim3(256), 0, stream, zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity, n_seq_active);
+    case 8: return launch_pdl(evidence_kernel<8>, grid, dim3(256), 0, stream, zbuf, stats, f, seq_len, active, batch, n_kv_heads, capacity, n_seq_active);
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

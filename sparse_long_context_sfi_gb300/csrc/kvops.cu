@@ -82,9 +82,13 @@ __global__ void __launch_bounds__(256) compact_kernel(
     int32_t *__restrict__ rows_out, const int32_t *__restrict__ seq_len,
     const uint8_t *__restrict__ active, const int32_t *__restrict__ page_table, int batch,
     int n_kv_heads, int capacity, int page_size, int n_pages, int max_pages, int n_sink,
-    int n_select, uint32_t *err)
+    int n_select, uint32_t *err, int n_seq_active)
 {
-    const int u = blockIdx.x;
+    // (with n_seq_active > 0 the grid covers only the active sequences' units; `active` is an
+    // input complete at launch, so it is read before the wait)
+    const int u = launched_unit(static_cast<int>(blockIdx.x), n_seq_active, active, batch, n_kv_heads);
+    if (u < 0)
+        return;
     const int kvh = u % n_kv_heads;
     const int b = (u / n_kv_heads) % batch;
     const int layer = u / (n_kv_heads * batch);
@@ -169,16 +173,17 @@ cudaError_t launch_compact(const void *k, const void *v, void *kc, void *vc, con
                            const int32_t *sel_cnt, int32_t *rows, const int32_t *seq_len,
                            const uint8_t *active, const int32_t *page_table, int n_layers, int batch,
                            int n_kv_heads, int capacity, int page_size, int n_pages, int max_pages,
-                           int n_sink, int n_select, uint32_t *err, cudaStream_t stream)
+                           int n_sink, int n_select, uint32_t *err, cudaStream_t stream,
+                           int n_seq_active)
 {
-    const int units = n_layers * batch * n_kv_heads;
+    const int units = n_layers * (n_seq_active > 0 ? n_seq_active : batch) * n_kv_heads;
     const int comp_cap = n_sink + n_select;
     dim3 grid(units, (comp_cap + kCompactBlockRows - 1) / kCompactBlockRows);
     const cudaError_t e = launch_pdl(
         compact_kernel, grid, dim3(256), 0, stream, static_cast<const uint4 *>(k),
         static_cast<const uint4 *>(v), static_cast<uint4 *>(kc), static_cast<uint4 *>(vc), sel_idx,
         sel_cnt, rows, seq_len, active, page_table, batch, n_kv_heads, capacity, page_size, n_pages,
-        max_pages, n_sink, n_select, err);
+        max_pages, n_sink, n_select, err, n_seq_active);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

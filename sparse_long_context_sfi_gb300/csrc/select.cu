@@ -255,7 +255,10 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
     // fast step reads the packed memory that follows from it before its own wait.
     const int tid = threadIdx.x, lane = tid & 31;
     pdl_wait();
-    const int u = blockIdx.x;
+    const int u = launched_unit(static_cast<int>(blockIdx.x), p.n_seq_active, p.active, p.batch,
+                                p.n_kv_heads);
+    if (u < 0)
+        return;
     const int b = (u / p.n_kv_heads) % p.batch;
     if (p.active && !p.active[b])
         return;
@@ -540,7 +543,10 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
     pdl_wait();
     const int C = p.cluster;
     const int rank = static_cast<int>(blockIdx.x) % C;
-    const int u = static_cast<int>(blockIdx.x) / C;
+    const int u = launched_unit(static_cast<int>(blockIdx.x) / C, p.n_seq_active, p.active,
+                                p.batch, p.n_kv_heads);
+    if (u < 0)
+        return;   // (every CTA of the cluster alike: no cluster barrier is reached)
     const int b = (u / p.n_kv_heads) % p.batch;
     if (p.active && !p.active[b])
         return;

@@ -101,6 +101,61 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// The j-th sequence b (0-based, in order) with active[b] != 0, found by one warp (call
+// from every lane of a warp; every lane gets the result); B <= 256. -1 when fewer are active.
+__device__ __forceinline__ int nth_active_seq(const uint8_t *active, int B, int j)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t bits = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int b = lane * 8 + k;
+        if (b < B && active[b])
+            bits |= 1u << k;
+    }
+    const int mine = __popc(bits);
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += y;
+    }
+    const int before = incl - mine;
+    const unsigned here = __ballot_sync(0xffffffffu, before <= j && j < incl);
+    if (here == 0u)
+        return -1;
+    const int src = __ffs(here) - 1;
+    int res = -1;
+    if (lane == src) {
+        int cnt = before;
+        for (int k = 0; k < 8; ++k) {
+            if ((bits >> k) & 1u) {
+                if (cnt == j) {
+                    res = lane * 8 + k;
+                    break;
+                }
+                ++cnt;
+            }
+        }
+    }
+    return __shfl_sync(0xffffffffu, res, src);
+}
+
+// Unit of launched index ci: ci itself, or with n_seq_active > 0 the ci-th unit among the
+// active sequences' units ((layer, j-th active sequence, kv head) in order); -1 when none.
+__device__ __forceinline__ int launched_unit(int ci, int n_seq_active, const uint8_t *active,
+                                             int batch, int n_kv_heads)
+{
+    if (n_seq_active <= 0)
+        return ci;
+    const int per_layer = n_seq_active * n_kv_heads;
+    const int layer = ci / per_layer, r = ci - layer * per_layer;
+    const int j = r / n_kv_heads, kvh = r - j * n_kv_heads;
+    const int b = nth_active_seq(active, batch, j);
+    return b < 0 ? -1 : (layer * batch + b) * n_kv_heads + kvh;
+}
+
 // ----------------------------------------------------- programmatic dependent launch
 
 // Publish global writes at GPU scope, then let the next kernel be scheduled. For kernels

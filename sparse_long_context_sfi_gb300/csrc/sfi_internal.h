@@ -56,7 +56,8 @@ struct AttnParams {
 
 struct SelectParams {
     const float *f;             // [units][capacity]
-    int capacity, batch, n_kv_heads, n_units;
+    int capacity, batch, n_kv_heads;
+    int n_units;                // units launched (all, or the active sequences' with n_seq_active)
     const int32_t *seq_len;
     const uint8_t *active;
     int n_sink, n_window, n_select, prior_tau;
@@ -66,6 +67,9 @@ struct SelectParams {
     int staged;                 // candidates' evidence copied to shared memory (see kStageCap)
     int cluster;                // > 1: CTAs per unit in one cluster (select_cluster_size)
     uint32_t *err;              // device error word
+    // > 0: the grid covers only the units of the first n_seq_active sequences with active[b]
+    // set, per layer in order (the caller knows how many are active); 0: every unit
+    int n_seq_active;
 };
 // The Selector stages a unit's evidence in shared memory when it has at most this many
 // candidates (plus alignment slack); larger units stream it from global memory.
@@ -105,7 +109,7 @@ int sparse_cluster_size(int group, int units, int max_cluster);
 cudaError_t launch_evidence(const float *zbuf, const float2 *stats, float *f,
                             const int32_t *seq_len, const uint8_t *active, int n_layers,
                             int batch, int n_kv_heads, int group, int capacity, int max_len,
-                            cudaStream_t stream);
+                            cudaStream_t stream, int n_seq_active = 0);
 cudaError_t launch_select(const SelectParams &p, cudaStream_t stream);
 // Clustered Selector: the largest cluster size (4 or 2, at most max_cluster) that can be
 // launched on this device (1 when none can); and the most candidates one of its CTAs can
@@ -121,7 +125,8 @@ cudaError_t launch_compact(const void *k, const void *v, void *kc, void *vc,
                            const int32_t *seq_len, const uint8_t *active,
                            const int32_t *page_table, int n_layers, int batch, int n_kv_heads,
                            int capacity, int page_size, int n_pages, int max_pages, int n_sink,
-                           int n_select, uint32_t *err, cudaStream_t stream);
+                           int n_select, uint32_t *err, cudaStream_t stream,
+                           int n_seq_active = 0);
 
 size_t attention_smem_bytes();
 // Fast-step attention with its split-KV scratch in a library-owned device array instead of
