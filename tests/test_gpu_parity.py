@@ -356,6 +356,53 @@ def test_end_to_end_ragged_paged_per_sequence_schedule():
     compare_run(wl, 40, check_steps=range(0, 40, 3))
 
 
+@pytest.mark.parametrize("layers", [1, 2])
+def test_slow_subset_launch_bit_exact(layers):
+    """A decode run whose second step is slow for two of six sequences: the Selector, the
+    packing and the evidence pass launch only those sequences' units (each CTA finds its unit
+    through the activity mask). Their selections equal the oracle's on the GPU's own evidence,
+    bit for bit, and their packed rows are the selected cache rows; the other units keep the
+    selections of the first step."""
+    wl = small("ragged_paged_b32", batch=6, ctx=2400, ctx_lo=600, steps=2, n_layers=layers)
+    cfg = wl.cfg
+    st = sdev.make_state(wl, on_device=True)
+    ins = sdev.DeviceInputs(wl, 2, st.k.device, on_device=True)
+    slow = np.zeros((2, cfg.batch), np.uint8)
+    slow[0] = 1
+    slow[1, [1, 4]] = 1
+    out = torch.zeros((2, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
+                      dtype=torch.float32, device=st.k.device)
+    st.run(st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, t0=0, t1=1))
+    torch.cuda.synchronize()
+    sel0, cnt0 = st.sel_idx.cpu().numpy().copy(), st.sel_cnt.cpu().numpy().copy()
+    st.run(st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, t0=1, t1=2))
+    torch.cuda.synchronize()
+    assert int(st.err[0]) == 0
+    S, W, K, D = cfg.n_sink, cfg.n_window, cfg.n_select, cfg.head_dim
+    f = st.scores.cpu().numpy()
+    sel, cnt, rows = st.sel_idx.cpu().numpy(), st.sel_cnt.cpu().numpy(), st.rows.cpu().numpy()
+    kc = st.kc.view(torch.int16).cpu().numpy().view(np.uint16).reshape(st.n_units, S + K, D)
+    vc = st.vc.view(torch.int16).cpu().numpy().view(np.uint16).reshape(st.n_units, S + K, D)
+    n_slow_units = 0
+    for u in range(st.n_units):
+        layer, b, kvh = unit_coords(cfg, u)
+        if not slow[1, b]:
+            assert cnt[u] == cnt0[u], f"unit {u}: a fast unit's selection changed"
+            np.testing.assert_array_equal(sel[u, :cnt[u]], sel0[u, :cnt0[u]])
+            continue
+        n_slow_units += 1
+        L = int(wl.len0[b]) + 2
+        want = oracle.select(L, S, W, K, cfg.prior_tau, cfg.lam, f[u, :L])
+        assert cnt[u] == len(want), f"unit {u}"
+        np.testing.assert_array_equal(sel[u, :cnt[u]], want, err_msg=f"unit {u}")
+        n_s = min(S, L)
+        assert rows[u] == n_s + cnt[u]
+        pos = np.concatenate([np.arange(n_s), want]).astype(np.int64)
+        np.testing.assert_array_equal(kc[u, :rows[u]], wl.rows("k", layer, b, kvh, pos))
+        np.testing.assert_array_equal(vc[u, :rows[u]], wl.rows("v", layer, b, kvh, pos))
+    assert n_slow_units == 2 * cfg.n_kv_heads * cfg.n_layers
+
+
 def test_end_to_end_32k_batch4_sampled():
     """The 32K-context, batch-4 workload at full size through the native driver: sampled
     units over the first 20 decode steps -- slow steps 0, 3 and 15 (two selection refreshes)
