@@ -266,7 +266,7 @@ def cpu_baseline(wl):
 
 
 def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=None,
-            dense_only_runs=0, pipeline_runs=0, cold_fast=False):
+            dense_only_runs=0, pipeline_runs=0, cold_fast=False, concurrent_runs=0):
     """Time whole decode runs of one workload (CUDA-graph replays), the per-kernel durations
     (event-instrumented replays), and optionally the dense-only / fast-only modes and the
     end-to-end run with host buffers."""
@@ -351,7 +351,7 @@ def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=N
         events[2 * t1 + 1] = torch.cuda.Event(enable_timing=True)
         groups.append((t, t1))
         t = t1 + 1
-    g_ev = capture(run_of(slow, events=events))
+    g_ev = capture(run_of(slow, events=events, concurrent=False))
     reps = 3
     d_dense, d_sparse = [], []                     # (steps, seconds)
     with torch.cuda.stream(stream):
@@ -479,6 +479,16 @@ def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=N
             res["layer_pipeline"][f"group_{grp}"] = {
                 "tokens_per_s": world * tokens_per_run * pipeline_runs / (ms_p / 1000.0),
                 "ms_per_run": ms_p / pipeline_runs, "layers_per_dense_launch": grp}
+    mixed_steps = int(sum(1 for r in slow if r.any() and not r.all()))
+    if concurrent_runs and mixed_steps:
+        # the timed runs issue the fast step of a mixed step's fast sequences on a side stream
+        # beside the slow sequences' chain; the same runs on one stream, for comparison
+        g_seq = capture(run_of(slow, concurrent=False))
+        ms_s = time_graph(g_seq, concurrent_runs, 1)
+        del g_seq
+        res["one_stream"] = {
+            "tokens_per_s": world * tokens_per_run * concurrent_runs / (ms_s / 1000.0),
+            "ms_per_run": ms_s / concurrent_runs, "mixed_steps": mixed_steps}
     if cold_fast:
         res["fast_cold"] = fast_step_cold(wl, st, ins, stream, dev, world)
     if extras:
@@ -676,7 +686,8 @@ def main():
             multi = w2.cfg.n_layers > 1
             r2 = measure(w2, args, world, dev, stream, 2 if big else max(3, args.steps // 4),
                          1 if big else 2, extras=False, dense_only_runs=1 if big else 2,
-                         pipeline_runs=(1 if big else 2) if multi else 0, cold_fast=not big)
+                         pipeline_runs=(1 if big else 2) if multi else 0, cold_fast=not big,
+                         concurrent_runs=1 if big else max(3, args.steps // 4))
             others[name] = {"tokens_per_s": r2["value"], "ms_per_run": r2["ms_per_run"],
                             "config": workload_config(w2, r2["slow_steps"]),
                             "kernels": r2["kernels"],
@@ -688,6 +699,8 @@ def main():
                 others[name]["layer_pipeline"] = r2["layer_pipeline"]
             if "fast_cold" in r2:
                 others[name]["fast_step_cold"] = r2["fast_cold"]
+            if "one_stream" in r2:
+                others[name]["mixed_steps_on_one_stream"] = r2["one_stream"]
             torch.cuda.empty_cache()
 
     peak, peak_kind = measured_peaks()

@@ -65,7 +65,8 @@ class SfiDecodePlan(C.Structure):
                 ("out_fp32", C.c_int32), ("out_per_step", C.c_int32), ("scores_f", C.c_void_p),
                 ("masks", C.c_void_p), ("len_start", C.c_int32), ("dense_only", C.c_int32),
                 ("events", C.c_void_p), ("side_stream", C.c_void_p), ("fork_event", C.c_void_p),
-                ("join_event", C.c_void_p), ("pipeline_group", C.c_int32)]
+                ("join_event", C.c_void_p), ("pipeline_group", C.c_int32),
+                ("concurrent_fast", C.c_int32)]
 
 
 class SfiError(RuntimeError):

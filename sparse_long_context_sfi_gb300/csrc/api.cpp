@@ -685,8 +685,9 @@ sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
         return SFI_ERR_INVALID_ARG;
     if (plan->len_start + plan->n_steps > kv->capacity)
         return SFI_ERR_CAPACITY;
-    const bool pipe = plan->side_stream != nullptr && !plan->dense_only;
-    if (pipe && (!plan->fork_event || !plan->join_event))
+    const bool conc_req = plan->concurrent_fast != 0 && !plan->dense_only;
+    const bool pipe = plan->side_stream != nullptr && !plan->dense_only && !conc_req;
+    if ((pipe || conc_req) && (!plan->side_stream || !plan->fork_event || !plan->join_event))
         return SFI_ERR_INVALID_ARG;
     const int B = kv->batch, g = kv->n_q_heads / kv->n_kv_heads;
     const size_t q_step = static_cast<size_t>(kv->n_layers) * B * kv->n_q_heads * kHeadDim;
@@ -721,6 +722,38 @@ sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
         if (plan->dense_only) {
             if ((st = dense_impl(&k, q, out, plan->out_fp32, nullptr, nullptr, ws, ws_bytes, stream,
                                  e0, e1)) != SFI_OK)
+                return st;
+            continue;
+        }
+        if (mixed && conc_req) {
+            // The slow subset's chain and the other sequences' fused fast step touch disjoint
+            // sequences, cache rows, packed memory and workspace regions: the fast step runs
+            // on the side stream beside the chain. Both attention grids are sized for the
+            // whole GPU and the hardware interleaves their CTAs (splitting the SMs between
+            // them by bytes was measured slower: the chain's Selector and packing then leave
+            // the slow side's share idle).
+            cudaStream_t ms = as_stream(stream), ss = as_stream(plan->side_stream);
+            cudaEvent_t fork = static_cast<cudaEvent_t>(plan->fork_event);
+            cudaEvent_t join = static_cast<cudaEvent_t>(plan->join_event);
+            if (cudaEventRecord(fork, ms) != cudaSuccess || cudaStreamWaitEvent(ss, fork, 0) != cudaSuccess)
+                return SFI_ERR_CUDA;
+            sfi_kv_cache kf = k;
+            kf.max_len = plan->len_start + t;  // the fused append's bound before appending
+            st = sparse_impl(&kf, mem, budget, q, out, plan->out_fp32, m_fast, ws, ws_bytes,
+                             plan->side_stream, nullptr, nullptr, k_new, v_new);
+            // joined on every path once forked, so a stream capture around the call stays joinable
+            if (cudaEventRecord(join, ss) != cudaSuccess && st == SFI_OK)
+                st = SFI_ERR_CUDA;
+            if (st == SFI_OK)
+                st = dense_impl(&k, q, out, plan->out_fp32, plan->scores_f, m_slow, ws, ws_bytes,
+                                stream, e0, e1, nullptr, 0, n_slow);
+            if (st == SFI_OK)
+                st = select_impl(&k, plan->scores_f, budget, mem, m_slow, n_slow, stream);
+            if (st == SFI_OK)
+                st = compact_impl(&k, budget, mem, m_slow, n_slow, stream);
+            if (cudaStreamWaitEvent(ms, join, 0) != cudaSuccess && st == SFI_OK)
+                st = SFI_ERR_CUDA;
+            if (st != SFI_OK)
                 return st;
             continue;
         }

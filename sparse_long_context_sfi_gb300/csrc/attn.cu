@@ -304,6 +304,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
     }
 
+    // Clustered fast step: the unit's query rows and (fused append) its new K/V rows are
+    // read only after the wait, as they may come from the preceding kernel; prefetching them
+    // into L2 now is harmless either way (L2 is where the preceding kernel's writes land)
+    // and takes a DRAM round trip off the path after the wait when they were written
+    // earlier. (Done for the tile-range step's first unit as well, it was measured slower:
+    // finding that unit before the wait costs the late CTAs more than the prefetch saves.)
+    if (clustered && warp == 3 && lane == 0) {
+        tma_prefetch_l2_2d(&tm_q, 0, cl_u * G);
+        tma_prefetch_l2_2d(&tm_q, 64, cl_u * G);
+        if (fused) {
+            bulk_prefetch_l2(static_cast<const char *>(p.k_new) + static_cast<size_t>(cl_u) * 256, 256u);
+            bulk_prefetch_l2(static_cast<const char *>(p.v_new) + static_cast<size_t>(cl_u) * 256, 256u);
+        }
+    }
+
     // Tile t of the slice in ring stage i % kStages (producer warp, clustered): its row mask
     // is written and published on meta_full (what the softmax waits for), and with `issue`
     // its boxes are requested on full (what the MMA waits for): the packed rows below

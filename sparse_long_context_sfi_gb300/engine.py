@@ -136,14 +136,18 @@ class SfiState:
         return self._side
 
     def make_plan(self, slow: np.ndarray, q, k_new, v_new, out, out_fp32=True, out_per_step=True,
-                  dense_only=False, events=None, t0=0, t1=None, pipeline=False, pipeline_group=0):
+                  dense_only=False, events=None, t0=0, t1=None, pipeline=False, pipeline_group=0,
+                  concurrent=None):
         """slow: uint8 [steps][B]; q/k_new/v_new/out: device tensors with a leading step axis.
         events: optional list of 2 * (t1 - t0) torch.cuda.Event(enable_timing=True) or None,
         recorded before (2 t) and after (2 t + 1) step t's attention kernel (None: not
         recorded). [t0, t1): the steps this plan covers (a run can be issued as several
         consecutive plans). pipeline: run slow steps group of layers by group, with the
         Selector and compaction of each group on a side stream beside the next group's
-        attention; pipeline_group: layers per group (0: about a quarter of the layers)."""
+        attention; pipeline_group: layers per group (0: about a quarter of the layers).
+        concurrent: on steps that mix slow and fast sequences, the fast sequences' fused fast
+        step runs on a side stream beside the slow sequences' chain (not with pipeline; the
+        results are the same bits); None: on when the plan has such a step."""
         t1 = slow.shape[0] if t1 is None else t1
         q, k_new, v_new = q[t0:t1], k_new[t0:t1], v_new[t0:t1]
         if out_per_step:
@@ -152,6 +156,8 @@ class SfiState:
         steps = slow.shape[0]
         mixed = np.array([(r.any() and not r.all()) for r in slow])
         masks = None
+        if concurrent is None:
+            concurrent = bool(mixed.any()) and not pipeline and not dense_only
         if mixed.any():
             m = np.stack([slow, 1 - slow], axis=1).astype(np.uint8)
             masks = torch.from_numpy(m).to(self.device)
@@ -161,11 +167,12 @@ class SfiState:
             out_per_step=1 if out_per_step else 0, scores_f=self.scores.data_ptr(),
             masks=None if masks is None else masks.data_ptr(),
             len_start=int(self.len0.max()) + t0, dense_only=1 if dense_only else 0)
-        if pipeline:
+        if pipeline or concurrent:
             side, fork, join = self.side_stream()
             plan.side_stream, plan.fork_event, plan.join_event = (side.cuda_stream, fork.cuda_event,
                                                                   join.cuda_event)
             plan.pipeline_group = int(pipeline_group)
+            plan.concurrent_fast = 1 if concurrent and not pipeline else 0
         ev_arr = None
         if events is not None:
             assert len(events) == 2 * steps

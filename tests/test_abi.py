@@ -87,6 +87,7 @@ def test_decode_plan_layout_matches_header(lib):
     assert sfi.SfiDecodePlan.masks.offset == 64 and sfi.SfiDecodePlan.events.offset == 80
     assert sfi.SfiDecodePlan.side_stream.offset == 88 and sfi.SfiDecodePlan.join_event.offset == 104
     assert sfi.SfiDecodePlan.pipeline_group.offset == 112
+    assert sfi.SfiDecodePlan.concurrent_fast.offset == 116
     assert C.sizeof(sfi.SfiDecodePlan) == 120
 
 
@@ -107,6 +108,24 @@ def test_layer_pipeline_needs_both_events(lib):
     plan.fork_event, plan.join_event = None, dummy
     assert lib.sfi_decode_run(C.byref(kv), C.byref(bud), C.byref(mem), C.byref(plan), dummy,
                               1 << 30, None) == sfi.SFI_ERR_INVALID_ARG
+
+
+def test_concurrent_fast_needs_side_stream_and_events(lib):
+    """concurrent_fast without a side stream, or without its fork or join event, is refused
+    before any CUDA call."""
+    dummy = 1 << 20  # never dereferenced: the checks fail first
+    kv = sfi.SfiKvCache(n_layers=1, batch=2, n_q_heads=8, n_kv_heads=2, head_dim=128, capacity=64,
+                        max_len=8, k=dummy, v=dummy, seq_len=dummy, err=dummy)
+    bud = sfi.SfiBudget(n_sink=4, n_window=16, n_select=8, prior_tau=16, lambda_=0.1)
+    mem = sfi.SfiSparseMem(kc=dummy, vc=dummy, sel_idx=dummy, sel_cnt=dummy, rows=dummy)
+    slow = np.array([[1, 1], [1, 0]], np.uint8)
+    plan = sfi.SfiDecodePlan(n_steps=2, slow=slow.ctypes.data, q=dummy, k_new=dummy, v_new=dummy,
+                             out=dummy, out_fp32=1, out_per_step=1, scores_f=dummy, masks=dummy,
+                             len_start=8, concurrent_fast=1)
+    for side, fork, join in ((None, dummy, dummy), (dummy, None, dummy), (dummy, dummy, None)):
+        plan.side_stream, plan.fork_event, plan.join_event = side, fork, join
+        assert lib.sfi_decode_run(C.byref(kv), C.byref(bud), C.byref(mem), C.byref(plan), dummy,
+                                  1 << 30, None) == sfi.SFI_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("t_max", [0, 7, 64])

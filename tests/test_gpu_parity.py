@@ -316,23 +316,23 @@ def test_fused_fast_step_equals_append_then_sparse(case):
 
 # ------------------------------------------------------------------ whole decode, end to end
 
-def decode_on_gpu(wl, steps, on_device=True):
+def decode_on_gpu(wl, steps, on_device=True, concurrent=False):
     cfg = wl.cfg
     st = sdev.make_state(wl, on_device=on_device)
     ins = sdev.DeviceInputs(wl, steps, st.k.device, on_device=on_device)
     slow = sdev.schedule(wl, st, steps)
     out = torch.zeros((steps, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
                       dtype=torch.float32, device=st.k.device)
-    plan = st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out)
+    plan = st.make_plan(slow, ins.q, ins.k_new, ins.v_new, out, concurrent=concurrent)
     st.run(plan)
     torch.cuda.synchronize()
     assert int(st.err[0]) == 0
     return st, slow, out.cpu().numpy()
 
 
-def compare_run(wl, steps, units=None, check_steps=None):
+def compare_run(wl, steps, units=None, check_steps=None, concurrent=False):
     cfg = wl.cfg
-    st, slow, out = decode_on_gpu(wl, steps)
+    st, slow, out = decode_on_gpu(wl, steps, concurrent=concurrent)
     ref = odecode.run(wl, steps=steps, units=units)
     assert np.array_equal(ref["slow"].T, slow)
     units = list(range(st.n_units)) if units is None else units
@@ -354,6 +354,25 @@ def test_end_to_end_small_workload():
 def test_end_to_end_ragged_paged_per_sequence_schedule():
     wl = small("ragged_paged_b32", batch=6, ctx=2400, ctx_lo=600, steps=40, mask_param=6)
     compare_run(wl, 40, check_steps=range(0, 40, 3))
+
+
+@pytest.mark.parametrize("name", ["ragged_paged_b32", "llama8b_ctx32k_b4_tok"])
+def test_end_to_end_concurrent_fast_on_mixed_steps(name):
+    """concurrent_fast: on steps that mix slow and fast sequences, the fast sequences' fused
+    fast step runs on a side stream beside the slow sequences' chain. Every step and unit
+    against the oracle (mixed steps are most of them with these per-sequence schedules), and
+    bit for bit against the same run issued on one stream (the launches are the same, only
+    their order across streams differs)."""
+    if name == "ragged_paged_b32":
+        wl = small(name, batch=6, ctx=2400, ctx_lo=600, steps=24, mask_param=5)
+    else:
+        wl = small(name, batch=4, ctx=3000, ctx_lo=3000, steps=24)
+    st, ref = compare_run(wl, 24, concurrent=True)
+    slow = ref["slow"].T
+    assert any(r.any() and not r.all() for r in slow), "no mixed step"
+    _, _, out_c = decode_on_gpu(wl, 24, concurrent=True)
+    _, _, out_s = decode_on_gpu(wl, 24)
+    assert np.array_equal(out_c, out_s)
 
 
 @pytest.mark.parametrize("layers", [1, 2])
