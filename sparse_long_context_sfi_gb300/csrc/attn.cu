@@ -467,13 +467,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         g1 = c.g1;
         n_tiles = static_cast<int>(blockIdx.x) < c.P ? static_cast<int>(g1 - g0) : 0;
     };
-    // the first tile of the range: (layer, sequence, kv head, tile of the unit)
+    // the first tile of the range: (layer, sequence, kv head, tile of the unit); the
+    // sequence is the first with tiles whose range ends past r, found 32 sequences per step
+    // by a warp ballot (whole warp)
     auto first_tile = [&](int &layer, int &b, int &kvh, int &t) {
         layer = static_cast<int>(g0 / c.TL);
         const int r = static_cast<int>(g0 - static_cast<long long>(layer) * c.TL);
-        b = 0;
-        while (b + 1 < B && (c.nt[b] == 0 || c.pre[b] + Hkv * c.nt[b] <= r))
-            ++b;
+        b = B - 1;
+        for (int b0 = 0; b0 < B; b0 += 32) {
+            const int bb = b0 + lane;
+            const unsigned m = __ballot_sync(
+                0xffffffffu, bb < B && c.nt[bb] > 0 && c.pre[bb] + Hkv * c.nt[bb] > r);
+            if (m) {
+                b = b0 + __ffs(m) - 1;
+                break;
+            }
+        }
         kvh = (r - c.pre[b]) / c.nt[b];
         t = (r - c.pre[b]) - kvh * c.nt[b];
     };
@@ -681,7 +690,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // row count and selection count of the current (cur_meta) and the next (nxt_meta)
             // segment, the next loaded when the current one starts; lane j < n_wbox holds the
             // page of window box j of the current segment (paged cache, up to 32 boxes).
-            int cur_meta = 0, nxt_meta = 0, wpage = 0, app_page = 0;
+            int cur_meta = 0, nxt_meta = 0, wpage = 0, seg_jn = 0;
             const bool wpage_pf = !DENSE && p.page_size != 0 && p.n_wbox <= 32;
             const int my_q = lane >> 2, my_op = lane & 3;  // page / block and (K|V, half)
             // paged dense tiles: this lane's page id, loaded one tile ahead
@@ -705,8 +714,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (p.page_size == 0) {
                     row = static_cast<long long>(uu) * p.capacity + pos;
                 } else {
-                    const int page = wpage_pf ? app_page
-                                              : __ldg(p.page_table + bb * p.max_pages + (pos >> 4));
+                    // the page of window box seg_jn from the segment's prefetch (all lanes take
+                    // part in the shuffle), or, for a row outside the window (a sequence no
+                    // longer than its sinks), a direct lookup
+                    int page = wpage_pf ? __shfl_sync(0xffffffffu, wpage, max(0, min(seg_jn, 31))) : 0;
+                    if (!wpage_pf || seg_jn < 0 || seg_jn >= min(p.n_wbox, 32))
+                        page = __ldg(p.page_table + bb * p.max_pages + (pos >> 4));
                     good = page >= 0 && page < p.n_pages;
                     if (!good && lane == 0)
                         raise_error(p.err, 0x1u);  // SFI_DEVERR_PAGE_RANGE
@@ -724,6 +737,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             int app_tile = -1;       // tile of the current segment that holds the new row
             bool appended = false;
             bool ok = true;
+            bool pre_issued = false;  // the first tile's boxes were requested ahead (below)
             for (int i = 0; i < n_tiles; ++i, ++g) {
                 if (i > 0 && ++t == ntiles_of(b)) {
                     t = 0;
@@ -743,6 +757,48 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const int u = (layer * B + b) * Hkv + kvh;
                 const bool first = (i == 0) || (t == 0);
                 const bool last = (i == n_tiles - 1) || (t == ntiles_of(b) - 1);
+                // Sparse step: the range's first tile, when it holds packed rows only, is
+                // requested at once with the query, every box of it, before the unit's packed
+                // count and window start (two dependent global round trips) are known; its row
+                // mask is published once they are (rows past the packed count are masked, and
+                // their V rows zeroed, as in any tile).
+                if (!DENSE && i == 0 && (t + 1) * kTile <= 64 * p.n_cbox &&
+                    __shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+                    const int h2 = lane >> 4, j16 = lane & 15, kv0 = j16 >> 1, half0 = j16 & 1;
+                    const int y0 = u * p.comp_cap + t * kTile + 64 * h2;
+                    uint8_t *dst0 = smem + kv0 * 2 * kChunkBytes + half0 * kChunkBytes + 64 * h2 * 128;
+                    if (lane == 0) {
+                        TileMeta &mt = c.meta[0];
+                        mt.unit = u;
+                        mt.tile = t;
+                        mt.flags = kFlagFirst | (last ? kFlagLast : 0);
+                        mbar_arrive_expect_tx(&c.fullK[0], 2u * 2u * 64u * 128u + 2u * G * 128u +
+                                                               ((p.test_stall && blockIdx.x == 0) ? 16u : 0u));
+                    }
+                    __syncwarp();
+                    if (lane < 2)
+                        tma_load_2d(smem + kQOff + lane * kOpChunk, &tm_q, &c.fullK[0], 64 * lane, u * G);
+                    if (j16 < 2)
+                        tma_load_2d(dst0, &tm_kc, &c.fullK[0], 64 * half0, y0);
+                    issued = 1;
+                    pre_issued = true;
+                    bool okv = true;
+                    if (lane == 0)
+                        okv = mbar_wait(&c.emptyV[0], 1, &c.abort);
+                    if (!__shfl_sync(0xffffffffu, okv ? 1 : 0, 0)) {
+                        if (lane == 0) {   // no V requested: complete its phase for the drain
+                            mbar_arrive(&c.fullV[0]);
+                            fail(c, p.err);
+                        }
+                        break;
+                    }
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(&c.fullV[0], 2u * 2u * 64u * 128u);
+                    __syncwarp();
+                    if (j16 >= 2 && j16 < 4)
+                        tma_load_2d(dst0, &tm_vc, &c.fullV[0], 64 * half0, y0);
+                }
+                const bool pre = pre_issued && i == 0;
                 if (first) {
                     ++seg;
                     if (lane == 0 && ok && seg >= 2)
@@ -787,13 +843,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const int Ln = seg_len - 1;  // position of the new row
                         const int jn = p.page_size == 0 ? ((Ln - seg_ws) >> 4)
                                                         : ((Ln >> 4) - (seg_ws >> 4));
-                        if (wpage_pf) {
-                            app_page = __shfl_sync(0xffffffffu, wpage, max(0, min(jn, 31)));
-                            // the new row outside the window (a sequence no longer than its
-                            // sinks): look its page up directly
-                            if ((jn < 0 || jn >= min(p.n_wbox, 32)) && Ln >= 0)
-                                app_page = __ldg(p.page_table + b * p.max_pages + (Ln >> 4));
-                        }
+                        seg_jn = jn;
                         const int t_new = (64 * p.n_cbox + 16 * jn) / kTile;
                         const int t_end = min(ntiles_of(b) - 1, t + (n_tiles - 1 - i));
                         app_tile = (seg_len >= 1 && t_new >= t && t_new <= t_end) ? t_new : -1;
@@ -922,16 +972,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     __reduce_add_sync(0xffffffffu, kv == 1 ? static_cast<uint32_t>(rows) * 128u : 0u);
                 if (lane == 0) {
                     TileMeta &mt = c.meta[i % kMetaRing];
-                    mt.unit = u;
-                    mt.tile = t;
-                    mt.flags = (first ? kFlagFirst : 0) | (last ? kFlagLast : 0);
+                    if (!pre) {
+                        mt.unit = u;
+                        mt.tile = t;
+                        mt.flags = (first ? kFlagFirst : 0) | (last ? kFlagLast : 0);
+                    }
 #pragma unroll
                     for (int w = 0; w < 4; ++w)
                         mt.valid[w] = vw[w];
                     mbar_arrive(&c.meta_full[i % kMetaRing]);  // releases the metadata
-                    mbar_arrive_expect_tx(&c.fullK[s], bytes_k);  // (and for the MMA's flags)
+                    if (!pre)
+                        mbar_arrive_expect_tx(&c.fullK[s], bytes_k);  // (and for the MMA's flags)
                 }
                 __syncwarp();
+                if (pre) {
+                    // requested ahead; only the append may remain
+                    if (fused && app_tile >= 0 && !appended) {
+                        append_row(u, layer, b, kvh, L - 1);
+                        appended = true;
+                    }
+                    continue;
+                }
                 if (first && lane < 2) {
                     uint8_t *qb = smem + kQOff + (seg & 1) * kOpBytes;
                     tma_load_2d(qb + lane * kOpChunk, &tm_q, &c.fullK[s], 64 * lane, u * G);
