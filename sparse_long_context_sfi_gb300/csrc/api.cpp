@@ -426,6 +426,7 @@ static sfi_status select_impl(const sfi_kv_cache *kv, const float *scores_f,
     p.n_seq_active = (active && n_seq_active > 0 && n_seq_active < kv->batch) ? n_seq_active : 0;
     p.n_units = kv->n_layers * (p.n_seq_active > 0 ? p.n_seq_active : kv->batch) * kv->n_kv_heads;
     p.seq_len = kv->seq_len;
+    p.max_len = kv->max_len;
     p.active = active;
     p.n_sink = budget->n_sink;
     p.n_window = budget->n_window;

@@ -262,7 +262,13 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
     const int b = (u / p.n_kv_heads) % p.batch;
     if (p.active && !p.active[b])
         return;
-    const int L = min(p.seq_len[b], p.capacity);
+    const int L0 = p.seq_len[b];
+    if (L0 < 0 || L0 > p.max_len) {   // outside the caller's bound: no selection
+        if (tid == 0)
+            raise_error(p.err, 0x8u);  // SFI_DEVERR_LENGTH
+        return;
+    }
+    const int L = min(L0, p.capacity);
     const int S = p.n_sink, W = p.n_window;
     const int nC = max(0, L - W - S);
     const int K = min(p.n_select, nC);
@@ -517,6 +523,7 @@ __global__ void __maxnreg__(56) select_kernel(const SelectParams p)
 // all candidates kept) are taken by all of them together.
 
 constexpr int kClusterKeyCap = 33280;  // candidates per CTA (a 131K context in 4 CTAs)
+static_assert(kClusterKeyCap < 65536, "a CTA's first-pass counts are packed in 16 bits");
 constexpr int kMergeCap = 4096;        // threshold-bin keys exchanged as lists (else radix)
 constexpr int kMaxCluster = 4;         // CTAs per unit (the host picks 4 or 2)
 static_assert(NT == 1024, "the cluster's histogram passes take 4096 and 1024 bins");
@@ -525,7 +532,7 @@ size_t select_cluster_smem_bytes()
 {
     // keys: up to kClusterKeyCap candidates, 3 words of alignment slack before them and up
     // to 3 after (the copy is whole 16-byte pieces)
-    return (3 * 4096 + kClusterKeyCap + 8) * sizeof(uint32_t);
+    return (3 * 4096 + 2048 + kClusterKeyCap + 8) * sizeof(uint32_t);
 }
 
 __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
@@ -551,7 +558,15 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
     if (p.active && !p.active[b])
         return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int L = min(p.seq_len[b], p.capacity);
+    const int L0 = p.seq_len[b];
+    // outside the caller's bound (which sized the shared-memory staging): no selection, in
+    // every CTA of the cluster alike
+    if (L0 < 0 || L0 > p.max_len) {
+        if (tid == 0 && rank == 0)
+            raise_error(p.err, 0x8u);  // SFI_DEVERR_LENGTH
+        return;
+    }
+    const int L = min(L0, p.capacity);
     const int S = p.n_sink, W = p.n_window;
     const int nC = max(0, L - W - S);
     const int K = min(p.n_select, nC);
@@ -578,7 +593,8 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
     extern __shared__ __align__(16) uint32_t dyn[];
     uint32_t *hbuf0 = dyn, *hbuf1 = dyn + 4096;  // local histograms, by pass parity
     uint32_t *gsum = dyn + 2 * 4096;             // the cluster's sums
-    uint32_t *kraw = dyn + 3 * 4096;             // staged evidence, then keys
+    uint32_t *hpk = dyn + 3 * 4096;              // the first pass's counts, packed for the peers
+    uint32_t *kraw = dyn + 3 * 4096 + 2048;      // staged evidence, then keys
 
     // ---- stage this CTA's candidates (16-byte loads, all in flight together) ------------
     const float *fg = p.f + static_cast<size_t>(u) * p.capacity + S + c0;
@@ -617,6 +633,16 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
         ks[i] = k;
         atomicAdd(&hbuf0[k >> 20], 1u);
     }
+    // the counts packed for the exchange in 16 bits, bins 2j and 2j + 1 in the low and high
+    // half of word j (a CTA holds at most kClusterKeyCap < 2^16 keys): the peers then read
+    // half the bytes (counting into packed words directly was slower: the few occupied bins
+    // collide)
+    __syncthreads();
+    {
+        const uint4 h4 = reinterpret_cast<const uint4 *>(hbuf0)[tid];
+        reinterpret_cast<uint2 *>(hpk)[tid] = make_uint2((h4.x & 0xFFFFu) | (h4.y << 16),
+                                                         (h4.z & 0xFFFFu) | (h4.w << 16));
+    }
     // digit of the histogram hist (nb bins) where the running count from the top first
     // reaches krem (sh_digit, and the count above it in sh_above; two barriers)
     auto find_digit = [&](const uint32_t *hist, int nb, int krem_now) {
@@ -624,22 +650,23 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
     };
     // the same over the cluster's summed histogram; every CTA computes the same digit
     // (this thread's nb / NT bins, 4 consecutive ones for the 4096-bin pass, from each of the
-    // C <= 4 CTAs: one 16-byte remote load per CTA, all issued before the first is used)
+    // C <= 4 CTAs: one 8-byte remote load of packed 16-bit counts per CTA for the 4096-bin
+    // pass, all issued before the first is used; the sums in 32 bits)
     auto merged_digit = [&](const uint32_t *mine, int nb, int krem_now) {
         cluster_sync_all();  // every CTA's local histogram of this pass is complete
         if (nb == 4 * NT) {
-            uint4 v[kMaxCluster];
+            uint2 v[kMaxCluster];
 #pragma unroll
             for (int r = 0; r < kMaxCluster; ++r)
-                v[r] = r < C ? ld_cluster_v4_u32(map_to_rank(mine + 4 * tid, static_cast<uint32_t>(r)))
-                             : make_uint4(0u, 0u, 0u, 0u);
+                v[r] = r < C ? ld_cluster_v2_u32(map_to_rank(mine + 2 * tid, static_cast<uint32_t>(r)))
+                             : make_uint2(0u, 0u);
             uint4 h = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
             for (int r = 0; r < kMaxCluster; ++r) {
-                h.x += v[r].x;
-                h.y += v[r].y;
-                h.z += v[r].z;
-                h.w += v[r].w;
+                h.x += v[r].x & 0xFFFFu;
+                h.y += v[r].x >> 16;
+                h.z += v[r].y & 0xFFFFu;
+                h.w += v[r].y >> 16;
             }
             reinterpret_cast<uint4 *>(gsum)[tid] = h;
         } else {
@@ -657,7 +684,7 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
         find_digit(gsum, nb, krem_now);
     };
     int krem = K;
-    merged_digit(hbuf0, 4096, krem);
+    merged_digit(hpk, 4096, krem);
     const uint32_t d0 = sh_digit;
     uint32_t prefix = d0 << 20, pmask = 0xFFF00000u;
     krem -= sh_above;
@@ -693,7 +720,7 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
             sh_counts[1] = sh_lcnt;
         }
         cluster_sync_all();  // every CTA's list and counts are in place
-        // the merged list in hbuf0 (free now: the peers read it before this barrier), the
+        // the merged list in hbuf0 (free now: the peers read the packed copy), the
         // CTAs' lists in rank order; the lists before this CTA's end at `mine0`
         int lens[kMaxCluster], gts[kMaxCluster];
 #pragma unroll

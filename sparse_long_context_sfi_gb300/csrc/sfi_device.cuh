@@ -501,6 +501,17 @@ __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_addr)
     return v;
 }
 
+// Two consecutive 32-bit words of a cluster shared-memory address (8-byte aligned).
+__device__ __forceinline__ uint2 ld_cluster_v2_u32(uint32_t cluster_addr)
+{
+    uint2 v;
+    asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
 // Four consecutive 32-bit words of a cluster shared-memory address (16-byte aligned).
 __device__ __forceinline__ uint4 ld_cluster_v4_u32(uint32_t cluster_addr)
 {

@@ -58,6 +58,7 @@ struct SelectParams {
     const float *f;             // [units][capacity]
     int capacity, batch, n_kv_heads;
     int n_units;                // units launched (all, or the active sequences' with n_seq_active)
+    int max_len;                // bound of every seq_len entry (a longer one: SFI_DEVERR_LENGTH)
     const int32_t *seq_len;
     const uint8_t *active;
     int n_sink, n_window, n_select, prior_tau;

@@ -153,3 +153,35 @@ def test_single_cta_selector_on_refined_scores_bit_exact(lo, hi):
             want = oracle.topk(ref[h], K) + S
             np.testing.assert_array_equal(sel[u0 + h, :cnt[u0 + h]], want,
                                           err_msg=f"sequence {b} head {h}, L={L}")
+
+
+@pytest.mark.parametrize("batch", [BATCH, CL_BATCH], ids=["single_cta", "clustered"])
+def test_length_beyond_bound_sets_error_and_skips_unit(batch):
+    """A sequence whose length exceeds the launch's bound (kv.max_len, which sizes the
+    shared-memory staging) gets no selection and raises SFI_DEVERR_LENGTH, on both Selector
+    kernels; the other sequences' selections still equal the oracle's bit for bit."""
+    import sparse_long_context_sfi_gb300 as sfi
+    cfg, st, rng = make_state(12000, 30000, 1980, seed=11 + batch, batch=batch)
+    S, W, K, H = cfg.n_sink, cfg.n_window, cfg.n_select, cfg.n_kv_heads
+    f = np.zeros((st.n_units, st.capacity), np.float32)
+    for u in range(st.n_units):
+        L = int(st.len0[u // H])
+        f[u, :L] = evidence(KINDS[u % len(KINDS)], L, rng)
+    st.scores.copy_(torch.from_numpy(f))
+    lens = st.len0.astype(np.int32).copy()
+    lens[0] = st.kv.max_len + 100
+    st.seq_len.copy_(torch.from_numpy(lens))
+    st.sel_cnt.fill_(-7)
+    sfi.sfi_select(st.kv, st.scores, st.budget, st.mem)
+    torch.cuda.synchronize()
+    assert sfi.sfi_read_error(st.kv) == 0x8
+    sfi.sfi_clear_error(st.kv)
+    sel, cnt = st.sel_idx.cpu().numpy(), st.sel_cnt.cpu().numpy()
+    for u in range(st.n_units):
+        if u // H == 0:
+            assert cnt[u] == -7, f"unit {u}: selected beyond the bound"
+            continue
+        L = int(lens[u // H])
+        want = oracle.select(L, S, W, K, cfg.prior_tau, cfg.lam, f[u, :L])
+        assert cnt[u] == len(want)
+        np.testing.assert_array_equal(sel[u, :cnt[u]], want, err_msg=f"unit {u}")
