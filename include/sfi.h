@@ -333,11 +333,12 @@ sfi_status sfi_schedule_tokens(int32_t steps, const int32_t *tokens, const int32
  *   pipeline_group layers per dense launch with side_stream set (the Selector and packing of
  *             one group overlap the attention of the next): 0 = about a quarter of the layers
  *   concurrent_fast 1: on a step that mixes slow and fast sequences, the fast sequences'
- *             sfi_fast_decode_step runs on side_stream beside the slow sequences'
- *             append -> dense -> select -> compact chain on `stream` (they touch disjoint
- *             sequences, packed memory and workspace regions), both grids sized for the
- *             whole GPU; `stream` waits for side_stream before the step ends. Requires side_stream, fork_event and join_event (re-used per
- *             step as a fork and a join); replaces the layer-wise pipeline; 0 = off.
+ *             sfi_fast_decode_step runs on side_stream beside the slow sequences' Selector
+ *             and packing on `stream`, forked after their append, dense and evidence
+ *             launches (they touch disjoint sequences, packed memory and workspace
+ *             regions); `stream` waits for side_stream before the step ends. Requires
+ *             side_stream, fork_event and join_event (re-used per step as a fork and a
+ *             join); replaces the layer-wise pipeline; 0 = off.
  *             events[2t], events[2t+1] then bracket the slow chain's dense kernel alone.
  * Results with the layer-wise pipeline equal those without up to the rounding of the dense
  * step's split-KV partition (one launch per group of layers instead of one for all layers);

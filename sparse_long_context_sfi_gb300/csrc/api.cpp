@@ -729,13 +729,17 @@ sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
         if (mixed && conc_req) {
             // The slow subset's chain and the other sequences' fused fast step touch disjoint
             // sequences, cache rows, packed memory and workspace regions: the fast step runs
-            // on the side stream beside the chain. Both attention grids are sized for the
-            // whole GPU and the hardware interleaves their CTAs (splitting the SMs between
-            // them by bytes was measured slower: the chain's Selector and packing then leave
-            // the slow side's share idle).
+            // on the side stream beside the chain's Selector and packing, forked after the
+            // chain's dense and evidence launches. Both attention kernels take one CTA per SM
+            // and would mostly queue behind each other; the Selector and packing leave the
+            // GPU largely idle (forking before the dense launch, or splitting the SMs between
+            // the two by bytes, was measured slower).
             cudaStream_t ms = as_stream(stream), ss = as_stream(plan->side_stream);
             cudaEvent_t fork = static_cast<cudaEvent_t>(plan->fork_event);
             cudaEvent_t join = static_cast<cudaEvent_t>(plan->join_event);
+            if ((st = dense_impl(&k, q, out, plan->out_fp32, plan->scores_f, m_slow, ws, ws_bytes,
+                                 stream, e0, e1, nullptr, 0, n_slow)) != SFI_OK)
+                return st;
             if (cudaEventRecord(fork, ms) != cudaSuccess || cudaStreamWaitEvent(ss, fork, 0) != cudaSuccess)
                 return SFI_ERR_CUDA;
             sfi_kv_cache kf = k;
@@ -745,9 +749,6 @@ sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
             // joined on every path once forked, so a stream capture around the call stays joinable
             if (cudaEventRecord(join, ss) != cudaSuccess && st == SFI_OK)
                 st = SFI_ERR_CUDA;
-            if (st == SFI_OK)
-                st = dense_impl(&k, q, out, plan->out_fp32, plan->scores_f, m_slow, ws, ws_bytes,
-                                stream, e0, e1, nullptr, 0, n_slow);
             if (st == SFI_OK)
                 st = select_impl(&k, plan->scores_f, budget, mem, m_slow, n_slow, stream);
             if (st == SFI_OK)
