@@ -112,7 +112,8 @@ int sm_count()
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-    size_t tickets_dense, tickets_sparse, append_ctr, stats, part_dense, part_sparse, zbuf, total;
+    size_t tickets_dense, tickets_sparse, append_ctr, append_ctr_dense, stats, part_dense,
+        part_sparse, zbuf, total;
 };
 
 WsLayout ws_layout(const sfi_kv_cache *kv, int sms)
@@ -125,6 +126,7 @@ WsLayout ws_layout(const sfi_kv_cache *kv, int sms)
     w.tickets_dense = o;  o = align256(o + units * sizeof(int));
     w.tickets_sparse = o; o = align256(o + units * sizeof(int));
     w.append_ctr = o;     o = align256(o + sizeof(int));
+    w.append_ctr_dense = o; o = align256(o + sizeof(int));
     w.stats = o;          o = align256(o + units * g * sizeof(float2));
     w.part_dense = o;     o = align256(o + part);
     w.part_sparse = o;    o = align256(o + part);
@@ -182,30 +184,48 @@ uint64_t cache_rows(const sfi_kv_cache *kv)
 // that kv covers (a one-layer view of a larger cache keeps the per-unit regions of the whole
 // cache, so the tickets and counters of every other launch stay where they are).
 // n_seq_active > 0: exactly that many sequences have active[b] set (the evidence pass then
-// launches only their units).
+// launches only their units). k_new/v_new: the append of the active sequences' new rows is
+// fused in, as in the fast step (kv->max_len then bounds the lengths before the append; whole
+// caches only: the last CTA advances seq_len).
 sfi_status dense_impl(const sfi_kv_cache *kv, const void *q, void *out, int32_t out_fp32,
                       float *scores_f, const uint8_t *active, void *ws, size_t ws_bytes,
                       void *stream, cudaEvent_t e0, cudaEvent_t e1,
                       const sfi_kv_cache *ws_kv = nullptr, long long unit0 = 0,
-                      int n_seq_active = 0)
+                      int n_seq_active = 0, const void *k_new = nullptr,
+                      const void *v_new = nullptr)
 {
     sfi_status st = check_kv(kv);
     if (st != SFI_OK)
         return st;
     if (!q || !out || !aligned16(q))
         return SFI_ERR_INVALID_ARG;
+    const bool fused = k_new != nullptr || v_new != nullptr;
+    if (fused) {
+        if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new) || ws_kv)
+            return SFI_ERR_INVALID_ARG;
+        if (kv->max_len + 1 > kv->capacity)
+            return SFI_ERR_CAPACITY;
+    }
+    const int len_bound = kv->max_len + (fused ? 1 : 0);  // lengths after the append
     const int sms = sm_count();
     if (sms <= 0)
         return SFI_ERR_CUDA;
     const WsLayout w = ws_layout(ws_kv ? ws_kv : kv, sms);
     if (!ws || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u))
         return SFI_ERR_WORKSPACE;
-    if (kv->max_len == 0)
+    if (len_bound == 0)
         return SFI_OK;
     char *base = static_cast<char *>(ws);
     AttnParams p;
     fill_common(p, kv, active);
     const int g = p.group;
+    if (fused) {
+        p.k_new = k_new;
+        p.v_new = v_new;
+        p.k_cache = kv->k;
+        p.v_cache = kv->v;
+        p.append_counter = reinterpret_cast<int *>(base + w.append_ctr_dense);
+    }
     p.out = out;
     p.out_fp32 = out_fp32 ? 1 : 0;
     p.zbuf = scores_f ? reinterpret_cast<float *>(base + w.zbuf) +
@@ -221,7 +241,7 @@ sfi_status dense_impl(const sfi_kv_cache *kv, const void *q, void *out, int32_t 
     if (!make_map(&tk, kv->k, cache_rows(kv), box) || !make_map(&tv, kv->v, cache_rows(kv), box) ||
         !make_map(&tq, q, static_cast<uint64_t>(units) * g, static_cast<uint32_t>(g)))
         return SFI_ERR_CUDA;
-    const long long t_upper = units * ((kv->max_len + kTile - 1) / kTile);
+    const long long t_upper = units * ((len_bound + kTile - 1) / kTile);
     const int grid = static_cast<int>(t_upper < sms ? t_upper : sms);
     if (e0 && record_event(e0, as_stream(stream)) != cudaSuccess)
         return SFI_ERR_CUDA;
@@ -232,7 +252,7 @@ sfi_status dense_impl(const sfi_kv_cache *kv, const void *q, void *out, int32_t 
         return SFI_ERR_CUDA;
     if (scores_f) {
         e = launch_evidence(p.zbuf, p.stats, scores_f, kv->seq_len, active, kv->n_layers,
-                            kv->batch, kv->n_kv_heads, g, kv->capacity, kv->max_len,
+                            kv->batch, kv->n_kv_heads, g, kv->capacity, len_bound,
                             as_stream(stream),
                             (active && n_seq_active > 0 && n_seq_active < kv->batch) ? n_seq_active : 0);
         if (e != cudaSuccess)
@@ -708,21 +728,32 @@ sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
         const uint8_t *m_fast = mixed ? m_slow + B : nullptr;
         const void *k_new = static_cast<const char *>(plan->k_new) + t * kv_step * 2;
         const void *v_new = static_cast<const char *>(plan->v_new) + t * kv_step * 2;
-        // The slow sequences' rows are appended here; the fast ones' inside the fast step.
-        k.max_len = plan->len_start + t;
-        if (plan->dense_only || n_slow > 0) {
-            st = sfi_append_kv(&k, k_new, v_new, plan->dense_only ? nullptr : m_slow, stream);
+        // The new rows are appended inside the step's attention kernel: the fast sequences'
+        // by the fast step, the slow sequences' by the dense step (kd: the dense launch's
+        // cache view, whose max_len then bounds the lengths before the append) on a
+        // contiguous cache. A paged cache, and the layer-wise pipeline's per-group dense
+        // launches, append the slow sequences' rows first (on a paged cache the dense step's
+        // page lookup for the row, on the producer's path, was measured slower than the
+        // separate launch).
+        sfi_kv_cache kd = k;
+        kd.max_len = plan->len_start + t;
+        const bool sep_append = (plan->dense_only || n_slow > 0) && (k.page_size != 0 || (n_slow > 0 && pipe));
+        if (sep_append) {
+            st = sfi_append_kv(&kd, k_new, v_new, plan->dense_only ? nullptr : m_slow, stream);
             if (st != SFI_OK)
                 return st;
+            kd.max_len = plan->len_start + t + 1;
         }
+        const void *kd_new = sep_append ? nullptr : k_new;
+        const void *vd_new = sep_append ? nullptr : v_new;
         k.max_len = plan->len_start + t + 1;
         const void *q = static_cast<const char *>(plan->q) + t * q_step * 2;
         void *out = static_cast<char *>(plan->out) + t * o_step;
         cudaEvent_t e0 = plan->events ? static_cast<cudaEvent_t>(plan->events[2 * t]) : nullptr;
         cudaEvent_t e1 = plan->events ? static_cast<cudaEvent_t>(plan->events[2 * t + 1]) : nullptr;
         if (plan->dense_only) {
-            if ((st = dense_impl(&k, q, out, plan->out_fp32, nullptr, nullptr, ws, ws_bytes, stream,
-                                 e0, e1)) != SFI_OK)
+            if ((st = dense_impl(&kd, q, out, plan->out_fp32, nullptr, nullptr, ws, ws_bytes, stream,
+                                 e0, e1, nullptr, 0, 0, kd_new, vd_new)) != SFI_OK)
                 return st;
             continue;
         }
@@ -737,8 +768,8 @@ sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
             cudaStream_t ms = as_stream(stream), ss = as_stream(plan->side_stream);
             cudaEvent_t fork = static_cast<cudaEvent_t>(plan->fork_event);
             cudaEvent_t join = static_cast<cudaEvent_t>(plan->join_event);
-            if ((st = dense_impl(&k, q, out, plan->out_fp32, plan->scores_f, m_slow, ws, ws_bytes,
-                                 stream, e0, e1, nullptr, 0, n_slow)) != SFI_OK)
+            if ((st = dense_impl(&kd, q, out, plan->out_fp32, plan->scores_f, m_slow, ws, ws_bytes,
+                                 stream, e0, e1, nullptr, 0, n_slow, kd_new, vd_new)) != SFI_OK)
                 return st;
             if (cudaEventRecord(fork, ms) != cudaSuccess || cudaStreamWaitEvent(ss, fork, 0) != cudaSuccess)
                 return SFI_ERR_CUDA;
@@ -764,8 +795,9 @@ sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
                                        stream, e0, e1)) != SFI_OK)
                 return st;
         } else if (n_slow > 0) {
-            if ((st = dense_impl(&k, q, out, plan->out_fp32, plan->scores_f, m_slow, ws, ws_bytes,
-                                 stream, e0, e1, nullptr, 0, mixed ? n_slow : 0)) != SFI_OK ||
+            if ((st = dense_impl(&kd, q, out, plan->out_fp32, plan->scores_f, m_slow, ws, ws_bytes,
+                                 stream, e0, e1, nullptr, 0, mixed ? n_slow : 0, kd_new,
+                                 vd_new)) != SFI_OK ||
                 (st = select_impl(&k, plan->scores_f, budget, mem, m_slow, mixed ? n_slow : 0,
                                   stream)) != SFI_OK ||
                 (st = compact_impl(&k, budget, mem, m_slow, mixed ? n_slow : 0, stream)) != SFI_OK)

@@ -226,9 +226,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tma_prefetch_map(lane == 0 ? &tm_k : lane == 1 ? &tm_v : lane == 2 ? &tm_q
                                     : lane == 3 ? &tm_kc : &tm_vc);
     // CL: the clustered fast step, compiled as its own instance (launched only with
-    // p.cluster > 1), so neither instance carries the other's code paths
+    // p.cluster > 1), so neither instance carries the other's code paths; with DENSE, the
+    // dense step with the fused append
     constexpr bool clustered = !DENSE && CL;
-    const bool fused = !DENSE && p.k_new != nullptr;
+    // fused append (the fast step with p.k_new set; the dense step's instance with CL set):
+    // the new K/V rows are written at position seq_len[b] and attended, and the last CTA
+    // advances seq_len. The plain dense instance carries none of the append's code.
+    const bool fused = DENSE ? CL : (p.k_new != nullptr);
     // Clustered fast step: this CTA's unit and its static slice [cl_t0, cl_t0 + cl_n) of the
     // unit's tiles (the MMA and softmax roles iterate over the whole slice; a unit found
     // inactive only gets empty tiles and no output). Producer state: the unit's packed row
@@ -716,7 +720,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 } else {
                     // the page of window box seg_jn from the segment's prefetch (all lanes take
                     // part in the shuffle), or, for a row outside the window (a sequence no
-                    // longer than its sinks), a direct lookup
+                    // longer than its sinks) and in the dense step, a direct lookup
                     int page = wpage_pf ? __shfl_sync(0xffffffffu, wpage, max(0, min(seg_jn, 31))) : 0;
                     if (!wpage_pf || seg_jn < 0 || seg_jn >= min(p.n_wbox, 32))
                         page = __ldg(p.page_table + bb * p.max_pages + (pos >> 4));
@@ -841,10 +845,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                     if (fused) {
                         const int Ln = seg_len - 1;  // position of the new row
-                        const int jn = p.page_size == 0 ? ((Ln - seg_ws) >> 4)
-                                                        : ((Ln >> 4) - (seg_ws >> 4));
-                        seg_jn = jn;
-                        const int t_new = (64 * p.n_cbox + 16 * jn) / kTile;
+                        int t_new;
+                        if (DENSE) {
+                            t_new = Ln / kTile;  // the tile of the unit's positions that holds it
+                        } else {
+                            const int jn = p.page_size == 0 ? ((Ln - seg_ws) >> 4)
+                                                            : ((Ln >> 4) - (seg_ws >> 4));
+                            seg_jn = jn;
+                            t_new = (64 * p.n_cbox + 16 * jn) / kTile;
+                        }
                         const int t_end = min(ntiles_of(b) - 1, t + (n_tiles - 1 - i));
                         app_tile = (seg_len >= 1 && t_new >= t && t_new <= t_end) ? t_new : -1;
                         appended = false;
@@ -1681,7 +1690,10 @@ cudaError_t launch_attn_t(const CUtensorMap &tm_k, const CUtensorMap &tm_v, cons
                           int grid, cudaStream_t stream)
 {
     const int cluster = (!DENSE && p.cluster > 1) ? p.cluster : 1;
-    auto kern = cluster > 1 ? attn_kernel<G, false, true> : attn_kernel<G, DENSE, false>;
+    // dense: the instance with the fused append when p.k_new is set
+    auto kern = cluster > 1 ? attn_kernel<G, false, true>
+                            : (DENSE && p.k_new != nullptr) ? attn_kernel<G, DENSE, true>
+                                                            : attn_kernel<G, DENSE, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess)
         return e;

@@ -375,6 +375,37 @@ def test_end_to_end_concurrent_fast_on_mixed_steps(name):
     assert np.array_equal(out_c, out_s)
 
 
+@pytest.mark.parametrize("name", ["ragged_paged_b32", "llama8b_ctx32k_b4"])
+def test_dense_only_run_appends(name):
+    """A decode run in dense-only mode: every step is dense attention over the whole cache,
+    with the step's new K/V rows appended inside the dense kernel on a contiguous cache (its
+    last CTA advances the lengths) and by the append kernel on a paged one. Every step and
+    unit against the oracle's run with every step slow; the lengths end one row per step
+    longer."""
+    steps = 10
+    if name == "ragged_paged_b32":
+        wl = small(name, batch=6, ctx=2400, ctx_lo=600, steps=steps, mask_param=5)
+    else:
+        wl = small(name, batch=3, ctx=2000, ctx_lo=2000, steps=steps)
+    cfg = wl.cfg
+    st = sdev.make_state(wl, on_device=True)
+    ins = sdev.DeviceInputs(wl, steps, st.k.device, on_device=True)
+    every = np.ones((steps, cfg.batch), np.uint8)
+    out = torch.zeros((steps, cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim),
+                      dtype=torch.float32, device=st.k.device)
+    st.run(st.make_plan(every, ins.q, ins.k_new, ins.v_new, out, dense_only=True))
+    torch.cuda.synchronize()
+    assert int(st.err[0]) == 0
+    np.testing.assert_array_equal(st.seq_len.cpu().numpy(), wl.len0 + steps)
+    ref = odecode.run(wl, steps=steps, slow=every.T)
+    o, G = out.cpu().numpy(), cfg.group
+    for t in range(steps):
+        for u in range(st.n_units):
+            layer, b, kvh = unit_coords(cfg, u)
+            ok, err = close(o[t, layer, b, kvh * G:(kvh + 1) * G], ref["out"][t][u])
+            assert ok, f"step {t} unit {u}: max err {err}"
+
+
 @pytest.mark.parametrize("layers", [1, 2])
 def test_slow_subset_launch_bit_exact(layers):
     """A decode run whose second step is slow for two of six sequences: the Selector, the
