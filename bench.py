@@ -325,8 +325,11 @@ def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=N
     res["ms_per_run"] = ms / k_steps
     res["tokens_per_run"] = tokens_per_run
     res["slow_steps"] = int(slow.any(axis=1).sum())
-    # slow step: append, dense, evidence, select, compact; fast step: one fused kernel
-    res["launches_per_run"] = int(sum((5 if r.any() else 0) + (0 if r.all() else 1) for r in slow))
+    # slow step: dense (with the append fused in on a contiguous cache; a separate append
+    # kernel first on a paged one), evidence, select, compact; fast step: one fused kernel
+    per_slow = 4 if cfg.page_size == 0 else 5
+    res["launches_per_run"] = int(sum((per_slow if r.any() else 0) + (0 if r.all() else 1)
+                                      for r in slow))
     sel_rows = (st.rows.view(cfg.n_layers, cfg.batch, cfg.n_kv_heads).float().mean(dim=(0, 2))
                 .cpu().numpy())
 
