@@ -192,7 +192,7 @@ sfi_status dense_impl(const sfi_kv_cache *kv, const void *q, void *out, int32_t 
                       void *stream, cudaEvent_t e0, cudaEvent_t e1,
                       const sfi_kv_cache *ws_kv = nullptr, long long unit0 = 0,
                       int n_seq_active = 0, const void *k_new = nullptr,
-                      const void *v_new = nullptr)
+                      const void *v_new = nullptr, bool evidence = true)
 {
     sfi_status st = check_kv(kv);
     if (st != SFI_OK)
@@ -250,7 +250,9 @@ sfi_status dense_impl(const sfi_kv_cache *kv, const void *q, void *out, int32_t 
         return SFI_ERR_CUDA;
     if (e1 && record_event(e1, as_stream(stream)) != cudaSuccess)
         return SFI_ERR_CUDA;
-    if (scores_f) {
+    // (evidence false: the logits and statistics are left for the Selector, which computes
+    // the evidence itself)
+    if (scores_f && evidence) {
         e = launch_evidence(p.zbuf, p.stats, scores_f, kv->seq_len, active, kv->n_layers,
                             kv->batch, kv->n_kv_heads, g, kv->capacity, len_bound,
                             as_stream(stream),
@@ -424,12 +426,54 @@ sfi_status sfi_dense_decode_attn(const sfi_kv_cache *kv, const void *q, void *ou
                       nullptr);
 }
 
+// How sfi_select runs for these arguments: the units it launches, whether the evidence is
+// staged in shared memory, and the CTAs per unit (1: one CTA per unit; > 1: clustered).
+struct SelectShape {
+    int n_seq_active, n_units, staged, cluster;
+};
+
+static SelectShape select_shape(const sfi_kv_cache *kv, const float *scores_f,
+                                const sfi_budget *budget, const uint8_t *active, int n_seq_active)
+{
+    SelectShape sh;
+    sh.n_seq_active = (active && n_seq_active > 0 && n_seq_active < kv->batch) ? n_seq_active : 0;
+    sh.n_units = kv->n_layers * (sh.n_seq_active > 0 ? sh.n_seq_active : kv->batch) * kv->n_kv_heads;
+    // Stage in shared memory when every unit's candidates (with up to 3 values of alignment
+    // slack on either side) fit, and the copy's tail stays inside the unit's row.
+    const long long bound = static_cast<long long>(kv->max_len) - budget->n_window - budget->n_sink;
+    const bool stageable = aligned16(scores_f) &&
+                           static_cast<long long>(kv->max_len) - budget->n_window + 3 <= kv->capacity;
+    sh.staged = (stageable && bound + 3 <= kStageCap) ? 1 : 0;
+    // A unit's candidates split over a cluster of CTAs (each stages its share) when they fit.
+    sh.cluster = 1;
+    if (stageable) {
+        const int C = select_cluster_size(4);
+        const long long ctas = static_cast<long long>(sh.n_units) * C;
+        if (C > 1 && (bound + C - 1) / C <= select_cluster_key_cap() && ctas <= 2LL * sm_count())
+            sh.cluster = C;  // at most about two waves of CTAs
+    }
+    return sh;
+}
+
+// Whether sfi_decode_run's slow step leaves the evidence to the Selector (clustered, group of
+// 4): one launch fewer, the evidence computed as the Selector stages its candidates.
+static bool select_fuses_evidence(const sfi_kv_cache *kv, const float *scores_f,
+                                  const sfi_budget *budget, const uint8_t *active, int n_seq_active)
+{
+    return kv->n_q_heads == 4 * kv->n_kv_heads &&
+           select_shape(kv, scores_f, budget, active, n_seq_active).cluster > 1;
+}
+
 // sfi_select, with n_seq_active > 0 when the caller knows that exactly that many sequences
 // have active[b] set (sfi_decode_run's slow subsets): the launch then covers only their units,
-// which lets a small subset take the clustered Selector.
+// which lets a small subset take the clustered Selector. ev_ws: the workspace whose logits
+// and statistics the preceding dense launch (run without its evidence pass, whole-cache view)
+// left: the clustered Selector then computes the evidence itself and writes it to scores_f
+// (group of 4; the caller checked the shape with select_shape).
 static sfi_status select_impl(const sfi_kv_cache *kv, const float *scores_f,
                               const sfi_budget *budget, const sfi_sparse_mem *mem,
-                              const uint8_t *active, int n_seq_active, void *stream)
+                              const uint8_t *active, int n_seq_active, void *stream,
+                              void *ev_ws = nullptr)
 {
     sfi_status st = check_kv(kv);
     if (st != SFI_OK)
@@ -438,13 +482,15 @@ static sfi_status select_impl(const sfi_kv_cache *kv, const float *scores_f,
         return st;
     if (!scores_f || !mem || !mem->sel_idx || !mem->sel_cnt)
         return SFI_ERR_INVALID_ARG;
+    const SelectShape sh = select_shape(kv, scores_f, budget, active, n_seq_active);
     SelectParams p;
+    std::memset(&p, 0, sizeof p);
     p.f = scores_f;
     p.capacity = kv->capacity;
     p.batch = kv->batch;
     p.n_kv_heads = kv->n_kv_heads;
-    p.n_seq_active = (active && n_seq_active > 0 && n_seq_active < kv->batch) ? n_seq_active : 0;
-    p.n_units = kv->n_layers * (p.n_seq_active > 0 ? p.n_seq_active : kv->batch) * kv->n_kv_heads;
+    p.n_seq_active = sh.n_seq_active;
+    p.n_units = sh.n_units;
     p.seq_len = kv->seq_len;
     p.max_len = kv->max_len;
     p.active = active;
@@ -456,19 +502,16 @@ static sfi_status select_impl(const sfi_kv_cache *kv, const float *scores_f,
     p.sel_idx = mem->sel_idx;
     p.sel_cnt = mem->sel_cnt;
     p.err = kv->err;
-    // Stage in shared memory when every unit's candidates (with up to 3 values of alignment
-    // slack on either side) fit, and the copy's tail stays inside the unit's row.
-    const long long bound = static_cast<long long>(kv->max_len) - budget->n_window - budget->n_sink;
-    const bool stageable = aligned16(scores_f) &&
-                           static_cast<long long>(kv->max_len) - budget->n_window + 3 <= kv->capacity;
-    p.staged = (stageable && bound + 3 <= kStageCap) ? 1 : 0;
-    // A unit's candidates split over a cluster of CTAs (each stages its share) when they fit.
-    p.cluster = 1;
-    if (stageable) {
-        const int C = select_cluster_size(4);
-        const long long ctas = static_cast<long long>(p.n_units) * C;
-        if (C > 1 && (bound + C - 1) / C <= select_cluster_key_cap() && ctas <= 2LL * sm_count())
-            p.cluster = C;  // at most about two waves of CTAs
+    p.staged = sh.staged;
+    p.cluster = sh.cluster;
+    if (ev_ws) {
+        if (sh.cluster <= 1 || kv->n_q_heads != 4 * kv->n_kv_heads)
+            return SFI_ERR_INVALID_ARG;
+        const WsLayout w = ws_layout(kv, sm_count());
+        char *base = static_cast<char *>(ev_ws);
+        p.zbuf = reinterpret_cast<const float *>(base + w.zbuf);
+        p.stats = reinterpret_cast<const float2 *>(base + w.stats);
+        p.f_out = const_cast<float *>(scores_f);
     }
     return launch_status(launch_select(p, as_stream(stream)));
 }
@@ -768,8 +811,9 @@ sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
             cudaStream_t ms = as_stream(stream), ss = as_stream(plan->side_stream);
             cudaEvent_t fork = static_cast<cudaEvent_t>(plan->fork_event);
             cudaEvent_t join = static_cast<cudaEvent_t>(plan->join_event);
+            const bool fev = select_fuses_evidence(&k, plan->scores_f, budget, m_slow, n_slow);
             if ((st = dense_impl(&kd, q, out, plan->out_fp32, plan->scores_f, m_slow, ws, ws_bytes,
-                                 stream, e0, e1, nullptr, 0, n_slow, kd_new, vd_new)) != SFI_OK)
+                                 stream, e0, e1, nullptr, 0, n_slow, kd_new, vd_new, !fev)) != SFI_OK)
                 return st;
             if (cudaEventRecord(fork, ms) != cudaSuccess || cudaStreamWaitEvent(ss, fork, 0) != cudaSuccess)
                 return SFI_ERR_CUDA;
@@ -781,7 +825,8 @@ sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
             if (cudaEventRecord(join, ss) != cudaSuccess && st == SFI_OK)
                 st = SFI_ERR_CUDA;
             if (st == SFI_OK)
-                st = select_impl(&k, plan->scores_f, budget, mem, m_slow, n_slow, stream);
+                st = select_impl(&k, plan->scores_f, budget, mem, m_slow, n_slow, stream,
+                                 fev ? ws : nullptr);
             if (st == SFI_OK)
                 st = compact_impl(&k, budget, mem, m_slow, n_slow, stream);
             if (cudaStreamWaitEvent(ms, join, 0) != cudaSuccess && st == SFI_OK)
@@ -795,11 +840,12 @@ sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
                                        stream, e0, e1)) != SFI_OK)
                 return st;
         } else if (n_slow > 0) {
+            const int nsa = mixed ? n_slow : 0;
+            const bool fev = select_fuses_evidence(&k, plan->scores_f, budget, m_slow, nsa);
             if ((st = dense_impl(&kd, q, out, plan->out_fp32, plan->scores_f, m_slow, ws, ws_bytes,
-                                 stream, e0, e1, nullptr, 0, mixed ? n_slow : 0, kd_new,
-                                 vd_new)) != SFI_OK ||
-                (st = select_impl(&k, plan->scores_f, budget, mem, m_slow, mixed ? n_slow : 0,
-                                  stream)) != SFI_OK ||
+                                 stream, e0, e1, nullptr, 0, nsa, kd_new, vd_new, !fev)) != SFI_OK ||
+                (st = select_impl(&k, plan->scores_f, budget, mem, m_slow, nsa, stream,
+                                  fev ? ws : nullptr)) != SFI_OK ||
                 (st = compact_impl(&k, budget, mem, m_slow, mixed ? n_slow : 0, stream)) != SFI_OK)
                 return st;
         }

@@ -1614,7 +1614,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 constexpr int kEvPer = 4;   // positions per thread of the evidence kernel
 
 // Evidence f_j = (1/G) sum_h exp2(z_hj - M_h) / L_h from the dense step's base-2 logits
-// and merged statistics; one pass over [units][positions].
+// and merged statistics; one pass over [units][positions]. (The clustered Selector repeats
+// this arithmetic, term for term, when it computes the evidence itself.)
 template <int G>
 __global__ void __launch_bounds__(256) evidence_kernel(const float *__restrict__ zbuf,
                                                        const float2 *__restrict__ stats,
@@ -1670,7 +1671,7 @@ __global__ void __launch_bounds__(256) evidence_kernel(const float *__restrict__
             float acc = 0.f;
 #pragma unroll
             for (int h = 0; h < G; ++h)
-                acc += exp2f(z[r][h] - M[h]) * inv[h];
+                acc = fmaf(exp2f(z[r][h] - M[h]), inv[h], acc);
             fu[j] = acc * rg;
         }
     }
@@ -1679,7 +1680,7 @@ __global__ void __launch_bounds__(256) evidence_kernel(const float *__restrict__
         float acc = 0.f;
 #pragma unroll
         for (int h = 0; h < G; ++h)
-            acc += exp2f(__ldcs(zu + static_cast<size_t>(j) * G + h) - M[h]) * inv[h];
+            acc = fmaf(exp2f(__ldcs(zu + static_cast<size_t>(j) * G + h) - M[h]), inv[h], acc);
         fu[j] = acc * rg;
     }
 }

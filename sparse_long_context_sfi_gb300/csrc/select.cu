@@ -597,9 +597,31 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
     uint32_t *kraw = dyn + 3 * 4096 + 2048;      // staged evidence, then keys
 
     // ---- stage this CTA's candidates (16-byte loads, all in flight together) ------------
+    // With p.zbuf (group of 4) the evidence is computed here from the dense step's logits
+    // (one 16-byte load of four heads per candidate, the first 4 NT requested now) and the
+    // merged statistics, term for term as the evidence pass computes it, and written to
+    // p.f_out; otherwise the evidence pass's output is copied in.
+    const bool fev = p.zbuf != nullptr;
+    __shared__ float sh_M[4], sh_inv[4];
+    float4 zr[4];
     const float *fg = p.f + static_cast<size_t>(u) * p.capacity + S + c0;
-    const int off = static_cast<int>((reinterpret_cast<uintptr_t>(fg) & 15u) >> 2);
-    {
+    const int off = fev ? 0 : static_cast<int>((reinterpret_cast<uintptr_t>(fg) & 15u) >> 2);
+    const float4 *zg = fev ? reinterpret_cast<const float4 *>(p.zbuf) +
+                                 (static_cast<size_t>(u) * p.capacity + S + c0)
+                           : nullptr;
+    if (fev) {
+        if (tid < 4) {
+            const float2 st = __ldcg(p.stats + static_cast<size_t>(u) * 4 + tid);
+            sh_M[tid] = st.x;
+            sh_inv[tid] = st.y > 0.f ? 1.f / st.y : 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = e * NT + tid;
+            if (i < nloc)
+                zr[e] = __ldcg(zg + i);
+        }
+    } else {
         const uint4 *src = reinterpret_cast<const uint4 *>(fg - off);
         uint4 *dst = reinterpret_cast<uint4 *>(kraw);
         const int n16 = ((off + nloc) * 4 + 15) >> 4;
@@ -628,10 +650,42 @@ __global__ void __maxnreg__(56) select_cluster_kernel(const SelectParams p)
     uint32_t *ks = kraw + off;  // ks[i] = key of candidate c0 + i
 
     // ---- pass 0: keys in place, top-12-bit histogram --------------------------------------
-    for (int i = tid; i < nloc; i += NT) {
-        const uint32_t k = fz.key(__uint_as_float(ks[i]), c0 + i);
-        ks[i] = k;
-        atomicAdd(&hbuf0[k >> 20], 1u);
+    if (fev) {
+        const float M0 = sh_M[0], M1 = sh_M[1], M2 = sh_M[2], M3 = sh_M[3];
+        const float i0v = sh_inv[0], i1v = sh_inv[1], i2v = sh_inv[2], i3v = sh_inv[3];
+        float *fo = p.f_out + static_cast<size_t>(u) * p.capacity + S + c0;
+        for (int b0 = 0; b0 < nloc; b0 += 4 * NT) {
+            if (b0 > 0) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = b0 + e * NT + tid;
+                    if (i < nloc)
+                        zr[e] = __ldcg(zg + i);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = b0 + e * NT + tid;
+                if (i < nloc) {
+                    float acc = 0.f;
+                    acc = fmaf(exp2f(zr[e].x - M0), i0v, acc);
+                    acc = fmaf(exp2f(zr[e].y - M1), i1v, acc);
+                    acc = fmaf(exp2f(zr[e].z - M2), i2v, acc);
+                    acc = fmaf(exp2f(zr[e].w - M3), i3v, acc);
+                    const float fv = acc * 0.25f;
+                    fo[i] = fv;
+                    const uint32_t k = fz.key(fv, c0 + i);
+                    ks[i] = k;
+                    atomicAdd(&hbuf0[k >> 20], 1u);
+                }
+            }
+        }
+    } else {
+        for (int i = tid; i < nloc; i += NT) {
+            const uint32_t k = fz.key(__uint_as_float(ks[i]), c0 + i);
+            ks[i] = k;
+            atomicAdd(&hbuf0[k >> 20], 1u);
+        }
     }
     // the counts packed for the exchange in 16 bits, bins 2j and 2j + 1 in the low and high
     // half of word j (a CTA holds at most kClusterKeyCap < 2^16 keys): the peers then read

@@ -71,6 +71,12 @@ struct SelectParams {
     // > 0: the grid covers only the units of the first n_seq_active sequences with active[b]
     // set, per layer in order (the caller knows how many are active); 0: every unit
     int n_seq_active;
+    // clustered Selector, group of 4: with zbuf set the evidence of each candidate is computed
+    // here from the dense step's base-2 logits and merged statistics (as the evidence pass
+    // does) and written to f_out; f is then not read
+    const float *zbuf;          // [units][capacity][4]
+    const float2 *stats;        // [units][4]
+    float *f_out;               // [units][capacity]
 };
 // The Selector stages a unit's evidence in shared memory when it has at most this many
 // candidates (plus alignment slack); larger units stream it from global memory.
