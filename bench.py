@@ -117,9 +117,9 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def traffic_record(kernel: str):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on the current
-    kernel source (else None)."""
+def traffic_record(kernel: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on this workload
+    and the current kernel source (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -129,7 +129,7 @@ def traffic_record(kernel: str):
         return None
     src = os.path.join(ROOT, "sparse_long_context_sfi_gb300", "csrc", "attn.cu")
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return rec if rec.get("attn_cu_sha256_16") == h else None
+    return rec if rec.get("attn_cu_sha256_16") == h and rec.get("workload") == workload else None
 
 
 def dist_setup(n_gpus: int):
@@ -716,7 +716,7 @@ def main():
     peak, peak_kind = measured_peaks()
     ks = res["kernels"]
     dom_name, dom = max(ks.items(), key=lambda x: -1 if x[1] is None else x[1]["total_us_per_run"])
-    traffic = traffic_record(dom_name)
+    traffic = traffic_record(dom_name, args.workload)
     warm = {"achieved": dom["achieved_gbs"], "frac": dom["achieved_gbs"] / peak,
             "avg_launch_us": dom["avg_us"], "bytes_per_launch": dom["bytes_per_launch"],
             "how": "in the timed runs (CUDA events around every slow step's dense kernel and "
