@@ -325,16 +325,15 @@ def measure(wl, args, world, dev, stream, k_steps, warmup, extras, clock_index=N
     res["ms_per_run"] = ms / k_steps
     res["tokens_per_run"] = tokens_per_run
     res["slow_steps"] = int(slow.any(axis=1).sum())
-    # slow step: dense (with the append fused in on a contiguous cache; a separate append
-    # kernel first on a paged one), the evidence pass (computed inside the Selector when it
-    # runs clustered), select, compact; fast step: one fused kernel
+    # slow step: dense (with the append fused in), the evidence pass (computed inside the
+    # Selector when it runs clustered), select, compact; fast step: one fused kernel
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
     def slow_launches(n_slow):
         units = cfg.n_layers * n_slow * cfg.n_kv_heads
         bound = int(wl.len0.max()) + cfg.steps - cfg.n_window - cfg.n_sink
         clustered = cfg.group == 4 and -(-bound // 4) <= 33280 and units * 4 <= 2 * sms
-        return 3 + (0 if cfg.page_size == 0 else 1) + (0 if clustered else 1)
+        return 3 + (0 if clustered else 1)
     res["launches_per_run"] = int(sum((slow_launches(int(r.sum())) if r.any() else 0) +
                                       (0 if r.all() else 1) for r in slow))
     sel_rows = (st.rows.view(cfg.n_layers, cfg.batch, cfg.n_kv_heads).float().mean(dim=(0, 2))

@@ -299,7 +299,8 @@ sfi_status sfi_schedule_tokens(int32_t steps, const int32_t *tokens, const int32
  * A whole decode run on one stream (blog "How SFI Works": the two-speed loop). For each
  * step t, with row t of k_new/v_new: for the sequences whose slow flag is set,
  * sfi_append_kv -> sfi_dense_decode_attn (with evidence) -> sfi_select -> sfi_compact, where
- * on a contiguous cache (page_size 0) the append runs inside the dense launch; for the others
+ * the append runs inside the dense launch (and, with a clustered Selector, the evidence is
+ * computed by the Selector); for the others
  * sfi_fast_decode_step (append and sparse attention in one launch). Nothing is synchronised,
  * so the run can be captured in a CUDA graph and replayed (the caller restores seq_len before
  * each replay).
@@ -312,8 +313,8 @@ sfi_status sfi_schedule_tokens(int32_t steps, const int32_t *tokens, const int32
  *             when some step mixes slow and fast sequences; NULL if no step does
  *   len_start host bound of every seq_len before the first append
  *   dense_only 1: every step is append + dense attention without evidence (the full-KV
- *             baseline the pages compare against; the append fused into the dense launch
- *             on a contiguous cache); slow is ignored
+ *             baseline the pages compare against; the append fused into the dense
+ *             launch); slow is ignored
  *   events    optional host array of 2 * n_steps cudaEvent_t (as void*): events[2t] and
  *             events[2t+1] are recorded (external, so they survive graph capture) right
  *             before and after step t's attention kernel (the fused fast step's kernel on

@@ -773,16 +773,14 @@ sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
         const void *v_new = static_cast<const char *>(plan->v_new) + t * kv_step * 2;
         // The new rows are appended inside the step's attention kernel: the fast sequences'
         // by the fast step, the slow sequences' by the dense step (kd: the dense launch's
-        // cache view, whose max_len then bounds the lengths before the append) on a
-        // contiguous cache. A paged cache, and the layer-wise pipeline's per-group dense
-        // launches, append the slow sequences' rows first (on a paged cache the dense step's
-        // page lookup for the row, on the producer's path, was measured slower than the
-        // separate launch).
+        // cache view, whose max_len then bounds the lengths before the append). Only the
+        // layer-wise pipeline's per-group dense launches append the slow sequences' rows
+        // first.
         sfi_kv_cache kd = k;
         kd.max_len = plan->len_start + t;
-        const bool sep_append = (plan->dense_only || n_slow > 0) && (k.page_size != 0 || (n_slow > 0 && pipe));
+        const bool sep_append = n_slow > 0 && pipe;
         if (sep_append) {
-            st = sfi_append_kv(&kd, k_new, v_new, plan->dense_only ? nullptr : m_slow, stream);
+            st = sfi_append_kv(&kd, k_new, v_new, m_slow, stream);
             if (st != SFI_OK)
                 return st;
             kd.max_len = plan->len_start + t + 1;
