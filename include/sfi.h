@@ -338,8 +338,8 @@ sfi_status sfi_schedule_tokens(int32_t steps, const int32_t *tokens, const int32
  *             one group overlap the attention of the next): 0 = about a quarter of the layers
  *   concurrent_fast 1: on a step that mixes slow and fast sequences, the fast sequences'
  *             sfi_fast_decode_step runs on side_stream beside the slow sequences' Selector
- *             and packing on `stream`, forked after their append, dense and evidence
- *             launches (they touch disjoint sequences, packed memory and workspace
+ *             and packing on `stream`, forked after their dense launch (and evidence
+ *             pass, if separate) (they touch disjoint sequences, packed memory and workspace
  *             regions); `stream` waits for side_stream before the step ends. Requires
  *             side_stream, fork_event and join_event (re-used per step as a fork and a
  *             join); replaces the layer-wise pipeline; 0 = off.

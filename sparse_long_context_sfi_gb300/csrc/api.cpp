@@ -802,10 +802,11 @@ sfi_status sfi_decode_run(const sfi_kv_cache *kv, const sfi_budget *budget,
             // The slow subset's chain and the other sequences' fused fast step touch disjoint
             // sequences, cache rows, packed memory and workspace regions: the fast step runs
             // on the side stream beside the chain's Selector and packing, forked after the
-            // chain's dense and evidence launches. Both attention kernels take one CTA per SM
-            // and would mostly queue behind each other; the Selector and packing leave the
-            // GPU largely idle (forking before the dense launch, or splitting the SMs between
-            // the two by bytes, was measured slower).
+            // chain's dense launch (and its evidence pass, when the Selector does not compute
+            // the evidence itself). Both attention kernels take one CTA per SM and would
+            // mostly queue behind each other; the Selector and packing leave the GPU largely
+            // idle (forking before the dense launch, or splitting the SMs between the two by
+            // bytes, was measured slower).
             cudaStream_t ms = as_stream(stream), ss = as_stream(plan->side_stream);
             cudaEvent_t fork = static_cast<cudaEvent_t>(plan->fork_event);
             cudaEvent_t join = static_cast<cudaEvent_t>(plan->join_event);
