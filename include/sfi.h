@@ -101,6 +101,8 @@ typedef struct sfi_budget {
     float excl_mu;       /* cross-head exclusivity strength in [0, 1]                    */
     float norm_nu;       /* key-norm prior term: prior scaled by min(1, norm_nu/||k||)   */
     int32_t geometric;   /* 1: geometric (log-linear) mixture instead of arithmetic      */
+    float nms_delta;     /* Soft-NMS: only a neighbour at most nms_delta above suppresses */
+                         /* (scores that similar); 0 = any strictly higher neighbour     */
 } sfi_budget;
 
 /*
@@ -197,12 +199,15 @@ sfi_status sfi_key_norms(const sfi_kv_cache *kv, float *norms, const uint8_t *ac
  *   s_hj  = arithmetic: fl32(fl32(c1 f_hj) + fl32(c2 rt_hj))  (c1, c2 as in sfi_select), or
  *           geometric:  fl32(c1 log2 f_hj) + fl32(lambda log2 fl32(fl32(c2 rt_hj) / lambda))
  *           in fp32 with the library's own log2 (log-domain score of the geometric mixture);
- *   Soft-NMS: s'_hj = fl32(nms_gamma s_hj) if s_hj is strictly below the largest s_hi of the
- *           candidates i with 1 <= |i - j| <= nms_radius, else s_hj;
+ *   Soft-NMS (neighbouring tokens with similar scores are suppressed): s'_hj =
+ *           fl32(nms_gamma s_hj) if some candidate i with 1 <= |i - j| <= nms_radius has
+ *           s_hi > s_hj and, when nms_delta > 0, fl32(s_hi - s_hj) <= nms_delta; else s_hj;
  *   exclusivity: s''_hj = fl32(s'_hj - fl32(mu' fl32(T_j - s'_hj))), T_j = sum over heads of
  *           s'_hj in head order, mu' = fl32(excl_mu / (n_kv_heads - 1)).
  * refined: fp32 [units][capacity], written at the candidate positions. Select on it with
- * sfi_select and lambda = 0 (which keeps the scores as they are). n_kv_heads <= 16.
+ * sfi_select and lambda = 0 (which keeps the scores as they are). n_kv_heads <= 16, else
+ * SFI_ERR_UNSUPPORTED. A negative nms_radius, nms_gamma or excl_mu outside [0, 1], a
+ * negative or NaN nms_delta or norm_nu, or norm_nu > 0 without key_norms: SFI_ERR_INVALID_ARG.
  */
 sfi_status sfi_refine_scores(const sfi_kv_cache *kv, const float *scores_f,
                              const float *key_norms, const sfi_budget *budget, float *refined,

@@ -50,7 +50,7 @@ def load(path: str | None = None):
     lib.sfi_oracle_log2f.argtypes = [C.c_float]
     lib.sfi_oracle_log2f.restype = C.c_float
     lib.sfi_oracle_refine_scores.argtypes = [i32, i32, i32, i32, i32, f64, i32, C.c_float, P, i32,
-                                             C.c_float, C.c_float, P, P]
+                                             C.c_float, C.c_float, C.c_float, P, P]
     lib.sfi_oracle_key_norms.argtypes = [i32, i32, P, P]
     lib.sfi_oracle_key_norms.restype = None
     lib.sfi_oracle_attend_batch.argtypes = [i32, i32, i32, i32, P, P, P, P, i32, P, P, P, i32]
@@ -172,16 +172,17 @@ def log2f(x: float) -> float:
 
 
 def refine_scores(L, S, W, tau, lam, f32, geometric=False, nu=0.0, knorm=None, radius=0,
-                  gamma=1.0, mu=0.0):
+                  gamma=1.0, mu=0.0, delta=0.0):
     """Refined Selector scores of the H heads of one (layer, sequence): f32 [H][L] evidence,
-    knorm [H][L] key norms (or None). Returns fp32 [H][n_C]."""
+    knorm [H][L] key norms (or None); Soft-NMS over `radius` neighbours with factor `gamma`
+    and similarity limit `delta` (0: none). Returns fp32 [H][n_C]."""
     f32 = _c(f32, np.float32)
     H = f32.shape[0]
     n = max(0, L - W - S)
     out = np.zeros((H, max(n, 1)), dtype=np.float32)
     kn = None if knorm is None else _c(knorm, np.float32)
     n = lib().sfi_oracle_refine_scores(H, L, S, W, tau, lam, 1 if geometric else 0, nu,
-                                       None if kn is None else _p(kn), radius, gamma, mu,
+                                       None if kn is None else _p(kn), radius, gamma, delta, mu,
                                        _p(f32), _p(out))
     if n < 0:
         raise ValueError("oracle refine failed")

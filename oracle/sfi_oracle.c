@@ -294,17 +294,28 @@ float sfi_oracle_log2f(float x)
  *       geometric (log-linear) mixture of the reverse-KL objective, scored in the log domain:
  *       s = fl32(fl32(fl32(1 - lambda) log2 f) + fl32(fl32(lambda) log2 fl32(c2 rt / lambda)))
  *       (lambda = 0: s = log2 f; the log score ranks like the geometric mixture);
- *   Soft-NMS within a head: a candidate strictly below the largest score of its candidate
- *       neighbours at distance 1..radius is scaled by gamma: s' = fl32(gamma s);
+ *   Soft-NMS within a head ("neighbouring tokens with similar scores are suppressed"): a
+ *       candidate is scaled by gamma, s' = fl32(gamma s), when a candidate neighbour at
+ *       distance 1..radius scores strictly higher and, with a similarity limit delta > 0,
+ *       at most delta higher: fl32(s_i - s_j) <= delta (delta = 0: no limit);
  *   cross-head exclusivity: with T_j = s'_0j + ... + s'_(H-1)j summed in head order,
  *       s''_hj = fl32(s'_hj - fl32(mu' fl32(T_j - s'_hj))),  mu' = fl32(mu / (H - 1)).
  * f: fp32 [H][L] evidence of the H kv heads of one (layer, sequence); knorm: fp32 [H][L]
  * key norms or NULL; out: fp32 [H][n_C] refined scores of candidates S .. L-W-1.
  * Returns n_C.
  */
+/* Soft-NMS: does the neighbour's score w suppress the score v? Strictly higher, and when
+ * delta > 0 similar as well (the difference, rounded to fp32, at most delta). */
+static int nms_neighbour_suppresses(float w, float v, float delta)
+{
+    if (!(w > v))
+        return 0;
+    return delta <= 0.0f || w - v <= delta;
+}
+
 int sfi_oracle_refine_scores(int H, int L, int S, int W, int tau, double lambda, int geometric,
-                             float nu, const float *knorm, int radius, float gamma, float mu,
-                             const float *f, float *out)
+                             float nu, const float *knorm, int radius, float gamma, float delta,
+                             float mu, const float *f, float *out)
 {
     const int n = sfi_oracle_num_candidates(L, S, W);
     if (n == 0)
@@ -348,18 +359,20 @@ int sfi_oracle_refine_scores(int H, int L, int S, int W, int tau, double lambda,
             s[(size_t)h * n + i] = v;
         }
     /* Soft-NMS within each head */
-    for (int h = 0; h < H; ++h)
+    for (int h = 0; h < H; ++h) {
+        const float *sh = s + (size_t)h * n;
         for (int i = 0; i < n; ++i) {
-            const float v = s[(size_t)h * n + i];
-            float best = -INFINITY;
+            const float v = sh[i];
+            int suppressed = 0;
             for (int k = 1; k <= radius; ++k) {
-                if (i - k >= 0 && s[(size_t)h * n + i - k] > best)
-                    best = s[(size_t)h * n + i - k];
-                if (i + k < n && s[(size_t)h * n + i + k] > best)
-                    best = s[(size_t)h * n + i + k];
+                if (i - k >= 0 && nms_neighbour_suppresses(sh[i - k], v, delta))
+                    suppressed = 1;
+                if (i + k < n && nms_neighbour_suppresses(sh[i + k], v, delta))
+                    suppressed = 1;
             }
-            out[(size_t)h * n + i] = (radius > 0 && v < best) ? gamma * v : v;
+            out[(size_t)h * n + i] = suppressed ? gamma * v : v;
         }
+    }
     /* cross-head exclusivity */
     if (mu != 0.0f && H > 1) {
         const float mu1 = (float)((double)mu / (double)(H - 1));

@@ -51,7 +51,7 @@ class SfiBudget(C.Structure):
     _fields_ = [("n_sink", C.c_int32), ("n_window", C.c_int32), ("n_select", C.c_int32),
                 ("prior_tau", C.c_int32), ("lambda_", C.c_double), ("nms_radius", C.c_int32),
                 ("nms_gamma", C.c_float), ("excl_mu", C.c_float), ("norm_nu", C.c_float),
-                ("geometric", C.c_int32)]
+                ("geometric", C.c_int32), ("nms_delta", C.c_float)]
 
 
 class SfiSparseMem(C.Structure):

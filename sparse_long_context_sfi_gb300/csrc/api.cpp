@@ -546,7 +546,7 @@ sfi_status sfi_refine_scores(const sfi_kv_cache *kv, const float *scores_f,
     if ((st = check_budget(budget)) != SFI_OK)
         return st;
     if (!scores_f || !refined || budget->nms_radius < 0 ||
-        !(budget->nms_gamma >= 0.f && budget->nms_gamma <= 1.f) ||
+        !(budget->nms_gamma >= 0.f && budget->nms_gamma <= 1.f) || !(budget->nms_delta >= 0.f) ||
         !(budget->excl_mu >= 0.f && budget->excl_mu <= 1.f) || !(budget->norm_nu >= 0.f) ||
         (budget->norm_nu > 0.f && !key_norms))
         return SFI_ERR_INVALID_ARG;
@@ -570,6 +570,7 @@ sfi_status sfi_refine_scores(const sfi_kv_cache *kv, const float *scores_f,
     p.norm_nu = budget->norm_nu;
     p.nms_radius = budget->nms_radius;
     p.nms_gamma = budget->nms_gamma;
+    p.nms_delta = budget->nms_delta;
     p.excl_mu = budget->excl_mu;
     const int max_cand = kv->max_len - budget->n_window - budget->n_sink;
     return launch_status(

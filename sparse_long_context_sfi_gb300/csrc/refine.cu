@@ -65,6 +65,14 @@ struct Fused {
     }
 };
 
+// Soft-NMS: a neighbour's score w suppresses v when it is strictly higher and, with a
+// similarity limit delta > 0, close to it: fl32(w - v) <= delta. NaN on either side never
+// suppresses.
+__device__ __forceinline__ bool nms_suppresses(float w, float v, float delta)
+{
+    return w > v && (delta <= 0.f || __fadd_rn(w, -v) <= delta);
+}
+
 __global__ void __launch_bounds__(256) refine_kernel(const RefineParams p)
 {
     pdl_trigger();
@@ -104,14 +112,14 @@ __global__ void __launch_bounds__(256) refine_kernel(const RefineParams p)
     float sp[kMaxHeads];
     for (int h = 0; h < H; ++h) {
         const float v = fz.at(u0 + h, i);
-        float best = -INFINITY;
+        bool dominated = false;
         for (int k = 1; k <= p.nms_radius; ++k) {
             if (i - k >= 0)
-                best = fmaxf(best, fz.at(u0 + h, i - k));
+                dominated |= nms_suppresses(fz.at(u0 + h, i - k), v, p.nms_delta);
             if (i + k < nC)
-                best = fmaxf(best, fz.at(u0 + h, i + k));
+                dominated |= nms_suppresses(fz.at(u0 + h, i + k), v, p.nms_delta);
         }
-        sp[h] = (p.nms_radius > 0 && v < best) ? __fmul_rn(p.nms_gamma, v) : v;
+        sp[h] = dominated ? __fmul_rn(p.nms_gamma, v) : v;
     }
     if (p.excl_mu != 0.f && H > 1) {
         const float mu1 = sh_c[4];

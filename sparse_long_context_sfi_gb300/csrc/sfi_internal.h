@@ -95,6 +95,7 @@ struct RefineParams {
     float norm_nu;
     int nms_radius;
     float nms_gamma;
+    float nms_delta;
     float excl_mu;
 };
 

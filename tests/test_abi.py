@@ -69,6 +69,11 @@ def test_argument_errors_return_before_any_launch(lib):
     bad.prior_tau, bad.lambda_ = 64, 1.5
     assert lib.sfi_compact(C.byref(kv), C.byref(bad), C.byref(mem), None, None) == \
         sfi.SFI_ERR_INVALID_ARG  # lambda outside [0, 1]
+    bad.lambda_, bad.nms_radius, bad.nms_gamma = 0.1, 1, 0.5
+    for delta in (-1e-3, float("nan")):  # Soft-NMS similarity limit negative or NaN
+        bad.nms_delta = delta
+        assert lib.sfi_refine_scores(C.byref(kv), dummy, None, C.byref(bad), dummy, None,
+                                     None) == sfi.SFI_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("t_max", [0, 1, 5, 64])
@@ -82,7 +87,8 @@ def test_native_scheduler_matches_oracle(lib, t_max):
 def test_decode_plan_layout_matches_header(lib):
     """ctypes structs mirror the C layouts (field offsets of the 64-bit ABI)."""
     assert C.sizeof(sfi.SfiKvCache) == 10 * 4 + 5 * 8
-    assert C.sizeof(sfi.SfiBudget) == 4 * 4 + 8 + 5 * 4 + 4  # padded to 8
+    assert C.sizeof(sfi.SfiBudget) == 4 * 4 + 8 + 6 * 4
+    assert sfi.SfiBudget.lambda_.offset == 16 and sfi.SfiBudget.nms_delta.offset == 44
     assert C.sizeof(sfi.SfiSparseMem) == 5 * 8
     assert sfi.SfiDecodePlan.masks.offset == 64 and sfi.SfiDecodePlan.events.offset == 80
     assert sfi.SfiDecodePlan.side_stream.offset == 88 and sfi.SfiDecodePlan.join_event.offset == 104

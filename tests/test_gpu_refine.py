@@ -21,6 +21,8 @@ OPTIONS = [
     dict(norm_nu=16.0),
     dict(geometric=1),
     dict(geometric=1, nms_radius=1, nms_gamma=0.25, excl_mu=0.3, norm_nu=14.0),
+    dict(nms_radius=3, nms_gamma=0.5, nms_delta=2e-4),
+    dict(geometric=1, nms_radius=2, nms_gamma=0.25, nms_delta=1.0, excl_mu=0.3),
 ]
 
 
@@ -85,7 +87,8 @@ def test_refined_scores_and_selection_bit_exact(slow_state, opt):
                                        geometric=bool(opt.get("geometric", 0)),
                                        nu=opt.get("norm_nu", 0.0), knorm=kn[u0:u0 + H, :L],
                                        radius=opt.get("nms_radius", 0),
-                                       gamma=opt.get("nms_gamma", 1.0), mu=opt.get("excl_mu", 0.0))
+                                       gamma=opt.get("nms_gamma", 1.0), mu=opt.get("excl_mu", 0.0),
+                                       delta=opt.get("nms_delta", 0.0))
             n = L - W - S
             np.testing.assert_array_equal(r_gpu[u0:u0 + H, S:S + n].view(np.uint32),
                                           ref.view(np.uint32))

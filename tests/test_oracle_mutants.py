@@ -32,7 +32,10 @@ MUTANTS = {
     "first_step_not_slow": ("int s = (t == 0) || mask[t - 1]", "int s = (t < 0) || mask[t - 1]"),
     "token_trigger_off_by_one": ("if (tokens[t - 1] == trigger_ids[i])",
                                  "if (tokens[t] == trigger_ids[i])"),
-    "nms_non_strict": ("(radius > 0 && v < best)", "(radius > 0 && v <= best)"),
+    "nms_non_strict": ("if (!(w > v))", "if (!(w >= v))"),
+    "nms_similarity_ignored": ("return delta <= 0.0f || w - v <= delta;", "return 1;"),
+    "nms_similarity_reversed": ("return delta <= 0.0f || w - v <= delta;",
+                                "return delta <= 0.0f || w - v >= delta;"),
     "exclusivity_wrong_sign": ("s[(size_t)h * n + i] = v - pen;", "s[(size_t)h * n + i] = v + pen;"),
     "geometric_weights_swapped": ("const float a = c1 * sfi_oracle_log2f(fj);",
                                   "const float a = lam_f * sfi_oracle_log2f(fj);"),

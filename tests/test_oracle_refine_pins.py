@@ -51,6 +51,49 @@ def test_soft_nms_hand_example():
                                   np.float32([0.3, 0.3, 0.05]))
 
 
+def test_soft_nms_similarity_hand_example():
+    # the page suppresses neighbours "with similar scores": with delta = 0.35 only a
+    # neighbour at most 0.35 higher suppresses (same scores as the example above)
+    s = np.array([[0.1, 0.5, 0.2, 0.2, 0.9, 0.05, 0.0]], np.float32)
+    r = oracle.refine_scores(7, 0, 1, 1, 0.0, s, radius=1, gamma=0.5, delta=0.35)[0]
+    # 0.1: 0.5 is 0.4 higher -> kept; 0.5 local max; 0.2: 0.5 is 0.3 higher -> halved;
+    # 0.2: 0.9 is 0.7 higher, the other 0.2 not higher -> kept; 0.9 kept; 0.05: 0.85 -> kept
+    np.testing.assert_array_equal(r, np.float32([0.1, 0.5, 0.1, 0.2, 0.9, 0.05]))
+    # radius 2: 0.1 now sees 0.2 (0.1 higher) -> halved; the second 0.2 sees 0.5 (0.3
+    # higher) -> halved; 0.05 sees 0.2 (0.15 higher) -> halved
+    r2 = oracle.refine_scores(7, 0, 1, 1, 0.0, s, radius=2, gamma=0.5, delta=0.35)[0]
+    np.testing.assert_array_equal(r2, np.float32([0.05, 0.5, 0.1, 0.1, 0.9, 0.025]))
+    # a limit above every gap is the unlimited rule; one below every gap suppresses nobody
+    for radius in (1, 2, 3):
+        np.testing.assert_array_equal(
+            oracle.refine_scores(7, 0, 1, 1, 0.0, s, radius=radius, gamma=0.5, delta=10.0),
+            oracle.refine_scores(7, 0, 1, 1, 0.0, s, radius=radius, gamma=0.5))
+        np.testing.assert_array_equal(
+            oracle.refine_scores(7, 0, 1, 1, 0.0, s, radius=radius, gamma=0.5, delta=1e-3),
+            s[:, :6])
+
+
+def test_soft_nms_similarity_brute_force():
+    # every candidate against the definition, evaluated here position by position: scaled
+    # iff a neighbour within the radius is strictly higher by at most delta (fp32 difference)
+    f = evidence4()
+    n = L - W - S
+    for radius, delta in ((1, 0.0), (3, 2e-4), (2, 5e-5)):
+        plain = oracle.refine_scores(L, S, W, TAU, 0.1, f)
+        r = oracle.refine_scores(L, S, W, TAU, 0.1, f, radius=radius, gamma=0.25, delta=delta)
+        n_scaled = 0
+        for h in range(4):
+            for i in range(n):
+                v = plain[h, i]
+                nb = [plain[h, j] for j in range(max(0, i - radius), min(n, i + radius + 1))
+                      if j != i]
+                hit = any(w > v and (delta == 0.0 or np.float32(w - v) <= np.float32(delta))
+                          for w in nb)
+                n_scaled += hit
+                assert r[h, i] == (np.float32(0.25) * v if hit else v)
+        assert 0 < n_scaled < 4 * n
+
+
 def test_exclusivity_identical_heads_keep_each_ranking():
     f = evidence4()
     same = np.repeat(f[:1], 4, axis=0)
