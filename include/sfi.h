@@ -97,7 +97,7 @@ typedef struct sfi_budget {
     double lambda;
     /* Selector refinements, read by sfi_refine_scores only (each is off when zero):     */
     int32_t nms_radius;  /* Soft-NMS: neighbours at distance 1..nms_radius in a head     */
-    float nms_gamma;     /* Soft-NMS: factor for a candidate below its neighbourhood max */
+    float nms_gamma;     /* Soft-NMS: factor for a candidate that a neighbour suppresses */
     float excl_mu;       /* cross-head exclusivity strength in [0, 1]                    */
     float norm_nu;       /* key-norm prior term: prior scaled by min(1, norm_nu/||k||)   */
     int32_t geometric;   /* 1: geometric (log-linear) mixture instead of arithmetic      */
