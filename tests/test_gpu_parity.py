@@ -580,3 +580,65 @@ def test_bad_page_entry_sets_device_error_and_skips():
     bits = sfi_read_error(st.kv)
     assert bits & SFI_DEVERR_PAGE_RANGE
     assert np.isfinite(out.cpu().numpy()).all()
+
+
+# ------------------------------------------------------------------------------- empty input
+
+@pytest.mark.parametrize("shape", [dict(ctx=1500, batch=2), dict(ctx=1300, batch=3, n_layers=5)],
+                         ids=["clustered_16_units", "tile_ranges_120_units"])
+def test_no_active_sequence_leaves_everything_untouched(shape):
+    """Every entry point called with an activity mask that selects no sequence is a no-op:
+    caches, lengths, packed memory, selections, evidence and outputs keep their contents and
+    no error is raised; the following fast step then matches one on a state that never saw
+    the empty calls."""
+    import sparse_long_context_sfi_gb300 as sfi
+    wl = small("llama8b_ctx32k_b4", steps=3, **shape)
+    cfg = wl.cfg
+    shp = (cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.head_dim)
+    states = []
+    for _ in range(2):
+        st = sdev.make_state(wl)
+        ins = sdev.DeviceInputs(wl, 2, st.k.device)
+        st.step(ins.q[0], ins.k_new[0], ins.v_new[0], np.ones(cfg.batch, bool),
+                torch.zeros(shp, device=st.k.device))
+        states.append((st, ins))
+    torch.cuda.synchronize()
+    st, ins = states[0]
+    dev = st.k.device
+    kv = st.kv
+    none = torch.zeros(cfg.batch, dtype=torch.uint8, device=dev)
+    kept = dict(k=st.k, v=st.v, seq_len=st.seq_len, kc=st.kc, vc=st.vc, sel_idx=st.sel_idx,
+                sel_cnt=st.sel_cnt, rows=st.rows, scores=st.scores)
+    before = {n: t.clone() for n, t in kept.items()}
+    out = torch.full(shp, float("nan"), device=dev)
+    norms = torch.full_like(st.scores, float("nan"))
+    refined = torch.full_like(st.scores, float("nan"))
+    q, k1, v1 = ins.q[1], ins.k_new[1], ins.v_new[1]
+    kv.max_len = int(st.len0.max()) + 1
+    sfi.sfi_append_kv(kv, k1, v1, active=none)
+    sfi.sfi_fast_decode_step(kv, st.mem, st.budget, k1, v1, q, out, True, st.ws, st.ws_bytes,
+                             active=none)
+    sfi.sfi_dense_decode_attn(kv, q, out, True, st.scores, st.ws, st.ws_bytes, active=none)
+    sfi.sfi_select(kv, st.scores, st.budget, st.mem, active=none)
+    sfi.sfi_compact(kv, st.budget, st.mem, active=none)
+    sfi.sfi_sparse_decode_attn(kv, st.mem, st.budget, q, out, True, st.ws, st.ws_bytes,
+                               active=none)
+    sfi.sfi_sparse_decode_attn_static(kv, st.mem, st.budget, q, out, True, active=none)
+    sfi.sfi_key_norms(kv, norms, active=none)
+    sfi.sfi_refine_scores(kv, st.scores, norms, st.budget, refined, active=none)
+    torch.cuda.synchronize()
+    assert sfi.sfi_read_error(kv) == 0
+    for n, t in kept.items():
+        assert torch.equal(t, before[n]), f"{n} changed"
+    assert torch.isnan(out).all() and torch.isnan(norms).all() and torch.isnan(refined).all()
+    # the next (fast) step is unaffected
+    outs = []
+    for s, i in states:
+        o = torch.zeros(shp, device=dev)
+        s.step(i.q[1], i.k_new[1], i.v_new[1], np.zeros(cfg.batch, bool), o)
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert sfi.sfi_read_error(kv) == 0
+    assert torch.equal(st.seq_len, states[1][0].seq_len)
+    ok, err = close(outs[0].cpu().numpy(), outs[1].cpu().numpy())
+    assert ok, f"fast step after the empty calls differs by {err}"
