@@ -76,6 +76,18 @@ def test_argument_errors_return_before_any_launch(lib):
                                      None) == sfi.SFI_ERR_INVALID_ARG
 
 
+def test_static_fast_step_rejects_units_beyond_its_scratch(lib):
+    """The allocation-free fast step has scratch for 16384 units; more give SFI_ERR_CAPACITY
+    before any device call (the pointers are never dereferenced)."""
+    dummy = 1 << 20
+    bud = sfi.SfiBudget(n_sink=4, n_window=64, n_select=256, prior_tau=64, lambda_=0.1)
+    mem = sfi.SfiSparseMem(kc=dummy, vc=dummy, sel_idx=dummy, sel_cnt=dummy, rows=dummy)
+    kv = sfi.SfiKvCache(n_layers=65, batch=32, n_q_heads=32, n_kv_heads=8, head_dim=128,
+                        capacity=1024, max_len=4, k=dummy, v=dummy, seq_len=dummy, err=dummy)
+    assert lib.sfi_sparse_decode_attn_static(C.byref(kv), C.byref(mem), C.byref(bud), dummy,
+                                             dummy, 1, None, None) == sfi.SFI_ERR_CAPACITY
+
+
 @pytest.mark.parametrize("t_max", [0, 1, 5, 64])
 def test_native_scheduler_matches_oracle(lib, t_max):
     rng = np.random.default_rng(t_max)
