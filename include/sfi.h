@@ -199,7 +199,7 @@ sfi_status sfi_key_norms(const sfi_kv_cache *kv, float *norms, const uint8_t *ac
  *   s_hj  = arithmetic: fl32(fl32(c1 f_hj) + fl32(c2 rt_hj))  (c1, c2 as in sfi_select), or
  *           geometric:  fl32(c1 log2 f_hj) + fl32(lambda log2 fl32(fl32(c2 rt_hj) / lambda))
  *           in fp32 with the library's own log2 (log-domain score of the geometric mixture);
- *   Soft-NMS (neighbouring tokens with similar scores are suppressed): s'_hj =
+ *   Soft-NMS (a candidate is damped by a nearby one that scores a little higher): s'_hj =
  *           fl32(nms_gamma s_hj) if some candidate i with 1 <= |i - j| <= nms_radius has
  *           s_hi > s_hj and, when nms_delta > 0, fl32(s_hi - s_hj) <= nms_delta; else s_hj;
  *   exclusivity: s''_hj = fl32(s'_hj - fl32(mu' fl32(T_j - s'_hj))), T_j = sum over heads of

@@ -294,7 +294,7 @@ float sfi_oracle_log2f(float x)
  *       geometric (log-linear) mixture of the reverse-KL objective, scored in the log domain:
  *       s = fl32(fl32(fl32(1 - lambda) log2 f) + fl32(fl32(lambda) log2 fl32(c2 rt / lambda)))
  *       (lambda = 0: s = log2 f; the log score ranks like the geometric mixture);
- *   Soft-NMS within a head ("neighbouring tokens with similar scores are suppressed"): a
+ *   Soft-NMS within a head (nearby candidates whose scores are close damp one another): a
  *       candidate is scaled by gamma, s' = fl32(gamma s), when a candidate neighbour at
  *       distance 1..radius scores strictly higher and, with a similarity limit delta > 0,
  *       at most delta higher: fl32(s_i - s_j) <= delta (delta = 0: no limit);

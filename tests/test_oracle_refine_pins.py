@@ -52,8 +52,8 @@ def test_soft_nms_hand_example():
 
 
 def test_soft_nms_similarity_hand_example():
-    # the page suppresses neighbours "with similar scores": with delta = 0.35 only a
-    # neighbour at most 0.35 higher suppresses (same scores as the example above)
+    # the damping acts only between close scores: with delta = 0.35 only a neighbour at
+    # most 0.35 higher suppresses (same scores as the example above)
     s = np.array([[0.1, 0.5, 0.2, 0.2, 0.9, 0.05, 0.0]], np.float32)
     r = oracle.refine_scores(7, 0, 1, 1, 0.0, s, radius=1, gamma=0.5, delta=0.35)[0]
     # 0.1: 0.5 is 0.4 higher -> kept; 0.5 local max; 0.2: 0.5 is 0.3 higher -> halved;
