@@ -287,7 +287,7 @@ float sfi_oracle_log2f(float x)
 
 /*
  * Selector refinements ([Sum 2B]): the pages name them without formulas; the readings:
- *   prior with a key-norm term ("avoid tokens with extremely high key norms"):
+ *   prior with a key-norm term (it steers the selection away from keys of very large norm):
  *       rt_j = fl32(min(1, d_j/tau)) * g_j,  g_j = min(1, fl32(nu / ||k_j||))  (nu = 0: g = 1),
  *       still divided by the closed-form Z of the plain ramp (the term only removes mass);
  *   fusion: arithmetic s = fl32(fl32(c1 f) + fl32(c2 rt)) as sfi_oracle_fused_scores, or the
